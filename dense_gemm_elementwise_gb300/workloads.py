@@ -1,0 +1,351 @@
+"""Workload table and seeded synthetic input generators.
+
+This module holds data only: problem shapes, element types, the epilogue of
+each workload written as a DAG (plain tuples), scalar values, and the seeded
+generators that draw the operands on the host.  It contains none of the
+GEMM or epilogue arithmetic; both the CUDA path (through the C-ABI binding)
+and the CPU oracle consume what it produces.
+
+DAG tuples are ``(op, a, b, slot)`` with ``op`` one of ``accum, load, scalar,
+broadcast, mul, add, relu, store``; ``a``/``b`` index earlier nodes; ``slot``
+selects the aux tensor (load, broadcast), the scalar (scalar) or the output
+(store).  Output slot 0 is D.
+"""
+from dataclasses import dataclass, field
+from typing import List, Optional, Tuple
+
+import numpy as np
+import torch
+
+TORCH_DTYPE = {"f16": torch.float16, "bf16": torch.bfloat16, "f32": torch.float32}
+ESIZE = {"f16": 2, "bf16": 2, "f32": 4}
+
+
+class Dag:
+    """Tiny builder for epilogue DAGs in single assignment order."""
+
+    def __init__(self):
+        self.nodes: List[Tuple[str, int, int, int]] = []
+
+    def _add(self, op, a=0, b=0, slot=0):
+        self.nodes.append((op, a, b, slot))
+        return len(self.nodes) - 1
+
+    def accum(self):
+        return self._add("accum")
+
+    def load(self, slot):
+        return self._add("load", slot=slot)
+
+    def broadcast(self, slot):
+        return self._add("broadcast", slot=slot)
+
+    def scalar(self, slot):
+        return self._add("scalar", slot=slot)
+
+    def mul(self, a, b):
+        return self._add("mul", a, b)
+
+    def add(self, a, b):
+        return self._add("add", a, b)
+
+    def relu(self, a):
+        return self._add("relu", a)
+
+    def store(self, a, slot):
+        return self._add("store", a, 0, slot)
+
+
+@dataclass
+class Workload:
+    name: str
+    L: int
+    M: int
+    N: int
+    K: int
+    ab: str                                   # element type of A and B
+    aux: List[Tuple[str, str, str]]           # (name, "tensor" (L,M,N) | "row" (N,), dtype)
+    scalars: List[Tuple[str, float]]          # (name, value)
+    outs: List[Tuple[str, str]]               # (name, dtype); outs[0] is D
+    dag: List[Tuple[str, int, int, int]]
+    dist: str                                 # "randint", "ceil_uniform", "normal"
+    seed: int
+    exact: bool                               # integer-valued: results must be bit-exact
+    sample_rows: Optional[int] = None         # oracle rows per batch at full size (None: all)
+    cite: str = ""
+    notes: str = field(default="")
+
+    def flops(self) -> float:
+        return 2.0 * self.L * self.M * self.N * self.K
+
+    def alg_bytes(self) -> int:
+        """Read A, B and each aux once; write each output once."""
+        L, M, N, K = self.L, self.M, self.N, self.K
+        b = (L * M * K + L * K * N) * ESIZE[self.ab]
+        for _, kind, dt in self.aux:
+            b += (L * M * N if kind == "tensor" else N) * ESIZE[dt]
+        for _, dt in self.outs:
+            b += L * M * N * ESIZE[dt]
+        return b
+
+
+# ---------------------------------------------------------------- DAGs ----
+
+def dag_my_epilogue():
+    """Aux = alpha*accum + beta*C ; D = extra_scalar*Aux ; returns D, Aux.
+    ("CUTLASS Operator API: Custom epilogue fusions for GEMMs", cell [2])."""
+    g = Dag()
+    acc = g.accum()
+    alpha = g.scalar(0)
+    t0 = g.mul(alpha, acc)
+    c = g.load(0)
+    beta = g.scalar(1)
+    t1 = g.mul(beta, c)
+    aux = g.add(t0, t1)
+    s = g.scalar(2)
+    d = g.mul(s, aux)
+    g.store(d, 0)
+    g.store(aux, 1)
+    return g.nodes
+
+
+def dag_relu_linear():
+    """D = relu(alpha*accum + beta*C) ("Custom Epilogue Example",
+    "Activation Functions"; the legacy epilogue notebook's fused ReLU)."""
+    g = Dag()
+    acc = g.accum()
+    t0 = g.mul(acc, g.scalar(0))
+    t1 = g.mul(g.load(0), g.scalar(1))
+    d = g.relu(g.add(t0, t1))
+    g.store(d, 0)
+    return g.nodes
+
+
+def dag_alpha_beta_x():
+    """Y = accum ; D = accum*alpha + C*beta + X*x_factor ("Custom Epilogue
+    Example", "Basic Example: Alpha-Beta Scaling").  Outputs: D (slot 0), Y."""
+    g = Dag()
+    acc = g.accum()
+    t0 = g.mul(acc, g.scalar(0))
+    t1 = g.mul(g.load(0), g.scalar(1))
+    t2 = g.add(t0, t1)
+    t3 = g.mul(g.load(1), g.scalar(2))
+    d = g.add(t2, t3)
+    g.store(d, 0)
+    g.store(acc, 1)
+    return g.nodes
+
+
+def dag_bias_relu_square():
+    """D = relu(alpha*accum + beta*C + bias) ; E = D*D (row-broadcast bias,
+    "Row and column broadcasts"; squared second output, "Multiple Outputs")."""
+    g = Dag()
+    acc = g.accum()
+    t0 = g.mul(g.scalar(0), acc)
+    t1 = g.mul(g.scalar(1), g.load(0))
+    t2 = g.add(t0, t1)
+    t3 = g.add(t2, g.broadcast(1))
+    d = g.relu(t3)
+    e = g.mul(d, d)
+    g.store(d, 0)
+    g.store(e, 1)
+    return g.nodes
+
+
+def dag_relu_aux_store():
+    """F = accum*alpha + C*2.0 ; D = relu(F) ; returns D, F (cell [6]); the
+    constant 2.0 is passed as scalar slot 1."""
+    g = Dag()
+    acc = g.accum()
+    f = g.add(g.mul(acc, g.scalar(0)), g.mul(g.load(0), g.scalar(1)))
+    d = g.relu(f)
+    g.store(d, 0)
+    g.store(f, 1)
+    return g.nodes
+
+
+def dag_relu_scale_return_acc():
+    """F = relu(accum*alpha + C*beta) ; D = F*scale ; returns D, F, accum
+    (cell [7]; accum is stored as fp32)."""
+    g = Dag()
+    acc = g.accum()
+    f = g.relu(g.add(g.mul(acc, g.scalar(0)), g.mul(g.load(0), g.scalar(1))))
+    d = g.mul(f, g.scalar(2))
+    g.store(d, 0)
+    g.store(f, 1)
+    g.store(acc, 2)
+    return g.nodes
+
+
+def dag_row_bias():
+    """D = accum*alpha + row_bias (cell [9], row part)."""
+    g = Dag()
+    acc = g.accum()
+    d = g.add(g.mul(acc, g.scalar(0)), g.broadcast(0))
+    g.store(d, 0)
+    return g.nodes
+
+
+def dag_add_square():
+    """d = accum + c ; d_squared = d*d ("Multiple Outputs", first two)."""
+    g = Dag()
+    d = g.add(g.accum(), g.load(0))
+    g.store(d, 0)
+    g.store(g.mul(d, d), 1)
+    return g.nodes
+
+
+def dag_identity():
+    """D = accum (a plain GEMM stored through the epilogue)."""
+    g = Dag()
+    g.store(g.accum(), 0)
+    return g.nodes
+
+
+# ----------------------------------------------------------- workloads ----
+
+def my_epilogue(L, M, N, K, seed=2025, name=None):
+    return Workload(
+        name=name or "my_epilogue_%dx%dx%dx%d" % (L, M, N, K), L=L, M=M, N=N, K=K, ab="f16",
+        aux=[("C", "tensor", "f16")],
+        scalars=[("alpha", 1.0), ("beta", 2.0), ("extra_scalar", 0.5)],
+        outs=[("D", "f16"), ("Aux", "f16")], dag=dag_my_epilogue(), dist="randint",
+        seed=seed, exact=True,
+        cite="CUTLASS Operator API: Custom epilogue fusions for GEMMs, cells [2]-[5]")
+
+
+CONFIGS = [
+    my_epilogue(1, 128, 128, 128, name="cfg1_my_epilogue_128"),
+    my_epilogue(1, 1024, 1024, 1024, name="cfg2_my_epilogue_1024"),
+    Workload(
+        name="cfg3_relu_2400x3232x4096", L=1, M=2400, N=3232, K=4096, ab="f16",
+        aux=[("C", "tensor", "f16")], scalars=[("alpha", 1.0), ("beta", 2.0)],
+        outs=[("D", "f16")], dag=dag_relu_linear(), dist="ceil_uniform", seed=1234,
+        exact=True,
+        cite="CUTLASS Python examples walkthrough: basic GEMM notebook (2400x3232x4096, "
+             "beta=2) and epilogue notebook (fused ReLU)"),
+    Workload(
+        name="cfg4_alpha_beta_x_8192", L=1, M=8192, N=8192, K=8192, ab="f16",
+        aux=[("C", "tensor", "f16"), ("X", "tensor", "f16")],
+        scalars=[("alpha", 2.0), ("beta", 1.0), ("x_factor", 3.0)],
+        outs=[("D", "f16"), ("Y", "f16")], dag=dag_alpha_beta_x(), dist="normal", seed=2026,
+        exact=False, sample_rows=64,
+        cite="Custom Epilogue Example: Basic Example: Alpha-Beta Scaling; Running the Example"),
+    Workload(
+        name="cfg5_bias_relu_square_L8", L=8, M=4096, N=4096, K=2048, ab="bf16",
+        aux=[("C", "tensor", "bf16"), ("bias", "row", "f32")],
+        scalars=[("alpha", 0.5), ("beta", 1.0)],
+        outs=[("D", "bf16"), ("E", "bf16")], dag=dag_bias_relu_square(), dist="normal",
+        seed=2027, exact=False, sample_rows=64,
+        cite="Custom Epilogue Fusions: Row and column broadcasts; Custom Epilogue Example: "
+             "Activation Functions, Multiple Outputs"),
+]
+
+BY_NAME = {w.name: w for w in CONFIGS}
+
+# Tolerance for the non-integer workloads: |gpu - ref| <= ATOL + RTOL*|ref|,
+# ref being the oracle's value rounded to the output type.
+ATOL = 1e-2
+RTOL = 1e-2
+
+
+def page_examples(L=1, M=256, N=256, K=256):
+    """Further epilogues printed on the pages, at a small size, integer inputs."""
+    return [
+        Workload(name="relu_aux_store", L=L, M=M, N=N, K=K, ab="f16",
+                 aux=[("C", "tensor", "f16")], scalars=[("alpha", 3.0), ("two", 2.0)],
+                 outs=[("D", "f16"), ("F", "f16")], dag=dag_relu_aux_store(), dist="randint",
+                 seed=2025, exact=True, cite="Custom epilogue fusions for GEMMs, cell [6]"),
+        Workload(name="relu_scale_return_acc", L=L, M=M, N=N, K=K, ab="f16",
+                 aux=[("C", "tensor", "f16")],
+                 scalars=[("alpha", 1.0), ("beta", 2.0), ("scale", 0.5)],
+                 outs=[("D", "f16"), ("F", "f16"), ("accum", "f32")],
+                 dag=dag_relu_scale_return_acc(), dist="randint", seed=2025, exact=True,
+                 cite="Custom epilogue fusions for GEMMs, cell [7]"),
+        Workload(name="string_epilogue_beta_half", L=L, M=M, N=N, K=K, ab="f16",
+                 aux=[("C", "tensor", "f16")], scalars=[("alpha", 1.0), ("beta", 0.5)],
+                 outs=[("D", "f16"), ("F", "f16")], dag=dag_relu_aux_store(), dist="randint",
+                 seed=2025, exact=True, cite="Custom epilogue fusions for GEMMs, cell [8]"),
+        Workload(name="row_bias_f16", L=L, M=M, N=N, K=K, ab="f16",
+                 aux=[("row_bias", "row", "f16")], scalars=[("alpha", 1.0)],
+                 outs=[("D", "f16")], dag=dag_row_bias(), dist="randint", seed=2025,
+                 exact=True, cite="Custom epilogue fusions for GEMMs, cell [9] (row part)"),
+        Workload(name="add_square_bf16", L=L, M=M, N=N, K=K, ab="bf16",
+                 aux=[("c", "tensor", "bf16")], scalars=[],
+                 outs=[("d", "bf16"), ("d_squared", "bf16")], dag=dag_add_square(),
+                 dist="randint", seed=2025, exact=True,
+                 cite="Custom Epilogue Example: Multiple Outputs"),
+        Workload(name="identity_f32_out", L=L, M=M, N=N, K=K, ab="f16", aux=[], scalars=[],
+                 outs=[("D", "f32")], dag=dag_identity(), dist="ceil_uniform", seed=1234,
+                 exact=True, cite="Python examples walkthrough: basic GEMM (f32 accumulate)"),
+    ]
+
+
+# ---------------------------------------------------------- generators ----
+
+def _normal(gen, shape, dtype):
+    return torch.randn(shape, generator=gen, dtype=torch.float32).to(TORCH_DTYPE[dtype])
+
+
+def make_inputs(w: Workload):
+    """Seeded host tensors ``(A, B, aux_list, scalars)`` for a workload.
+
+    * ``randint``: integers from {-2,...,2} drawn with torch's CPU generator
+      (high end exclusive, as torch.randint(-2, 3, ...) on the page);
+    * ``ceil_uniform``: numpy RandomState, ceil(uniform(-4, 4) cast to fp16),
+      the basic-GEMM notebook's recipe;
+    * ``normal``: N(0, 1) from torch's CPU generator, rounded to the type.
+    Operands are drawn in the order A, B, then the aux slots.
+    """
+    L, M, N, K = w.L, w.M, w.N, w.K
+    shapes = [(L, M, K), (L, K, N)]
+    for _, kind, _dt in w.aux:
+        shapes.append((L, M, N) if kind == "tensor" else (N,))
+    dts = [w.ab, w.ab] + [dt for _, _, dt in w.aux]
+    out = []
+    if w.dist == "randint":
+        g = torch.Generator().manual_seed(w.seed)
+        for shp, dt in zip(shapes, dts):
+            out.append(torch.randint(-2, 3, shp, generator=g, dtype=torch.float32)
+                       .to(TORCH_DTYPE[dt]))
+    elif w.dist == "ceil_uniform":
+        rs = np.random.RandomState(w.seed)
+        for shp, dt in zip(shapes, dts):
+            v = np.ceil(rs.uniform(-4.0, 4.0, size=shp).astype(np.float16))
+            out.append(torch.from_numpy(v.astype(np.float32)).to(TORCH_DTYPE[dt]))
+    elif w.dist == "normal":
+        g = torch.Generator().manual_seed(w.seed)
+        for shp, dt in zip(shapes, dts):
+            out.append(_normal(g, shp, dt))
+    else:
+        raise ValueError(w.dist)
+    A, B = out[0].contiguous(), out[1].contiguous()
+    aux = [t.contiguous() for t in out[2:]]
+    scalars = [float(v) for _, v in w.scalars]
+    return A, B, aux, scalars
+
+
+def sample_rows(w: Workload, per_batch: Optional[int] = None, seed: int = 7):
+    """Seeded sample of flattened output rows ``l*M + i`` (sorted), ``per_batch``
+    rows from every batch; always includes the first and last row of each batch
+    so the ragged last M tile is covered."""
+    per = per_batch or w.sample_rows
+    if per is None or per >= w.M:
+        return np.arange(w.L * w.M, dtype=np.int64)
+    rs = np.random.RandomState(seed)
+    rows = []
+    for l in range(w.L):
+        pick = set(rs.choice(w.M, size=per - 2, replace=False).tolist())
+        pick.update([0, w.M - 1])
+        rows.extend(sorted(l * w.M + i for i in pick))
+    return np.asarray(rows, dtype=np.int64)
+
+
+def to_codes(t: torch.Tensor) -> np.ndarray:
+    """Host tensor -> numpy array the oracle takes (uint16 codes or float32)."""
+    t = t.detach().cpu().contiguous()
+    if t.dtype in (torch.float16, torch.bfloat16):
+        return t.view(torch.int16).numpy().view(np.uint16)
+    if t.dtype == torch.float32:
+        return t.numpy()
+    raise TypeError(t.dtype)

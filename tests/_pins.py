@@ -1,0 +1,415 @@
+"""Pins for the CPU oracle: checks that fix what the oracle must compute
+without calling the oracle to produce the expected values.
+
+Every pin takes the loaded oracle library (so a deliberately mutated build can
+be run through the same pins) and raises AssertionError on a mismatch.
+
+Sources of truth used here:
+  * the IEEE 754 binary16 layout as implemented by numpy's float16, and the
+    bfloat16 layout as the upper half of numpy's float32;
+  * exact integer arithmetic (numpy int64) for integer-valued inputs, the
+    closed form the legacy basic-GEMM notebook asserts with
+    assert_array_equal (D = alpha*(A@B) + beta*C);
+  * exact rational arithmetic (fractions.Fraction) plus a table search for the
+    nearest representable value, on tiny random problems;
+  * hand-worked examples stored under tests/golden/;
+  * special cases: A = 0, B = identity.
+"""
+import json
+import os
+from fractions import Fraction
+
+import numpy as np
+
+import oracle
+from dense_gemm_elementwise_gb300 import workloads as W
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+
+
+# ------------------------------------------------------------ references --
+
+def np_decode(codes, fmt):
+    """Codes -> float64 through numpy's own IEEE types (independent of the oracle)."""
+    c = np.asarray(codes, dtype=np.uint16)
+    if fmt == "f16":
+        return c.view(np.float16).astype(np.float64)
+    if fmt == "bf16":
+        return (c.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    raise ValueError(fmt)
+
+
+def np_encode_exact(values, fmt):
+    """Codes of values that are exactly representable in ``fmt``."""
+    v = np.asarray(values, dtype=np.float64)
+    if fmt == "f16":
+        c = v.astype(np.float16)
+        assert np.array_equal(c.astype(np.float64), v), "value not representable in f16"
+        return c.view(np.uint16)
+    f = v.astype(np.float32)
+    assert np.array_equal(f.astype(np.float64), v)
+    bits = f.view(np.uint32)
+    assert np.all((bits & 0xFFFF) == 0), "value not representable in bf16"
+    return (bits >> 16).astype(np.uint16)
+
+
+_TABLES = {}
+
+
+def _table(fmt):
+    """Sorted non-negative finite values of a 16-bit format and their codes."""
+    if fmt not in _TABLES:
+        top = 0x7C00 if fmt == "f16" else 0x7F80  # first inf code
+        codes = np.arange(0, top, dtype=np.uint16)
+        vals = np_decode(codes, fmt)
+        assert np.all(np.diff(vals) > 0)
+        _TABLES[fmt] = (vals, codes, top)
+    return _TABLES[fmt]
+
+
+def nearest_even_code(x, fmt):
+    """Nearest ``fmt`` code to the exact value x (Fraction or exact float),
+    ties to the even code, overflow to inf; found by table search with exact
+    rational comparisons."""
+    x = Fraction(x)
+    vals, codes, inf_code = _table(fmt)
+    sign = 0x8000 if x < 0 else 0
+    ax = abs(x)
+    top = Fraction(float(vals[-1]))
+    half_ulp_top = (top - Fraction(float(vals[-2]))) / 2
+    if ax >= top + half_ulp_top:
+        return sign | inf_code
+    k = int(np.searchsorted(vals, float(ax)))
+    best = None
+    for idx in (k - 1, k, k + 1):
+        if 0 <= idx < len(vals):
+            d = abs(Fraction(float(vals[idx])) - ax)
+            if best is None or d < best[0] or (d == best[0] and int(codes[idx]) % 2 == 0):
+                best = (d, int(codes[idx]))
+    return sign | best[1]
+
+
+def nearest_even_f32(x):
+    """Nearest float32 to the exact value x, ties to even (exact comparisons)."""
+    x = Fraction(x)
+    g = np.float32(float(x))
+    cands = {g, np.nextafter(g, np.float32(np.inf)), np.nextafter(g, np.float32(-np.inf))}
+    best = None
+    for c in sorted(cands):
+        if not np.isfinite(c):
+            continue
+        d = abs(Fraction(float(c)) - x)
+        even = int(np.array(c, dtype=np.float32).view(np.uint32)) % 2 == 0
+        if best is None or d < best[0] or (d == best[0] and even):
+            best = (d, c)
+    return np.float32(best[1])
+
+
+def eval_dag_exact(dag, acc, aux_vals, scalars, n_out):
+    """Evaluate a DAG on exact rationals for one element.  ``aux_vals[s]`` is
+    the (already selected) exact value of aux slot s at this element."""
+    v = [None] * len(dag)
+    outs = [None] * n_out
+    for n, (op, a, b, s) in enumerate(dag):
+        if op == "accum":
+            v[n] = acc
+        elif op in ("load", "broadcast"):
+            v[n] = aux_vals[s]
+        elif op == "scalar":
+            v[n] = Fraction(scalars[s])
+        elif op == "mul":
+            v[n] = v[a] * v[b]
+        elif op == "add":
+            v[n] = v[a] + v[b]
+        elif op == "relu":
+            v[n] = v[a] if v[a] > 0 else Fraction(0)
+        elif op == "store":
+            outs[s] = v[a]
+    return outs
+
+
+def zero_norm(codes):
+    """Map -0 codes to +0 (results are compared as values, -0 == +0)."""
+    c = np.array(codes, dtype=np.uint16, copy=True)
+    c[c == 0x8000] = 0
+    return c
+
+
+def run_oracle(L_, w, A, B, aux, scalars, rows=None, threads=0, want_pre=False):
+    return oracle.gemm_epilogue(w.L, w.M, w.N, w.K, w.ab, W.to_codes(A), W.to_codes(B),
+                                [W.to_codes(a) for a in aux], [dt for _, _, dt in w.aux],
+                                scalars, w.dag, [dt for _, dt in w.outs], rows=rows,
+                                threads=threads, want_pre=want_pre, lib_handle=L_)
+
+
+def small(w, L, M, N, K, seed=None, dist=None):
+    import dataclasses
+    return dataclasses.replace(w, L=L, M=M, N=N, K=K, seed=w.seed if seed is None else seed,
+                               dist=dist or w.dist, sample_rows=None)
+
+
+# ------------------------------------------------------------------ pins --
+
+def pin_decode_exhaustive(L_):
+    codes = np.arange(65536, dtype=np.uint16)
+    for fmt, fn in (("f16", oracle.f16_to_f64), ("bf16", oracle.bf16_to_f64)):
+        got = fn(codes, L_)
+        ref = np_decode(codes, fmt)
+        nan = np.isnan(ref)
+        assert np.array_equal(np.isnan(got), nan), fmt + ": NaN codes differ"
+        assert np.array_equal(got[~nan], ref[~nan]), fmt + ": decoded values differ"
+        assert np.array_equal(np.signbit(got[~nan]), np.signbit(ref[~nan])), fmt + ": sign"
+
+
+def pin_encode_roundtrip(L_):
+    codes = np.arange(65536, dtype=np.uint16)
+    for fmt, enc in (("f16", oracle.f64_to_f16), ("bf16", oracle.f64_to_bf16)):
+        vals = np_decode(codes, fmt)
+        ok = ~np.isnan(vals)
+        got = enc(vals[ok], L_)
+        assert np.array_equal(got, codes[ok]), fmt + ": encode(decode(c)) != c"
+        nan_codes = enc(np.array([np.nan]), L_)
+        assert np.isnan(np_decode(nan_codes, fmt)).all(), fmt + ": NaN must stay NaN"
+
+
+def pin_encode_midpoints(L_):
+    """Halfway points between neighbours go to the even code; a hair above or
+    below goes to the nearer neighbour; the halfway point above the largest
+    finite value goes to inf."""
+    for fmt, enc in (("f16", oracle.f64_to_f16), ("bf16", oracle.f64_to_bf16)):
+        vals, codes, inf_code = _table(fmt)
+        lo, hi = vals[:-1], vals[1:]
+        mid = (lo + hi) / 2  # exact: neighbours differ by a power of two in a binade
+        assert np.all((mid > lo) & (mid < hi))
+        even = np.where(codes[:-1] % 2 == 0, codes[:-1], codes[1:])
+        for sgn in (1.0, -1.0):
+            sbit = np.uint16(0x8000) if sgn < 0 else np.uint16(0)
+            got = enc(sgn * mid, L_)
+            assert np.array_equal(got, even | sbit), fmt + ": ties must go to even"
+            # a hair further from zero goes to the larger magnitude, a hair
+            # closer to zero to the smaller, whatever the sign
+            up = enc(sgn * np.nextafter(mid, np.inf), L_)
+            dn = enc(sgn * np.nextafter(mid, -np.inf), L_)
+            assert np.array_equal(up, codes[1:] | sbit), fmt + ": above midpoint"
+            assert np.array_equal(dn, codes[:-1] | sbit), fmt + ": below midpoint"
+        top, prev = vals[-1], vals[-2]
+        edge = top + (top - prev) / 2
+        assert int(enc(np.array([edge]), L_)[0]) == inf_code, fmt + ": overflow midpoint"
+        assert int(enc(np.array([np.nextafter(edge, 0)]), L_)[0]) == int(codes[-1])
+        assert int(enc(np.array([-edge]), L_)[0]) == (inf_code | 0x8000)
+
+
+def pin_encode_random_vs_table(L_):
+    """Random doubles over the whole exponent range against the exact table
+    search (and, for f16, numpy's own double -> half conversion)."""
+    rs = np.random.RandomState(11)
+    x = rs.standard_normal(4000) * np.exp2(rs.uniform(-30, 18, 4000))
+    got16 = oracle.f64_to_f16(x, L_)
+    with np.errstate(over="ignore"):
+        np16 = x.astype(np.float16).view(np.uint16)
+    assert np.array_equal(zero_norm(got16), zero_norm(np16))
+    sub = x[:600]
+    ref16 = np.array([nearest_even_code(float(v), "f16") for v in sub], dtype=np.uint16)
+    assert np.array_equal(zero_norm(got16[:600]), zero_norm(ref16))
+    y = rs.standard_normal(600) * np.exp2(rs.uniform(-140, 130, 600))
+    gotb = oracle.f64_to_bf16(y, L_)
+    refb = np.array([nearest_even_code(float(v), "bf16") for v in y], dtype=np.uint16)
+    assert np.array_equal(zero_norm(gotb), zero_norm(refb))
+
+
+def _golden_cases():
+    dags = {
+        "my_epilogue_2x2x2.json": (W.dag_my_epilogue(), [("C", "tensor", "f16")],
+                                   [("D", "f16"), ("Aux", "f16")]),
+        "relu_linear_2x2x2.json": (W.dag_relu_linear(), [("C", "tensor", "f16")], [("D", "f16")]),
+        "alpha_beta_x_2x2x2.json": (W.dag_alpha_beta_x(),
+                                    [("C", "tensor", "f16"), ("X", "tensor", "f16")],
+                                    [("D", "f16"), ("Y", "f16")]),
+        "bias_relu_square_2x2x2x2.json": (W.dag_bias_relu_square(),
+                                          [("C", "tensor", "bf16"), ("bias", "row", "f32")],
+                                          [("D", "bf16"), ("E", "bf16")]),
+    }
+    for fname, (dag, aux_spec, outs) in dags.items():
+        with open(os.path.join(GOLDEN, fname)) as f:
+            yield fname, json.load(f), dag, aux_spec, outs
+
+
+def pin_golden(L_):
+    for fname, g, dag, aux_spec, outs in _golden_cases():
+        L, M, N, K, ab = g["L"], g["M"], g["N"], g["K"], g["ab"]
+        A = np_encode_exact(np.array(g["A"], dtype=np.float64).reshape(L, M, K), ab)
+        B = np_encode_exact(np.array(g["B"], dtype=np.float64).reshape(L, K, N), ab)
+        aux, aux_dt = [], []
+        for name, kind, dt in aux_spec:
+            a = np.array(g["aux"][name], dtype=np.float64)
+            aux.append(a.astype(np.float32) if dt == "f32" else np_encode_exact(a, dt))
+            aux_dt.append(dt)
+        res, _ = oracle.gemm_epilogue(L, M, N, K, ab, A, B, aux, aux_dt, g["scalars"], dag,
+                                      [dt for _, dt in outs], lib_handle=L_)
+        for (name, dt), got in zip(outs, res):
+            want = np.array(g["expected"][name], dtype=np.float64).reshape(L * M, N)
+            val = got.astype(np.float64) if dt == "f32" else np_decode(got, dt)
+            assert np.array_equal(val, want), "%s: %s = %s, hand-worked %s" % (
+                fname, name, val.tolist(), want.tolist())
+            if "expected_codes" in g and name in g["expected_codes"]:
+                wc = np.array(g["expected_codes"][name], dtype=np.uint16).reshape(L * M, N)
+                assert np.array_equal(got, wc), fname + ": codes"
+
+
+def _int_inputs(w):
+    A, B, aux, scalars = W.make_inputs(w)
+    Ai = A.float().numpy().astype(np.int64)
+    Bi = B.float().numpy().astype(np.int64)
+    auxi = [a.float().numpy().astype(np.int64) for a in aux]
+    return (A, B, aux, scalars), Ai, Bi, auxi
+
+
+def pin_integer_closed_form(L_):
+    """Integer inputs: the exact integer result, as the basic-GEMM notebook
+    asserts (assert_array_equal(D, alpha*(A@B) + beta*C))."""
+    w = small(W.CONFIGS[0], L=2, M=24, N=40, K=56)
+    (A, B, aux, sc), Ai, Bi, (Ci,) = _int_inputs(w)
+    acc = np.einsum("lik,lkj->lij", Ai, Bi)  # exact int64
+    aux_ref = 1 * acc + 2 * Ci
+    (D, Aux), _ = run_oracle(L_, w, A, B, aux, sc)
+    assert np.array_equal(np_decode(Aux, "f16"), aux_ref.reshape(-1, w.N).astype(np.float64))
+    assert np.array_equal(np_decode(D, "f16"), 0.5 * aux_ref.reshape(-1, w.N))
+    # ceil(uniform(-4, 4)) inputs and the fused ReLU: D = max(A@B + 2*C, 0)
+    w3 = small(W.CONFIGS[2], L=2, M=20, N=24, K=72)
+    (A, B, aux, sc), Ai, Bi, (Ci,) = _int_inputs(w3)
+    ref = np.maximum(np.einsum("lik,lkj->lij", Ai, Bi) + 2 * Ci, 0).reshape(-1, w3.N)
+    (D,), _ = run_oracle(L_, w3, A, B, aux, sc)
+    assert np.array_equal(np_decode(D, "f16"), ref.astype(np.float64))
+
+
+def pin_broadcast_closed_form(L_):
+    """Row-broadcast bias indexed by column j, same vector for every row and
+    batch: integer inputs, D = relu(0.5*A@B + C + bias), E = D*D rounded."""
+    w = small(W.CONFIGS[4], L=3, M=6, N=16, K=8, dist="randint")
+    (A, B, aux, sc), Ai, Bi, (Ci, biasi) = _int_inputs(w)
+    acc = np.einsum("lik,lkj->lij", Ai, Bi)
+    d = np.maximum(0.5 * acc + Ci + biasi[None, None, :], 0.0).reshape(-1, w.N)
+    (D, E), _ = run_oracle(L_, w, A, B, aux, sc)
+    assert np.array_equal(np_decode(D, "bf16"), d)
+    e_ref = np.array([nearest_even_code(v * v, "bf16") for v in d.ravel()], dtype=np.uint16)
+    assert np.array_equal(zero_norm(E.ravel()), zero_norm(e_ref))
+
+
+def _exact_case(L_, w, rs):
+    """Fraction brute force for one workload at a tiny size with non-integer
+    inputs (N(0,1) rounded to the operand type)."""
+    import torch
+    g = torch.Generator().manual_seed(int(rs.randint(1 << 30)))
+    L, M, N, K = w.L, w.M, w.N, w.K
+    A = torch.randn(L, M, K, generator=g).to(W.TORCH_DTYPE[w.ab])
+    B = torch.randn(L, K, N, generator=g).to(W.TORCH_DTYPE[w.ab])
+    aux = []
+    for _, kind, dt in w.aux:
+        shp = (L, M, N) if kind == "tensor" else (N,)
+        aux.append(torch.randn(shp, generator=g).to(W.TORCH_DTYPE[dt]))
+    scalars = [float(np.float32(v)) for v in rs.uniform(-3, 3, len(w.scalars))]
+    outs, _ = run_oracle(L_, w, A, B, aux, scalars)
+    Af = [[[Fraction(float(x)) for x in r] for r in m] for m in A.double().tolist()]
+    Bf = [[[Fraction(float(x)) for x in r] for r in m] for m in B.double().tolist()]
+    auxf = [a.double().numpy() for a in aux]
+    for l in range(L):
+        for i in range(M):
+            for j in range(N):
+                acc = sum(Af[l][i][k] * Bf[l][k][j] for k in range(K))
+                av = []
+                for (_, kind, _dt), a in zip(w.aux, auxf):
+                    av.append(Fraction(float(a[l, i, j] if kind == "tensor" else a[j])))
+                want = eval_dag_exact(w.dag, acc, av, scalars, len(w.outs))
+                for o, (_, dt) in enumerate(w.outs):
+                    got = outs[o][l * M + i, j]
+                    if dt == "f32":
+                        ref = nearest_even_f32(want[o])
+                        assert got == ref or (got == 0 and ref == 0), (w.name, l, i, j)
+                    else:
+                        ref = nearest_even_code(want[o], dt)
+                        assert zero_norm([got])[0] == zero_norm([ref])[0], (
+                            w.name, l, i, j, hex(int(got)), hex(ref), float(want[o]))
+
+
+def pin_fraction_brute_force(L_):
+    rs = np.random.RandomState(5)
+    cases = list(W.CONFIGS[1:]) + W.page_examples()
+    for w in cases:
+        _exact_case(L_, small(w, L=2, M=3, N=5, K=7), rs)
+
+
+def pin_special_cases(L_):
+    # A = 0: accum = 0, so Aux = beta*C and D = extra_scalar*beta*C
+    w = small(W.CONFIGS[0], L=1, M=8, N=16, K=24)
+    A, B, aux, sc = W.make_inputs(w)
+    A = A * 0
+    (D, Aux), _ = run_oracle(L_, w, A, B, aux, sc)
+    C = aux[0].double().numpy().reshape(-1, w.N)
+    assert np.array_equal(np_decode(Aux, "f16"), 2 * C)
+    assert np.array_equal(np_decode(D, "f16"), C)
+    # B = identity (K = N): accum = A exactly; Y is A's codes and D rounds
+    # 2A + C + 3X (exact in fp64 for fp16 operands) once
+    import torch
+    w4 = small(W.CONFIGS[3], L=2, M=8, N=16, K=16)
+    A, B, aux, sc = W.make_inputs(w4)
+    B = torch.eye(16, dtype=torch.float16).expand(2, 16, 16).contiguous()
+    (D, Y), _ = run_oracle(L_, w4, A, B, aux, sc)
+    assert np.array_equal(zero_norm(Y), zero_norm(W.to_codes(A).reshape(-1, 16)))
+    a, c, x = (t.double().numpy().reshape(-1, 16) for t in (A, aux[0], aux[1]))
+    ref = (2 * a + c + 3 * x).astype(np.float16).view(np.uint16)
+    assert np.array_equal(zero_norm(D), zero_norm(ref))
+
+
+def pin_relu_positive_zero(L_):
+    """ReLU of a non-positive value is +0 ("where(d > 0, d, 0)"), including
+    ReLU of -0: with negative scalars, a zero row of A and a zero row of C
+    make alpha*accum + beta*C = (-0) + (-0) = -0 there."""
+    w = small(W.CONFIGS[2], L=1, M=16, N=16, K=16)
+    A, B, aux, sc = W.make_inputs(w)
+    A[0, 0, :] = 0
+    aux[0][0, 0, :] = 0
+    sc = [-1.0, -2.0]
+    (D,), _ = run_oracle(L_, w, A, B, aux, sc)
+    (F,), _ = run_oracle(L_, small(w, 1, 16, 16, 16), A, B, aux, [1.0, 2.0])
+    vals = np_decode(D, "f16")
+    assert np.all(vals >= 0)
+    assert (vals == 0).sum() > 100
+    assert np.all(D[vals == 0] == 0), "relu must give +0 (code 0x0000)"
+    assert np.all(D[0] == 0)
+    # with the signs flipped every element that was cut to zero is positive
+    flip = np_decode(F, "f16")
+    assert np.all((vals > 0) | (flip >= 0))
+
+
+def pin_rows_and_threads(L_):
+    """A row subset equals the same rows of the full result; thread count
+    does not change any bit."""
+    w = small(W.CONFIGS[3], L=2, M=12, N=24, K=40)
+    A, B, aux, sc = W.make_inputs(w)
+    full, _ = run_oracle(L_, w, A, B, aux, sc, threads=1)
+    rows = np.array([0, 5, 11, 12, 23], dtype=np.int64)
+    part, _ = run_oracle(L_, w, A, B, aux, sc, rows=rows, threads=3)
+    for f, p in zip(full, part):
+        assert np.array_equal(f[rows], p)
+    many, _ = run_oracle(L_, w, A, B, aux, sc, threads=7)
+    for f, m in zip(full, many):
+        assert np.array_equal(f, m)
+
+
+ALL_PINS = [pin_decode_exhaustive, pin_encode_roundtrip, pin_encode_midpoints,
+            pin_encode_random_vs_table, pin_golden, pin_integer_closed_form,
+            pin_broadcast_closed_form, pin_fraction_brute_force, pin_special_cases,
+            pin_relu_positive_zero, pin_rows_and_threads]
+
+
+def run_all(lib_path):
+    """Run every pin against the library at ``lib_path``; used on mutated
+    builds of the oracle.  Exit status 1 when some pin fails."""
+    L_ = oracle.lib(lib_path)
+    failed = []
+    for p in ALL_PINS:
+        try:
+            p(L_)
+        except Exception as e:  # any failure counts as caught
+            failed.append("%s: %s" % (p.__name__, str(e)[:120]))
+    return failed
