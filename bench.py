@@ -1,0 +1,387 @@
+"""Benchmark: fused GEMM + elementwise epilogue on GB300, one JSON line.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload NAME]
+
+A step is one pass of the whole hot path over one batch of synthetic input:
+one fused GEMM + epilogue launch (plan creation is outside the timed region).
+The default workload is the 8192^3 fp16 GEMM with the Alpha-Beta-Scaling
+epilogue (Y = accum; D = 2*accum + C + 3*X), whose inputs (512 MiB) are larger
+than the 129 MB L2, so no L2 flush is needed between steps.
+
+Reported next to the device-timed value:
+  roofline      the fused kernel's achieved TFLOP/s (CUDA events on its
+                launch stream) against the measured dense bf16 peak
+                (MEASURED_PEAKS.json; fp16 has the same nominal rate)
+  e2e           the same metric with pinned-host inputs copied in and the
+                outputs copied back inside every timed step
+  unfused       the same GEMM storing fp32 accum + a separate elementwise
+                kernel (the bytes fusion saves)
+  cpu_baseline  the fp64 CPU oracle on a bounded sample of rows
+  clocks        nvidia-smi samples taken during the timed region
+
+Under torchrun (N > 1) every rank runs an independent replica on its own GPU
+(the problem has no exchange step); value = all ranks' FLOPs / max time.
+"""
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "fused GEMM+epilogue TFLOP/s and % of GB300 dense FP16 peak (1 GPU)"
+DEFAULT_WORKLOAD = "cfg4_alpha_beta_x_8192"
+FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0}
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-unfused", action="store_true")
+    return ap.parse_args()
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "dense_gemm_elementwise_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(workload):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current kernel sources."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+    except (OSError, ValueError):
+        return None
+    ent = d.get(workload)
+    if not ent or ent.get("kernel_hash") != kernel_source_hash():
+        return None
+    return ent.get("dram_bytes_per_launch")
+
+
+# ------------------------------------------------------------ clocks ---
+
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.proc = None
+        self.gpu = gpu_index
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[4:8]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------ helpers ---
+
+def dist_setup(n):
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        dist.init_process_group("gloo", rank=rank, world_size=world)
+    return rank, world, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x, world):
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def oracle_sample(w, A, Bm, aux, scalars, rows, threads):
+    import numpy as np
+
+    import oracle
+    from dense_gemm_elementwise_gb300 import workloads as W
+    t0 = time.perf_counter()
+    oracle.gemm_epilogue(w.L, w.M, w.N, w.K, w.ab, W.to_codes(A), W.to_codes(Bm),
+                         [W.to_codes(a) for a in aux], [dt for _, _, dt in w.aux], scalars, w.dag,
+                         [dt for _, dt in w.outs], rows=np.asarray(rows, dtype=np.int64),
+                         threads=threads)
+    return time.perf_counter() - t0
+
+
+def cpu_baseline(w, inputs, target_s=10.0):
+    """The oracle as it stands, timed on this host's cores on a bounded
+    sample of output rows (each row: N*K multiply-adds)."""
+    import oracle
+    threads = oracle.threads_default()
+    A, Bm, aux, scalars = inputs
+    n = max(threads, 1)
+    t = oracle_sample(w, A, Bm, aux, scalars, list(range(n)), threads)
+    rows = int(min(w.L * w.M, max(n, n * max(1.0, target_s / max(t, 1e-3)))))
+    rows = max(n, (rows // n) * n)
+    t = oracle_sample(w, A, Bm, aux, scalars, list(range(rows)), threads)
+    tflops = 2.0 * rows * w.N * w.K / t / 1e12
+    return {"value": tflops, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+            "sample": "%d of %d output rows (%d x %d multiply-adds each), fp64, %.1f s wall"
+                      % (rows, w.L * w.M, w.N, w.K, t)}
+
+
+# ------------------------------------------------------- reference arm ---
+
+def run_reference(args, w):
+    """The oracle, as it stands, on the same workload: every step evaluates
+    a bounded sample of output rows of it on the host cores."""
+    import oracle
+    from dense_gemm_elementwise_gb300 import workloads as W
+    rank, world, _ = dist_setup(args.gpus)
+    if rank != 0:
+        return
+    inputs = W.make_inputs(w)
+    A, Bm, aux, scalars = inputs
+    threads = oracle.threads_default()
+    rows_per_step = 2 * threads
+    n_rows = w.L * w.M
+    for i in range(args.warmup):
+        oracle_sample(w, A, Bm, aux, scalars, [(i * rows_per_step + r) % n_rows
+                                                for r in range(rows_per_step)], threads)
+    total = 0.0
+    for i in range(args.steps):
+        rows = [((args.warmup + i) * rows_per_step + r) % n_rows for r in range(rows_per_step)]
+        total += oracle_sample(w, A, Bm, aux, scalars, sorted(set(rows)), threads)
+    ms = total / args.steps * 1e3
+    value = 2.0 * rows_per_step * w.N * w.K / (ms * 1e-3) / 1e12
+    sample = "%d output rows per step of %d (%d x %d multiply-adds each), fp64" % (
+        rows_per_step, n_rows, w.N, w.K)
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f64", "data": "synthetic",
+            "config": {"workload": w.name, "L": w.L, "M": w.M, "N": w.N, "K": w.K},
+            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads,
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------ our arm ---
+
+def run_ours(args, w):
+    import torch
+
+    from dense_gemm_elementwise_gb300 import binding as B
+    from dense_gemm_elementwise_gb300 import workloads as W
+
+    rank, world, local = dist_setup(args.gpus)
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.Stream(device=dev)
+    inputs = W.make_inputs(w)
+    A, Bm, aux, scalars = inputs
+    Ad, Bd = A.to(dev), Bm.to(dev)
+    auxd = [a.to(dev) for a in aux]
+    outs = [torch.empty(w.L, w.M, w.N, dtype=W.TORCH_DTYPE[dt], device=dev) for _, dt in w.outs]
+    dtypes = B.make_dtypes(w.ab, [dt for _, _, dt in w.aux], len(w.scalars),
+                           [dt for _, dt in w.outs])
+    plan = B.gemm_epi_plan_create(w.L, w.M, w.N, w.K, dtypes, B.make_dag(w.dag))
+    info = B.gemm_epi_plan_info(plan)
+    flops = w.flops()
+
+    def timed(fn, steps):
+        """CUDA events around every step on the launch stream; returns ms/step."""
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(steps)]
+        torch.cuda.synchronize()
+        barrier(world)
+        torch.cuda.synchronize()
+        with torch.cuda.stream(stream):
+            for s, e in evs:
+                s.record(stream)
+                fn()
+                e.record(stream)
+        torch.cuda.synchronize()
+        barrier(world)
+        torch.cuda.synchronize()
+        return sum(s.elapsed_time(e) for s, e in evs) / steps
+
+    def fused():
+        B.gemm_epi_run(plan, Ad, Bd, auxd, scalars, outs, stream=stream)
+
+    for _ in range(args.warmup):
+        fused()
+    torch.cuda.synchronize()
+    if B.gemm_epi_last_error(plan) != B.GE_OK:
+        raise RuntimeError("device-side timeout during warm-up")
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.2)
+    ms = timed(fused, args.steps)
+    clk = clocks.stop()
+    ms_max = max_over_ranks(ms, world)
+    if B.gemm_epi_last_error(plan) != B.GE_OK:
+        raise RuntimeError("device-side timeout during the timed region")
+    value = world * flops / (ms_max * 1e-3) / 1e12
+
+    pk, pk_src = peaks()
+    peak = float(pk.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    peak_sus = float(pk.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
+    achieved = flops / (ms * 1e-3) / 1e12
+    roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                "frac": achieved / peak, "traffic": ncu_traffic(w.name),
+                "peak_source": "%s bf16 dense burst (fp16 has the same nominal rate)" % pk_src,
+                "frac_of_sustained": achieved / peak_sus,
+                "frac_of_nominal_2250": achieved / 2250.0,
+                "alg_bytes_per_launch": w.alg_bytes(),
+                "hbm_frac": w.alg_bytes() / (ms * 1e-3) / 1e9 / float(pk.get("hbm_gbs", 6800.0))}
+
+    unfused = None
+    if not args.no_unfused:
+        ws = torch.empty(B.gemm_epi_unfused_workspace_bytes(plan) // 4, dtype=torch.float32,
+                         device=dev)
+
+        def unf():
+            B.gemm_epi_run_unfused(plan, Ad, Bd, auxd, scalars, outs, ws, stream=stream)
+
+        for _ in range(max(3, args.warmup // 4)):
+            unf()
+        ums = timed(unf, max(3, args.steps // 4))
+        unfused = {"ms_per_step": ums, "value": flops / (ums * 1e-3) / 1e12,
+                   "fused_speedup": ums / ms, "launches_per_step": 2,
+                   "extra_bytes_per_step": 8 * w.L * w.M * w.N}
+        del ws
+
+    e2e = None
+    if not args.no_e2e:
+        hA, hB = A.pin_memory(), Bm.pin_memory()
+        haux = [a.pin_memory() for a in aux]
+        houts = [torch.empty(o.shape, dtype=o.dtype).pin_memory() for o in outs]
+        h2d = sum(t.numel() * t.element_size() for t in [hA, hB] + haux)
+        d2h = sum(t.numel() * t.element_size() for t in houts)
+
+        def e2e_step():
+            Ad.copy_(hA, non_blocking=True)
+            Bd.copy_(hB, non_blocking=True)
+            for d, h in zip(auxd, haux):
+                d.copy_(h, non_blocking=True)
+            B.gemm_epi_run(plan, Ad, Bd, auxd, scalars, outs, stream=stream)
+            for h, d in zip(houts, outs):
+                h.copy_(d, non_blocking=True)
+
+        for _ in range(3):
+            with torch.cuda.stream(stream):
+                e2e_step()
+        e_steps = max(3, args.steps // 10)
+        ems = max_over_ranks(timed(e2e_step, e_steps), world)
+        e2e = {"value": world * flops / (ems * 1e-3) / 1e12, "unit": "TFLOP/s",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e_steps,
+               "ms_per_step": ems}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(w, inputs)
+
+    B.gemm_epi_plan_destroy(plan)
+    if rank != 0:
+        return
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_max,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f16", "data": "synthetic",
+        "config": {"workload": w.name, "L": w.L, "M": w.M, "N": w.N, "K": w.K,
+                   "ab_dtype": w.ab, "acc_dtype": "f32", "epilogue_dtype": "f32",
+                   "outs": [n + ":" + dt for n, dt in w.outs],
+                   "l2": "no flush: inputs (%d MiB) larger than L2" % (
+                       (w.alg_bytes() - sum(w.L * w.M * w.N * W.ESIZE[dt]
+                                            for _, dt in w.outs)) >> 20),
+                   "plan": info, "parallelism": "replicas" if world > 1 else "single"},
+        "pct_of_peak": 100.0 * achieved / peak,
+        "roofline": roofline, "gpu_launches": args.steps, "clocks": clk,
+        "unfused": unfused, "e2e": e2e, "cpu_baseline": cpu,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    from dense_gemm_elementwise_gb300 import workloads as W
+    w = W.BY_NAME[args.workload]
+    if args.impl == "reference":
+        run_reference(args, w)
+    else:
+        from dense_gemm_elementwise_gb300 import build as gbuild
+        gbuild.build()
+        run_ours(args, w)
+
+
+if __name__ == "__main__":
+    main()

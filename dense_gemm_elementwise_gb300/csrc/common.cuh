@@ -1,0 +1,121 @@
+// common.cuh -- definitions shared by the host plan and the sm_103a kernels:
+// the compiled epilogue program and the kernel parameter block.
+#pragma once
+
+#include <cuda.h>  // CUtensorMap (type only; the driver is reached through cudart)
+#include <stdint.h>
+
+#include "../../include/gemm_epi.h"
+
+namespace ge {
+
+// ---------------------------------------------------------------------------
+// Epilogue program.
+//
+// The host compiles the ge_dag into a short two-address program over a few
+// fp32 vector registers, each holding CH consecutive columns of one output
+// row (a thread's share of an epilogue chunk).  Leaves of the DAG (the
+// accumulator, aux tensors, row-broadcast vectors, scalars) are read straight
+// from their source by the instruction that consumes them, so the program
+// only materialises intermediate values.  The interpreter loops over
+// instructions outside and over the CH columns inside: dispatch is paid once
+// per instruction per chunk, not per element.
+// ---------------------------------------------------------------------------
+constexpr int CH = 16;        // epilogue chunk: columns per thread per step
+constexpr int kRegs = 4;      // vector registers of the epilogue program
+constexpr int kMaxIns = 48;   // instructions in one program
+
+enum EpiOp : uint32_t {
+  OP_MOV = 0,    // r[dst]  = src
+  OP_MUL = 1,    // r[dst] *= src
+  OP_ADD = 2,    // r[dst] += src
+  OP_RELU = 3,   // r[dst]  = r[dst] > 0 ? r[dst] : +0
+  OP_STORE = 4,  // out[dst] = round(src)
+};
+
+enum EpiSrc : uint32_t {
+  SRC_REG = 0,     // r[idx]
+  SRC_ACC = 1,     // accumulator
+  SRC_AUX = 2,     // Load tensor number idx (TMA-staged in the fused kernel)
+  SRC_BCAST = 3,   // row-broadcast vector number idx
+  SRC_SCALAR = 4,  // scalar idx
+  SRC_NONE = 5,
+};
+
+__host__ __device__ constexpr uint32_t pack_ins(uint32_t op, uint32_t dst, uint32_t src,
+                                                uint32_t idx) {
+  return op | (dst << 8) | (src << 16) | (idx << 24);
+}
+
+struct EpiProgram {
+  int32_t n_ins;
+  uint32_t ins[kMaxIns];
+  float scalars[GE_MAX_SCALARS];
+  int32_t n_tma_aux;                      // Load tensors, in first-use order
+  int32_t tma_aux_slot[GE_MAX_TMA_AUX];   // their aux slots
+  int32_t tma_aux_dtype[GE_MAX_TMA_AUX];
+  int32_t n_bcast;                        // Broadcast vectors
+  int32_t bcast_slot[GE_MAX_AUX];
+  int32_t bcast_dtype[GE_MAX_AUX];
+  int32_t n_out;
+  int32_t out_dtype[GE_MAX_OUT];
+  int32_t n_regs;                         // registers the program uses
+};
+
+// ---------------------------------------------------------------------------
+// GEMM kernel parameter block (passed by value as a __grid_constant__).
+// ---------------------------------------------------------------------------
+constexpr int BM = 128;      // accumulator rows per CTA (TMEM lanes)
+constexpr int BK = 64;       // 16-bit elements per k-block: one 128-byte swizzle row
+constexpr int UMMA_K = 16;   // K of one tcgen05.mma.kind::f16
+constexpr int kEpiWarps = 4;
+constexpr int kThreads = 64 + 32 * kEpiWarps;  // producer warp, MMA warp, epilogue warps
+constexpr int kMaxStages = 8;
+constexpr int kMaxAuxStages = 4;
+
+struct alignas(64) KParams {
+  CUtensorMap tmA;                    // (K, M, L) box (64, 128, 1), 128B swizzle
+  CUtensorMap tmB;                    // (N, K, L) box (64, 64, 1), 128B swizzle
+  CUtensorMap tmAux[GE_MAX_TMA_AUX];  // (N, M, L) box (CH, 32, 1)
+  CUtensorMap tmOut[GE_MAX_OUT];      // (N, M, L) box (CH, 32, 1)
+  const void *bcast_ptr[GE_MAX_AUX];
+  uint32_t *status;                   // device status word (timeouts)
+  EpiProgram prog;
+  int32_t L, M, N, K;
+  int32_t ab_bf16;                     // A/B are bf16 (else fp16)
+  int32_t num_m_blk, num_n_blk, num_tiles, num_kb;
+  int32_t raster_group;
+  int32_t stages, aux_stages;
+  uint32_t off_A, off_B, off_aux, off_out, off_bar;  // byte offsets in dynamic smem
+  uint32_t aux_stage_bytes, out_stage_bytes;          // one epilogue warp, one stage
+  uint32_t aux_off[GE_MAX_TMA_AUX], out_off[GE_MAX_OUT];
+  uint32_t tx_bytes;      // bytes one k-block stage receives (both CTAs of a pair)
+  uint32_t aux_tx_bytes;  // bytes one epilogue warp's aux stage receives
+  uint32_t b_lbo, b_sbo;  // B smem descriptor strides (bytes)
+  uint64_t timeout_ns;
+  uint32_t debug_flags;
+};
+
+// Unfused elementwise kernel parameters.
+struct EwParams {
+  const float *acc;                   // (L, M, N) fp32 workspace
+  const void *aux_ptr[GE_MAX_TMA_AUX];
+  const void *bcast_ptr[GE_MAX_AUX];
+  void *out_ptr[GE_MAX_OUT];
+  EpiProgram prog;
+  int64_t rows;                       // L*M
+  int32_t N;
+  int32_t chunks_per_row;             // ceil(N / CH)
+};
+
+// Where a device-side wait gave up (second word of the status block).
+enum WaitSite : uint32_t {
+  SITE_PRODUCER_EMPTY = 1,
+  SITE_MMA_FULL = 2,
+  SITE_MMA_TMEM_EMPTY = 3,
+  SITE_EPI_TMEM_FULL = 4,
+  SITE_EPI_AUX_FULL = 5,
+  SITE_DRAIN = 6,
+};
+
+}  // namespace ge

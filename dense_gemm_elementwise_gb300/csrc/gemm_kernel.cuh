@@ -1,0 +1,418 @@
+// gemm_kernel.cuh -- persistent, warp-specialised GEMM + fused epilogue for sm_103a.
+//
+// One CTA per SM (or one 2x1 cluster per SM pair with cta_group::2), looping
+// over output tiles in a static round-robin order.  Warp roles:
+//   warp 0      TMA producer: A (K-major) and B (N-major) k-blocks into an
+//               S-stage shared-memory ring, full/empty mbarriers per stage.
+//   warp 1      TMEM allocator and MMA issuer: one thread issues
+//               tcgen05.mma (fp16/bf16 -> fp32) into one of two TMEM
+//               accumulators; tcgen05.commit frees ring stages and publishes
+//               finished accumulators.
+//   warps 2-5   epilogue: tcgen05.ld of 16-column chunks, aux tensors staged
+//               per warp by TMA (prefetched ahead, across tiles), the DAG
+//               program in fp32, rounding, TMA stores from swizzled staging.
+// The two TMEM accumulators let the epilogue of tile i overlap the mainloop of
+// tile i+1.  Ragged M/N/K edges are handled by TMA: out-of-range loads read
+// zeros, out-of-range stores are dropped.
+//
+// cta_group::2: the CTA pair computes a (256 x BN) tile.  Each CTA loads its
+// 128 rows of A and its BN/2 columns of B into its own shared memory; the
+// leader's MMA thread issues the pair MMA, which reads both CTAs' halves and
+// writes each CTA's 128 accumulator rows into that CTA's TMEM.  Stage
+// completion is counted on the leader's barriers; commits multicast to both.
+//
+// Every wait is bounded (globaltimer): on expiry the kernel records
+// GE_ERR_TIMEOUT in the status word, stops issuing work, waits (bounded) for
+// its own copies in flight, frees TMEM and exits.
+#pragma once
+
+#include "common.cuh"
+#include "epilogue.cuh"
+#include "ptx.cuh"
+
+namespace ge {
+
+template <int CG, int BN>
+struct TileCfg {
+  static constexpr int kMmaM = BM * CG;            // rows of one MMA tile
+  static constexpr int kBnLocal = BN / CG;         // B columns loaded per CTA
+  static constexpr int kABytes = BM * BK * 2;      // one A stage
+  static constexpr int kBBytes = kBnLocal * BK * 2;
+  static constexpr int kBAtoms = kBnLocal / 64;    // 64-column swizzle atoms of B
+  static constexpr int kChunks = BN / CH;
+  static constexpr int kTmemCols = 2 * BN;         // two accumulators
+  static_assert(kBnLocal % 64 == 0, "B half-tile must be whole 128-byte atoms");
+  static_assert(kTmemCols == 128 || kTmemCols == 256 || kTmemCols == 512, "TMEM alloc size");
+};
+
+// barrier block layout (bytes from off_bar)
+constexpr uint32_t kBarFull = 0;                       // kMaxStages x 8
+constexpr uint32_t kBarEmpty = 64;                     // kMaxStages x 8
+constexpr uint32_t kBarTmemFull = 128;                 // 2 x 8
+constexpr uint32_t kBarTmemEmpty = 144;                // 2 x 8
+constexpr uint32_t kBarAux = 160;                      // kEpiWarps x kMaxAuxStages x 8
+constexpr uint32_t kBarDrain = kBarAux + 8 * kEpiWarps * kMaxAuxStages;  // 288
+constexpr uint32_t kTmemSlot = kBarDrain + 8;          // 296
+constexpr uint32_t kAbortFlag = kTmemSlot + 4;         // 300
+constexpr uint32_t kBarBlockBytes = 512;
+
+__device__ __forceinline__ void tile_coords(const KParams &p, int t, int &l, int &mb, int &nb) {
+  const int per_batch = p.num_m_blk * p.num_n_blk;
+  l = t / per_batch;
+  const int r = t - l * per_batch;
+  // raster: groups of G m-blocks; within a group m varies fastest, so tiles
+  // processed at the same time share their B columns (and A rows across groups)
+  const int G = p.raster_group;
+  const int group = r / (G * p.num_n_blk);
+  const int first_m = group * G;
+  const int gsize = min(p.num_m_blk - first_m, G);
+  const int rr = r - group * G * p.num_n_blk;
+  mb = first_m + rr % gsize;
+  nb = rr / gsize;
+}
+
+struct Waiter {
+  volatile uint32_t *abort_flag;  // shared: this CTA gave up
+  uint32_t *status;               // global status block
+  uint64_t timeout_ns;
+
+  __device__ __forceinline__ void fail(uint32_t site) const {
+    *abort_flag = 1u;
+    if (atomicCAS(status, 0u, static_cast<uint32_t>(GE_ERR_TIMEOUT)) == 0u) {
+      status[1] = site;
+      status[2] = blockIdx.x;
+    }
+  }
+
+  template <bool kCluster = false>
+  __device__ __forceinline__ bool wait(uint32_t bar, uint32_t parity, uint32_t site) const {
+    if (kCluster ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    for (uint32_t it = 1;; ++it) {
+      if (kCluster ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity)) return true;
+      if ((it & 3u) == 0u) {
+        if (*abort_flag) return false;
+        if (globaltimer_ns() - t0 > timeout_ns) {
+          fail(site);
+          return false;
+        }
+      }
+    }
+  }
+
+  // teardown after an abort: ignores the abort flag, still bounded
+  __device__ __forceinline__ bool drain(uint32_t bar, uint32_t parity) const {
+    const uint64_t t0 = globaltimer_ns();
+    while (!mbar_try_wait(bar, parity)) {
+      if (globaltimer_ns() - t0 > timeout_ns) {
+        fail(SITE_DRAIN);
+        return false;
+      }
+    }
+    return true;
+  }
+};
+
+// Epilogue leaves and stores for the fused kernel: aux tensors and outputs
+// live in this warp's swizzled TMA staging boxes (row = lane), broadcast
+// vectors are read from global memory (the same addresses for every lane).
+struct FusedMem {
+  const KParams *p;
+  const uint8_t *aux_stage;
+  uint8_t *out_stage;
+  int row;
+  int col0;
+  __device__ __forceinline__ void aux(uint32_t i, float (&t)[CH]) const {
+    box_load(aux_stage + p->aux_off[i], p->prog.tma_aux_dtype[i], row, t);
+  }
+  __device__ __forceinline__ void bcast(uint32_t i, float (&t)[CH]) const {
+    row_load(p->bcast_ptr[i], p->prog.bcast_dtype[i], col0, p->N, t);
+  }
+  __device__ __forceinline__ void store(uint32_t o, const float (&t)[CH]) const {
+    box_store(out_stage + p->out_off[o], p->prog.out_dtype[o], row, t);
+  }
+};
+
+template <int CG, int BN>
+__global__ void __launch_bounds__(kThreads, 1) gemm_epi_kernel(const __grid_constant__ KParams p) {
+  using T = TileCfg<CG, BN>;
+  extern __shared__ uint8_t smem_raw[];
+  // 1024-byte alignment of the shared-window address (swizzle atoms)
+  uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  const uint32_t sb = smem_u32(smem);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t rank = (CG == 2) ? cluster_ctarank() : 0u;
+  const int unit = blockIdx.x / CG;    // this CTA's cluster (or CTA) index
+  const int n_units = gridDim.x / CG;
+
+  const uint32_t bar = sb + p.off_bar;
+  const uint32_t bar_aux = bar + kBarAux;
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + p.off_bar + kTmemSlot);
+  volatile uint32_t *abort_flag = reinterpret_cast<volatile uint32_t *>(smem + p.off_bar + kAbortFlag);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < p.stages; ++s) {
+      mbar_init(bar + kBarFull + 8 * s, 1);
+      mbar_init(bar + kBarEmpty + 8 * s, 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(bar + kBarTmemFull + 8 * b, 1);
+      mbar_init(bar + kBarTmemEmpty + 8 * b, kEpiWarps * CG);
+    }
+    for (int i = 0; i < kEpiWarps * kMaxAuxStages; ++i) mbar_init(bar_aux + 8 * i, 1);
+    mbar_init(bar + kBarDrain, 1);
+    *abort_flag = 0u;
+    fence_mbarrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    prefetch_tensormap(&p.tmA);
+    prefetch_tensormap(&p.tmB);
+  }
+  if (warp == 1) {
+    tmem_alloc<CG>(smem_u32(tmem_slot), T::kTmemCols);
+    tmem_relinquish<CG>();
+  }
+  __syncwarp();
+  tc_fence_before();
+  if constexpr (CG == 2) cluster_sync_all(); else __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t *>(tmem_slot);
+  const Waiter wt{abort_flag, p.status, p.timeout_ns};
+  const int my_tiles = unit < p.num_tiles ? (p.num_tiles - 1 - unit) / n_units + 1 : 0;
+
+  if (warp == 0) {
+    // ------------------------------------------------------ TMA producer --
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      int fills = 0, skipped = -1;
+      bool skip = (p.debug_flags & GE_DEBUG_SKIP_FIRST_LOAD) != 0u;
+      bool ok = true;
+      for (int i = 0; ok && i < my_tiles; ++i) {
+        int l, mb, nb;
+        tile_coords(p, unit + i * n_units, l, mb, nb);
+        const int m0 = mb * T::kMmaM + static_cast<int>(rank) * BM;
+        const int n0 = nb * BN + static_cast<int>(rank) * T::kBnLocal;
+        for (int kb = 0; kb < p.num_kb; ++kb) {
+          if (!wt.wait(bar + kBarEmpty + 8 * stage, phase ^ 1u, SITE_PRODUCER_EMPTY)) {
+            ok = false;
+            break;
+          }
+          if (skip) {
+            skip = false;
+            skipped = fills;
+          } else {
+            const uint32_t fb_local = bar + kBarFull + 8 * stage;
+            const uint32_t sa = sb + p.off_A + stage * T::kABytes;
+            const uint32_t sbb = sb + p.off_B + stage * T::kBBytes;
+            if constexpr (CG == 2) {
+              const uint32_t fb = mapa_shared(fb_local, 0);
+              if (rank == 0) mbar_arrive_expect_tx(fb_local, p.tx_bytes);
+              tma_load_3d_pair(sa, &p.tmA, fb, kb * BK, m0, l);
+#pragma unroll
+              for (int j = 0; j < T::kBAtoms; ++j)
+                tma_load_3d_pair(sbb + j * 8192, &p.tmB, fb, n0 + 64 * j, kb * BK, l);
+            } else {
+              mbar_arrive_expect_tx(fb_local, p.tx_bytes);
+              tma_load_3d(sa, &p.tmA, fb_local, kb * BK, m0, l);
+#pragma unroll
+              for (int j = 0; j < T::kBAtoms; ++j)
+                tma_load_3d(sbb + j * 8192, &p.tmB, fb_local, n0 + 64 * j, kb * BK, l);
+            }
+          }
+          ++fills;
+          if (++stage == p.stages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      if (ok) {
+        // tail: every stage released by the MMA, so all commit arrivals landed
+        for (int i = 0; i < p.stages; ++i) {
+          if (!wt.wait(bar + kBarEmpty + 8 * stage, phase ^ 1u, SITE_PRODUCER_EMPTY)) {
+            ok = false;
+            break;
+          }
+          if (++stage == p.stages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      if (!ok && rank == 0) {
+        // abort: wait for the copies still in flight into this CTA pair
+        for (int f = fills - p.stages; f < fills; ++f) {
+          if (f < 0 || f == skipped) continue;
+          wt.drain(bar + kBarFull + 8 * (f % p.stages), static_cast<uint32_t>(f / p.stages) & 1u);
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------- MMA issuer --
+    if (lane == 0 && rank == 0) {
+      const uint32_t id = make_idesc_f16(p.ab_bf16 != 0, T::kMmaM, BN);
+      int stage = 0;
+      uint32_t phase = 0;
+      int abuf = 0;
+      uint32_t aphase = 0;
+      bool ok = true;
+      for (int i = 0; ok && i < my_tiles; ++i) {
+        if (!wt.wait<CG == 2>(bar + kBarTmemEmpty + 8 * abuf, aphase ^ 1u, SITE_MMA_TMEM_EMPTY)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d = tmem_base + static_cast<uint32_t>(abuf * BN);
+        for (int kb = 0; kb < p.num_kb; ++kb) {
+          if (!wt.wait(bar + kBarFull + 8 * stage, phase, SITE_MMA_FULL)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sa = sb + p.off_A + stage * T::kABytes;
+          const uint32_t sbb = sb + p.off_B + stage * T::kBBytes;
+#pragma unroll
+          for (int k = 0; k < BK / UMMA_K; ++k) {
+            const uint64_t ad = smem_desc_sw128(sa + 32u * k, 16u, 1024u);
+            const uint64_t bd = smem_desc_sw128(sbb + 2048u * k, p.b_lbo, p.b_sbo);
+            umma_f16<CG>(d, ad, bd, id, (kb | k) != 0 ? 1u : 0u);
+          }
+          umma_commit<CG>(bar + kBarEmpty + 8 * stage);
+          if (++stage == p.stages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        umma_commit<CG>(bar + kBarTmemFull + 8 * abuf);
+        abuf ^= 1;
+        if (abuf == 0) aphase ^= 1u;
+      }
+      if (ok) {
+        // tail: both accumulators released, so every epilogue arrival landed
+        for (int i = 0; i < 2; ++i) {
+          if (!wt.wait<CG == 2>(bar + kBarTmemEmpty + 8 * abuf, aphase ^ 1u, SITE_MMA_TMEM_EMPTY))
+            break;
+          abuf ^= 1;
+          if (abuf == 0) aphase ^= 1u;
+        }
+      } else {
+        // abort: let the MMAs already issued finish before TMEM is freed
+        umma_commit<CG>(bar + kBarDrain);
+        wt.drain(bar + kBarDrain, 0u);
+      }
+    }
+  } else {
+    // --------------------------------------------------------- epilogue --
+    const int e = warp - 2;  // staging slot
+    const int q = warp & 3;  // TMEM lane quarter this warp may access
+    const uint32_t tq = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
+    uint8_t *aux_w = smem + p.off_aux + e * p.aux_stages * p.aux_stage_bytes;
+    uint8_t *out_w = smem + p.off_out + e * 2 * p.out_stage_bytes;
+    const uint32_t auxbar_w = bar_aux + 8u * e * kMaxAuxStages;
+    const bool has_aux = p.prog.n_tma_aux > 0;
+    const int SA = p.aux_stages;
+    const int total = my_tiles * T::kChunks;
+    int issued = 0, g = 0, abuf = 0, obuf = 0;
+    uint32_t aphase = 0;
+    bool ok = true;
+
+    // TMA loads of every Load tensor for this warp's 32 rows of chunk gi
+    auto issue_aux = [&](int gi) {
+      const int ii = gi / T::kChunks, cc = gi - ii * T::kChunks;
+      int l2, mb2, nb2;
+      tile_coords(p, unit + ii * n_units, l2, mb2, nb2);
+      const int as = gi % SA;
+      const uint32_t ab = auxbar_w + 8u * as;
+      uint8_t *dst = aux_w + as * p.aux_stage_bytes;
+      fence_proxy_async_smem();
+      mbar_arrive_expect_tx(ab, p.aux_tx_bytes);
+      const int x = nb2 * BN + cc * CH;
+      const int y = mb2 * T::kMmaM + static_cast<int>(rank) * BM + q * 32;
+      for (int a = 0; a < p.prog.n_tma_aux; ++a)
+        tma_load_3d(smem_u32(dst + p.aux_off[a]), &p.tmAux[a], ab, x, y, l2);
+    };
+
+    for (int i = 0; ok && i < my_tiles; ++i) {
+      int l, mb, nb;
+      tile_coords(p, unit + i * n_units, l, mb, nb);
+      const int m0 = mb * T::kMmaM + static_cast<int>(rank) * BM + q * 32;
+      const int n0 = nb * BN;
+      // start this tile's aux loads before its accumulator is ready
+      if (has_aux && lane == 0) {
+        while (issued < total && issued < g + SA) issue_aux(issued++);
+      }
+      __syncwarp();
+      const bool got = wt.wait(bar + kBarTmemFull + 8 * abuf, aphase, SITE_EPI_TMEM_FULL);
+      if (!__all_sync(0xffffffffu, got)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      for (int c = 0; c < T::kChunks; ++c, ++g) {
+        if (has_aux && lane == 0) {
+          while (issued < total && issued < g + SA) issue_aux(issued++);
+        }
+        __syncwarp();
+        float acc[CH];
+        tmem_ld16(tq + static_cast<uint32_t>(abuf * BN + c * CH), acc);
+        tmem_wait_ld();
+        if (c == T::kChunks - 1) {
+          // accumulator fully read: hand it back to the MMA warp
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) {
+            const uint32_t tb = bar + kBarTmemEmpty + 8 * abuf;
+            if constexpr (CG == 2) mbar_arrive_remote(mapa_shared(tb, 0));
+            else mbar_arrive(tb);
+          }
+        }
+        if (has_aux) {
+          const bool a_ok = wt.wait(auxbar_w + 8u * (g % SA), static_cast<uint32_t>(g / SA) & 1u,
+                                    SITE_EPI_AUX_FULL);
+          if (!__all_sync(0xffffffffu, a_ok)) {
+            ok = false;
+            break;
+          }
+        }
+        // the staging buffer written two chunks ago has been read by its store
+        if (lane == 0) bulk_wait_group_read<1>();
+        __syncwarp();
+        uint8_t *ostage = out_w + obuf * p.out_stage_bytes;
+        FusedMem mem{&p, aux_w + (g % SA) * p.aux_stage_bytes, ostage, lane, n0 + c * CH};
+        run_program(p.prog, acc, mem);
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          for (int o = 0; o < p.prog.n_out; ++o)
+            tma_store_3d(&p.tmOut[o], smem_u32(ostage + p.out_off[o]), n0 + c * CH, m0, l);
+          bulk_commit_group();
+        }
+        obuf ^= 1;
+      }
+      abuf ^= 1;
+      if (abuf == 0) aphase ^= 1u;
+    }
+    if (lane == 0) {
+      if (!ok)
+        for (int gi = g; gi < issued; ++gi)
+          wt.drain(auxbar_w + 8u * (gi % SA), static_cast<uint32_t>(gi / SA) & 1u);
+      bulk_wait_group<0>();
+    }
+    __syncwarp();
+  }
+
+  // ------------------------------------------------------------ teardown --
+  __syncwarp();
+  tc_fence_before();
+  if constexpr (CG == 2) cluster_sync_all(); else __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc<CG>(tmem_base, T::kTmemCols);
+  }
+}
+
+}  // namespace ge

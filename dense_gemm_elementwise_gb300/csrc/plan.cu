@@ -1,0 +1,769 @@
+// plan.cu -- host side of libgemm_epi.so: the C ABI declared in gemm_epi.h.
+//
+//   validate     DAG and type rules (host only, no device needed)
+//   compile      ge_dag -> two-address epilogue program (register allocation)
+//   configure    tile shape, CTA pairing, stage count, persistent grid
+//   run          TMA descriptors (cached per pointer set), one kernel launch
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+#include <new>
+
+#include "common.cuh"
+#include "launch.h"
+
+using namespace ge;
+
+// Device status block: [0] status (GE_OK / GE_ERR_TIMEOUT), [1] wait site,
+// [2] block index, [3] unused.  One per device (module global).
+__device__ uint32_t g_ge_status[4];
+
+namespace {
+
+int esize(int dt) { return dt == GE_F32 ? 4 : 2; }
+bool valid_dtype(int dt) { return dt == GE_F16 || dt == GE_BF16 || dt == GE_F32; }
+
+bool log_enabled() {
+  const char *v = std::getenv("GEMM_EPI_LOG");
+  return v && *v && *v != '0';
+}
+
+// ------------------------------------------------------------- validation --
+bool is_value_node(const ge_dag *dag, int ref, int before) {
+  return ref >= 0 && ref < before && dag->node[ref].op != GE_STORE;
+}
+
+int validate_impl(const ge_dtypes *dt, const ge_dag *dag) {
+  if (!dt || !dag) return GE_ERR_INVALID;
+  if (dt->ab != GE_F16 && dt->ab != GE_BF16) return GE_ERR_UNSUPPORTED;
+  if (dt->acc != GE_F32) return GE_ERR_UNSUPPORTED;
+  if (dt->n_aux < 0 || dt->n_aux > GE_MAX_AUX || dt->n_scalar < 0 ||
+      dt->n_scalar > GE_MAX_SCALARS || dt->n_out < 1 || dt->n_out > GE_MAX_OUT)
+    return GE_ERR_UNSUPPORTED;
+  for (int s = 0; s < dt->n_aux; ++s)
+    if (!valid_dtype(dt->aux[s])) return GE_ERR_UNSUPPORTED;
+  for (int o = 0; o < dt->n_out; ++o)
+    if (!valid_dtype(dt->out[o])) return GE_ERR_UNSUPPORTED;
+  if (dag->n < 1 || dag->n > GE_MAX_NODES) return GE_ERR_UNSUPPORTED;
+
+  bool has_acc = false;
+  int stored[GE_MAX_OUT] = {0};
+  int aux_kind[GE_MAX_AUX] = {0};  // 1 Load tensor, 2 Broadcast vector
+  for (int i = 0; i < dag->n; ++i) {
+    const ge_node &nd = dag->node[i];
+    switch (nd.op) {
+      case GE_ACCFETCH: has_acc = true; break;
+      case GE_LOAD:
+      case GE_BROADCAST: {
+        if (nd.slot < 0 || nd.slot >= dt->n_aux) return GE_ERR_MISSING_ARG;
+        const int kind = nd.op == GE_LOAD ? 1 : 2;
+        if (aux_kind[nd.slot] && aux_kind[nd.slot] != kind) return GE_ERR_UNSUPPORTED;
+        aux_kind[nd.slot] = kind;
+        break;
+      }
+      case GE_SCALAR:
+        if (nd.slot < 0 || nd.slot >= dt->n_scalar) return GE_ERR_MISSING_ARG;
+        break;
+      case GE_MUL:
+      case GE_ADD:
+        if (!is_value_node(dag, nd.b, i)) return GE_ERR_SSA;
+        if (!is_value_node(dag, nd.a, i)) return GE_ERR_SSA;
+        break;
+      case GE_RELU:
+        if (!is_value_node(dag, nd.a, i)) return GE_ERR_SSA;
+        break;
+      case GE_STORE:
+        if (!is_value_node(dag, nd.a, i)) return GE_ERR_SSA;
+        if (nd.slot < 0 || nd.slot >= dt->n_out) return GE_ERR_MISSING_ARG;
+        if (stored[nd.slot]++) return GE_ERR_SSA;
+        break;
+      default: return GE_ERR_UNSUPPORTED;
+    }
+  }
+  if (!has_acc) return GE_ERR_NO_ACCUM;
+  if (!stored[0]) return GE_ERR_NO_D;
+  for (int o = 1; o < dt->n_out; ++o)
+    if (!stored[o]) return GE_ERR_INVALID;
+  return GE_OK;
+}
+
+// -------------------------------------------------------------- compiler --
+// Greedy register allocation in node order.  Leaves are never copied into a
+// register unless an operation needs a destination for them; an operation
+// reuses an operand's register in place when this is the operand's last use.
+int compile_dag(const ge_dtypes *dt, const ge_dag *dag, EpiProgram *P) {
+  std::memset(P, 0, sizeof(*P));
+  const int n = dag->n;
+  int last_use[GE_MAX_NODES];
+  for (int i = 0; i < n; ++i) last_use[i] = -1;
+  for (int i = 0; i < n; ++i) {
+    const ge_node &nd = dag->node[i];
+    if (nd.op == GE_MUL || nd.op == GE_ADD) {
+      last_use[nd.a] = i;
+      last_use[nd.b] = i;
+    } else if (nd.op == GE_RELU || nd.op == GE_STORE) {
+      last_use[nd.a] = i;
+    }
+  }
+  int tma_of_slot[GE_MAX_AUX], bc_of_slot[GE_MAX_AUX];
+  for (int s = 0; s < GE_MAX_AUX; ++s) tma_of_slot[s] = bc_of_slot[s] = -1;
+  struct Loc {
+    uint32_t src, idx;
+  } loc[GE_MAX_NODES];
+  bool busy[kRegs] = {false, false, false, false};
+  int max_regs = 0;
+  bool overflow = false;
+
+  auto emit = [&](uint32_t op, uint32_t dst, Loc s) {
+    if (P->n_ins >= kMaxIns) {
+      overflow = true;
+      return;
+    }
+    P->ins[P->n_ins++] = pack_ins(op, dst, s.src, s.idx);
+  };
+  auto alloc = [&]() -> int {
+    for (int r = 0; r < kRegs; ++r)
+      if (!busy[r]) {
+        busy[r] = true;
+        max_regs = std::max(max_regs, r + 1);
+        return r;
+      }
+    return -1;
+  };
+  auto in_reg_dying = [&](int ref, int at) { return loc[ref].src == SRC_REG && last_use[ref] == at; };
+
+  for (int i = 0; i < n; ++i) {
+    const ge_node &nd = dag->node[i];
+    switch (nd.op) {
+      case GE_ACCFETCH: loc[i] = {SRC_ACC, 0}; break;
+      case GE_LOAD: {
+        int &t = tma_of_slot[nd.slot];
+        if (t < 0) {
+          if (P->n_tma_aux >= GE_MAX_TMA_AUX) return GE_ERR_UNSUPPORTED;
+          t = P->n_tma_aux++;
+          P->tma_aux_slot[t] = nd.slot;
+          P->tma_aux_dtype[t] = dt->aux[nd.slot];
+        }
+        loc[i] = {SRC_AUX, static_cast<uint32_t>(t)};
+        break;
+      }
+      case GE_BROADCAST: {
+        int &b = bc_of_slot[nd.slot];
+        if (b < 0) {
+          b = P->n_bcast++;
+          P->bcast_slot[b] = nd.slot;
+          P->bcast_dtype[b] = dt->aux[nd.slot];
+        }
+        loc[i] = {SRC_BCAST, static_cast<uint32_t>(b)};
+        break;
+      }
+      case GE_SCALAR: loc[i] = {SRC_SCALAR, static_cast<uint32_t>(nd.slot)}; break;
+      case GE_MUL:
+      case GE_ADD: {
+        const uint32_t op = nd.op == GE_MUL ? OP_MUL : OP_ADD;
+        int d, other;
+        if (in_reg_dying(nd.a, i)) {
+          d = static_cast<int>(loc[nd.a].idx);
+          other = nd.b;
+        } else if (in_reg_dying(nd.b, i)) {
+          d = static_cast<int>(loc[nd.b].idx);
+          other = nd.a;
+        } else {
+          d = alloc();
+          if (d < 0) return GE_ERR_UNSUPPORTED;
+          emit(OP_MOV, d, loc[nd.a]);
+          other = nd.b;
+        }
+        emit(op, d, loc[other]);
+        // free operand registers whose last use this was (other than d)
+        for (int ref : {nd.a, nd.b})
+          if (loc[ref].src == SRC_REG && last_use[ref] == i && static_cast<int>(loc[ref].idx) != d)
+            busy[loc[ref].idx] = false;
+        loc[i] = {SRC_REG, static_cast<uint32_t>(d)};
+        if (last_use[i] < 0) busy[d] = false;  // dead value
+        break;
+      }
+      case GE_RELU: {
+        int d;
+        if (in_reg_dying(nd.a, i)) {
+          d = static_cast<int>(loc[nd.a].idx);
+        } else {
+          d = alloc();
+          if (d < 0) return GE_ERR_UNSUPPORTED;
+          emit(OP_MOV, d, loc[nd.a]);
+        }
+        emit(OP_RELU, d, Loc{SRC_NONE, 0});
+        loc[i] = {SRC_REG, static_cast<uint32_t>(d)};
+        if (last_use[i] < 0) busy[d] = false;
+        break;
+      }
+      case GE_STORE: {
+        emit(OP_STORE, static_cast<uint32_t>(nd.slot), loc[nd.a]);
+        if (loc[nd.a].src == SRC_REG && last_use[nd.a] == i) busy[loc[nd.a].idx] = false;
+        break;
+      }
+      default: return GE_ERR_UNSUPPORTED;
+    }
+    if (overflow) return GE_ERR_UNSUPPORTED;
+  }
+  P->n_out = dt->n_out;
+  for (int o = 0; o < dt->n_out; ++o) P->out_dtype[o] = dt->out[o];
+  P->n_regs = max_regs;
+  return GE_OK;
+}
+
+// accumulator-only program of the unfused path's GEMM: out 0 (fp32) = accum
+void program_store_accum(EpiProgram *P) {
+  std::memset(P, 0, sizeof(*P));
+  P->n_ins = 1;
+  P->ins[0] = pack_ins(OP_STORE, 0, SRC_ACC, 0);
+  P->n_out = 1;
+  P->out_dtype[0] = GE_F32;
+}
+
+// ---------------------------------------------------------- TMA encoding --
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                  const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                  const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+CUtensorMapDataType tma_dtype(int dt) {
+  return dt == GE_F32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                      : (dt == GE_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16);
+}
+
+// 3-D tensor (d0 contiguous, d1, d2) with a (b0, b1, 1) box
+bool encode3d(CUtensorMap *m, int dt, const void *ptr, uint64_t d0, uint64_t d1, uint64_t d2,
+              uint32_t b0, uint32_t b1, CUtensorMapSwizzle sw, CUtensorMapL2promotion l2) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  const uint64_t es = static_cast<uint64_t>(esize(dt));
+  cuuint64_t dims[3] = {d0, d1, d2};
+  cuuint64_t strides[2] = {d0 * es, d0 * d1 * es};
+  cuuint32_t box[3] = {b0, b1, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return fn(m, tma_dtype(dt), 3, const_cast<void *>(ptr), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, sw, l2, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+CUtensorMapSwizzle epi_swizzle(int dt) {
+  return dt == GE_F32 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_32B;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// ------------------------------------------------------------ configuration --
+struct Layout {
+  int cg = 0, bn = 0, stages = 0, aux_stages = 0, grid = 0, num_tiles = 0;
+  int smem = 0;       // dynamic smem requested at launch
+  int smem_used = 0;  // bytes the layout occupies
+  int num_m_blk = 0, num_n_blk = 0, num_kb = 0, raster_group = 0;
+  uint32_t off_A = 0, off_B = 0, off_aux = 0, off_out = 0, off_bar = 0;
+  uint32_t aux_stage_bytes = 0, out_stage_bytes = 0;
+  uint32_t aux_off[GE_MAX_TMA_AUX] = {}, out_off[GE_MAX_OUT] = {};
+  uint32_t tx_bytes = 0, aux_tx_bytes = 0;
+};
+
+constexpr int kBarBlock = 512;
+constexpr int kAlignSlack = 1024;
+
+// Shared-memory layout for (cg, bn) and a program; stages = 0 picks the most
+// that fit.  Returns GE_ERR_SMEM if fewer than 2 (or the requested count) fit.
+int make_layout(Layout *Lo, int cg, int bn, int want_stages, const EpiProgram &P, int max_smem) {
+  const uint32_t a_bytes = BM * BK * 2;
+  const uint32_t b_bytes = static_cast<uint32_t>(bn / cg) * BK * 2;
+  uint32_t aux_stage = 0, out_stage = 0;
+  for (int t = 0; t < P.n_tma_aux; ++t) {
+    Lo->aux_off[t] = aux_stage;
+    aux_stage += 32u * CH * esize(P.tma_aux_dtype[t]);
+  }
+  for (int o = 0; o < P.n_out; ++o) {
+    Lo->out_off[o] = out_stage;
+    out_stage += 32u * CH * esize(P.out_dtype[o]);
+  }
+  auto fits = [&](int sa, int *stages_out) {
+    const int64_t epi = int64_t(kEpiWarps) * sa * aux_stage + int64_t(kEpiWarps) * 2 * out_stage;
+    const int64_t room = int64_t(max_smem) - kAlignSlack - kBarBlock - epi;
+    int s = room > 0 ? static_cast<int>(room / (a_bytes + b_bytes)) : 0;
+    s = std::min(s, kMaxStages);
+    *stages_out = s;
+  };
+  int sa = P.n_tma_aux > 0 ? kMaxAuxStages : 1;
+  int stages = 0;
+  fits(sa, &stages);
+  if (P.n_tma_aux > 0 && stages < 4) {
+    int s2 = 0;
+    fits(2, &s2);
+    if (s2 > stages) {
+      sa = 2;
+      stages = s2;
+    }
+  }
+  if (want_stages > 0) {
+    if (want_stages > stages || want_stages > kMaxStages) return GE_ERR_SMEM;
+    stages = want_stages;
+  }
+  if (stages < 2) return GE_ERR_SMEM;
+  Lo->cg = cg;
+  Lo->bn = bn;
+  Lo->stages = stages;
+  Lo->aux_stages = sa;
+  Lo->aux_stage_bytes = aux_stage;
+  Lo->out_stage_bytes = out_stage;
+  Lo->off_A = 0;
+  Lo->off_B = stages * a_bytes;
+  Lo->off_aux = Lo->off_B + stages * b_bytes;
+  Lo->off_out = Lo->off_aux + kEpiWarps * sa * aux_stage;
+  Lo->off_bar = Lo->off_out + kEpiWarps * 2 * out_stage;
+  Lo->smem_used = static_cast<int>(Lo->off_bar + kBarBlock + kAlignSlack);
+  // Always request the whole opt-in shared memory: exactly one CTA per SM, so
+  // co-resident CTAs never compete for TMEM columns (a CTA blocked in
+  // tcgen05.alloc behind another cluster's CTA could otherwise deadlock).
+  Lo->smem = max_smem;
+  Lo->tx_bytes = static_cast<uint32_t>(cg) * (a_bytes + b_bytes);
+  Lo->aux_tx_bytes = aux_stage;
+  return GE_OK;
+}
+
+}  // namespace
+
+// ------------------------------------------------------------------- plan --
+struct gemm_epi_plan {
+  int64_t L = 0, M = 0, N = 0, K = 0;
+  ge_dtypes dt{};
+  ge_dag dag{};
+  ge_options opt{};
+  int device = 0, num_sms = 0, max_smem = 0;
+  uint32_t *status = nullptr;
+  EpiProgram prog{}, prog_acc{};
+  Layout lay, lay_acc;
+  KParams kp{}, kp_acc{};
+  // pointers the cached tensor maps were encoded for
+  const void *mA = nullptr, *mB = nullptr;
+  const void *mAux[GE_MAX_TMA_AUX] = {};
+  void *mOut[GE_MAX_OUT] = {};
+  bool maps_ok = false;
+  const void *aA = nullptr, *aB = nullptr;
+  void *aWs = nullptr;
+  bool acc_maps_ok = false;
+};
+
+namespace {
+
+bool variant_exists(int cg, int bn) {
+  return (cg == 1 && (bn == 64 || bn == 128 || bn == 256)) || (cg == 2 && (bn == 128 || bn == 256));
+}
+
+// Rough cost model in SM clocks: waves x per-tile mainloop, where a k-block
+// costs the larger of its tensor-core time (2*BN clocks for 128 x BN x 64 at
+// 8192 flop/clk/SM) and its operand fill time at ~64 B/clk/SM of L2 bandwidth.
+double est_cycles(const gemm_epi_plan *pl, int cg, int bn, int units) {
+  const int64_t mt = (pl->M + BM * cg - 1) / (BM * cg);
+  const int64_t nt = (pl->N + bn - 1) / bn;
+  const int64_t tiles = pl->L * mt * nt;
+  const int64_t kb = (pl->K + BK - 1) / BK;
+  const double mma = 2.0 * bn;
+  const double fill = double((BM + bn / cg) * BK * 2) / 64.0;
+  const double per_tile = kb * std::max(mma, fill);
+  const int64_t waves = (tiles + units - 1) / units;
+  return waves * per_tile + (bn / CH) * 300.0;
+}
+
+int configure(gemm_epi_plan *pl) {
+  const ge_options &o = pl->opt;
+  if (o.cta_group != 0 && o.cta_group != 1 && o.cta_group != 2) return GE_ERR_INVALID;
+  if (o.tile_n != 0 && o.tile_n != 64 && o.tile_n != 128 && o.tile_n != 256) return GE_ERR_INVALID;
+  if (o.stages < 0 || o.stages > kMaxStages || o.max_ctas < 0 || o.raster_group < 0 ||
+      o.timeout_ms < 0)
+    return GE_ERR_INVALID;
+  const int cand[5][2] = {{2, 256}, {2, 128}, {1, 256}, {1, 128}, {1, 64}};
+  int best = -1;
+  double best_c = 0;
+  for (int c = 0; c < 5; ++c) {
+    const int cg = cand[c][0], bn = cand[c][1];
+    if (o.cta_group && o.cta_group != cg) continue;
+    if (o.tile_n && o.tile_n != bn) continue;
+    int sms = pl->num_sms;
+    if (o.max_ctas) sms = std::min(sms, o.max_ctas);
+    const int units = std::max(1, sms / cg);
+    const double cost = est_cycles(pl, cg, bn, units);
+    if (best < 0 || cost < best_c * 0.98) {
+      best = c;
+      best_c = cost;
+    }
+  }
+  if (best < 0) return GE_ERR_INVALID;  // e.g. cta_group 2 with tile_n 64
+  const int cg = cand[best][0], bn = cand[best][1];
+
+  int st = make_layout(&pl->lay, cg, bn, o.stages, pl->prog, pl->max_smem);
+  if (st != GE_OK) return st;
+  st = make_layout(&pl->lay_acc, cg, bn, o.stages, pl->prog_acc, pl->max_smem);
+  if (st != GE_OK) return st;
+
+  for (Layout *Lo : {&pl->lay, &pl->lay_acc}) {
+    Lo->num_m_blk = static_cast<int>((pl->M + BM * cg - 1) / (BM * cg));
+    Lo->num_n_blk = static_cast<int>((pl->N + bn - 1) / bn);
+    Lo->num_kb = static_cast<int>((pl->K + BK - 1) / BK);
+    const int64_t tiles = pl->L * Lo->num_m_blk * int64_t(Lo->num_n_blk);
+    if (tiles > (int64_t(1) << 30)) return GE_ERR_SHAPE;
+    Lo->num_tiles = static_cast<int>(tiles);
+    Lo->raster_group = o.raster_group ? o.raster_group : 8;
+    int sms = pl->num_sms;
+    if (o.max_ctas) sms = std::min(sms, o.max_ctas);
+    int units = std::max(1, sms / cg);
+    if (cg == 2) {
+      int clusters = 0;
+      if (gemm_prepare(cg, bn, Lo->smem) != cudaSuccess) return GE_ERR_CUDA;
+      if (gemm_max_active_clusters(cg, bn, Lo->smem, &clusters) == cudaSuccess && clusters > 0)
+        units = std::min(units, clusters);
+    }
+    units = static_cast<int>(std::min<int64_t>(units, tiles));
+    Lo->grid = units * cg;
+    if (gemm_prepare(cg, bn, Lo->smem) != cudaSuccess) return GE_ERR_CUDA;
+  }
+  return GE_OK;
+}
+
+void fill_params(const gemm_epi_plan *pl, const Layout &Lo, const EpiProgram &P, KParams *kp) {
+  std::memset(static_cast<void *>(kp), 0, sizeof(*kp));
+  kp->status = pl->status;
+  kp->prog = P;
+  kp->L = static_cast<int32_t>(pl->L);
+  kp->M = static_cast<int32_t>(pl->M);
+  kp->N = static_cast<int32_t>(pl->N);
+  kp->K = static_cast<int32_t>(pl->K);
+  kp->ab_bf16 = pl->dt.ab == GE_BF16;
+  kp->num_m_blk = Lo.num_m_blk;
+  kp->num_n_blk = Lo.num_n_blk;
+  kp->num_tiles = Lo.num_tiles;
+  kp->num_kb = Lo.num_kb;
+  kp->raster_group = Lo.raster_group;
+  kp->stages = Lo.stages;
+  kp->aux_stages = Lo.aux_stages;
+  kp->off_A = Lo.off_A;
+  kp->off_B = Lo.off_B;
+  kp->off_aux = Lo.off_aux;
+  kp->off_out = Lo.off_out;
+  kp->off_bar = Lo.off_bar;
+  kp->aux_stage_bytes = Lo.aux_stage_bytes;
+  kp->out_stage_bytes = Lo.out_stage_bytes;
+  for (int i = 0; i < GE_MAX_TMA_AUX; ++i) kp->aux_off[i] = Lo.aux_off[i];
+  for (int i = 0; i < GE_MAX_OUT; ++i) kp->out_off[i] = Lo.out_off[i];
+  kp->tx_bytes = Lo.tx_bytes;
+  kp->aux_tx_bytes = Lo.aux_tx_bytes;
+  // B tile in shared memory: 64-column (128-byte) swizzle atoms of 64 k-rows
+  // (8 KiB apart), 8-row groups 1 KiB apart
+  kp->b_lbo = 8192;
+  kp->b_sbo = 1024;
+  const int tmo = pl->opt.timeout_ms ? pl->opt.timeout_ms : 1000;
+  kp->timeout_ns = static_cast<uint64_t>(tmo) * 1000000ull;
+  kp->debug_flags = pl->opt.debug_flags;
+}
+
+bool encode_operands(const gemm_epi_plan *pl, KParams *kp, const void *A, const void *B) {
+  const uint64_t L = pl->L, M = pl->M, N = pl->N, K = pl->K;
+  const int ab = pl->dt.ab;
+  return encode3d(&kp->tmA, ab, A, K, M, L, BK, BM, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B) &&
+         encode3d(&kp->tmB, ab, B, N, K, L, 64, BK, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
+}
+
+bool encode_epilogue_map(const gemm_epi_plan *pl, CUtensorMap *m, int dt, const void *ptr) {
+  return encode3d(m, dt, ptr, pl->N, pl->M, pl->L, CH, 32, epi_swizzle(dt),
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_128B);
+}
+
+int check_device(int *dev, int *sms, int *max_smem) {
+  if (cudaGetDevice(dev) != cudaSuccess) {
+    cudaGetLastError();
+    return GE_ERR_ARCH;
+  }
+  int major = 0, minor = 0;
+  if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, *dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, *dev) != cudaSuccess) {
+    cudaGetLastError();
+    return GE_ERR_ARCH;
+  }
+  if (major != 10 || minor != 3) return GE_ERR_ARCH;
+  if (cudaDeviceGetAttribute(sms, cudaDevAttrMultiProcessorCount, *dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(max_smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, *dev) != cudaSuccess)
+    return GE_ERR_CUDA;
+  return GE_OK;
+}
+
+int check_run_args(const gemm_epi_plan *pl, const void *A, const void *B, const void *const *aux,
+                   const float *scalars, void *const *outs) {
+  if (!A || !B || !outs) return GE_ERR_MISSING_ARG;
+  if (pl->dt.n_scalar > 0 && !scalars) return GE_ERR_MISSING_ARG;
+  if (!aligned16(A) || !aligned16(B)) return GE_ERR_MISALIGNED;
+  const EpiProgram &P = pl->prog;
+  if ((P.n_tma_aux + P.n_bcast) > 0 && !aux) return GE_ERR_MISSING_ARG;
+  for (int t = 0; t < P.n_tma_aux; ++t) {
+    const void *p = aux[P.tma_aux_slot[t]];
+    if (!p) return GE_ERR_MISSING_ARG;
+    if (!aligned16(p)) return GE_ERR_MISALIGNED;
+  }
+  for (int b = 0; b < P.n_bcast; ++b) {
+    const void *p = aux[P.bcast_slot[b]];
+    if (!p) return GE_ERR_MISSING_ARG;
+    if (!aligned16(p)) return GE_ERR_MISALIGNED;
+  }
+  for (int o = 0; o < pl->dt.n_out; ++o) {
+    if (!outs[o]) return GE_ERR_MISSING_ARG;
+    if (!aligned16(outs[o])) return GE_ERR_MISALIGNED;
+  }
+  return GE_OK;
+}
+
+void log_plan(const gemm_epi_plan *pl) {
+  const Layout &Lo = pl->lay;
+  std::fprintf(stderr,
+               "[gemm_epi] L=%lld M=%lld N=%lld K=%lld: cta_group=%d tile=%dx%dx%d stages=%d "
+               "aux_stages=%d grid=%d tiles=%d smem=%d program=%d ins/%d regs\n",
+               (long long)pl->L, (long long)pl->M, (long long)pl->N, (long long)pl->K, Lo.cg,
+               BM * Lo.cg, Lo.bn, BK, Lo.stages, Lo.aux_stages, Lo.grid, Lo.num_tiles, Lo.smem_used,
+               pl->prog.n_ins, pl->prog.n_regs);
+}
+
+}  // namespace
+
+// ------------------------------------------------------------- C ABI --
+namespace ge {
+bool gemm_variant_exists(int cg, int bn) { return variant_exists(cg, bn); }
+cudaError_t gemm_prepare(int cg, int bn, int smem) {
+  return cg == 2 ? gemm_prepare_cg2(bn, smem) : gemm_prepare_cg1(bn, smem);
+}
+cudaError_t gemm_launch(int cg, int bn, const KParams &p, int grid, int smem, cudaStream_t s) {
+  return cg == 2 ? gemm_launch_cg2(bn, p, grid, smem, s) : gemm_launch_cg1(bn, p, grid, smem, s);
+}
+cudaError_t gemm_max_active_clusters(int cg, int bn, int smem, int *n) {
+  if (cg != 2) return cudaErrorInvalidValue;
+  return gemm_max_active_clusters_cg2(bn, smem, n);
+}
+}  // namespace ge
+
+extern "C" {
+
+int gemm_epi_validate(const ge_dtypes *dtypes, const ge_dag *dag) {
+  int st = validate_impl(dtypes, dag);
+  if (st != GE_OK) return st;
+  EpiProgram P;
+  return compile_dag(dtypes, dag, &P);
+}
+
+int gemm_epi_plan_create_ex(gemm_epi_plan **plan, int64_t L, int64_t M, int64_t N, int64_t K,
+                            const ge_dtypes *dtypes, const ge_dag *dag, const ge_options *opts) {
+  if (!plan) return GE_ERR_INVALID;
+  *plan = nullptr;
+  int st = validate_impl(dtypes, dag);
+  if (st != GE_OK) return st;
+  if (L <= 0 || M <= 0 || N <= 0 || K <= 0) return GE_ERR_SHAPE;
+  if (M > (int64_t(1) << 31) - 1 || N > (int64_t(1) << 31) - 1 || K > (int64_t(1) << 31) - 1 ||
+      L > (int64_t(1) << 31) - 1)
+    return GE_ERR_SHAPE;
+  // rows of every 2-D / 3-D operand must be whole 16-byte units
+  if ((K * esize(dtypes->ab)) % 16 != 0 || (N * esize(dtypes->ab)) % 16 != 0) return GE_ERR_MISALIGNED;
+  for (int o = 0; o < dtypes->n_out; ++o)
+    if ((N * esize(dtypes->out[o])) % 16 != 0) return GE_ERR_MISALIGNED;
+  for (int s = 0; s < dtypes->n_aux; ++s)
+    if ((N * esize(dtypes->aux[s])) % 16 != 0) return GE_ERR_MISALIGNED;
+
+  gemm_epi_plan *pl = new (std::nothrow) gemm_epi_plan();
+  if (!pl) return GE_ERR_INVALID;
+  pl->L = L;
+  pl->M = M;
+  pl->N = N;
+  pl->K = K;
+  pl->dt = *dtypes;
+  pl->dag = *dag;
+  if (opts) pl->opt = *opts;
+  st = compile_dag(dtypes, dag, &pl->prog);
+  if (st == GE_OK) {
+    program_store_accum(&pl->prog_acc);
+    st = check_device(&pl->device, &pl->num_sms, &pl->max_smem);
+  }
+  if (st == GE_OK) {
+    void *sym = nullptr;
+    if (cudaGetSymbolAddress(&sym, g_ge_status) != cudaSuccess) st = GE_ERR_CUDA;
+    pl->status = static_cast<uint32_t *>(sym);
+  }
+  if (st == GE_OK) st = configure(pl);
+  if (st == GE_OK && !encode_fn()) st = GE_ERR_CUDA;
+  if (st != GE_OK) {
+    cudaGetLastError();
+    delete pl;
+    return st;
+  }
+  fill_params(pl, pl->lay, pl->prog, &pl->kp);
+  fill_params(pl, pl->lay_acc, pl->prog_acc, &pl->kp_acc);
+  if (log_enabled()) log_plan(pl);
+  *plan = pl;
+  return GE_OK;
+}
+
+int gemm_epi_plan_create(gemm_epi_plan **plan, int64_t L, int64_t M, int64_t N, int64_t K,
+                         const ge_dtypes *dtypes, const ge_dag *dag) {
+  return gemm_epi_plan_create_ex(plan, L, M, N, K, dtypes, dag, nullptr);
+}
+
+void gemm_epi_plan_destroy(gemm_epi_plan *plan) { delete plan; }
+
+int gemm_epi_plan_info(const gemm_epi_plan *pl, ge_plan_info *info) {
+  if (!pl || !info) return GE_ERR_INVALID;
+  info->cta_group = pl->lay.cg;
+  info->tile_m = BM * pl->lay.cg;
+  info->tile_n = pl->lay.bn;
+  info->tile_k = BK;
+  info->stages = pl->lay.stages;
+  info->epi_chunk = CH;
+  info->aux_stages = pl->lay.aux_stages;
+  info->grid = pl->lay.grid;
+  info->num_tiles = pl->lay.num_tiles;
+  info->smem_bytes = pl->lay.smem_used;
+  info->n_instr = pl->prog.n_ins;
+  info->n_regs = pl->prog.n_regs;
+  info->num_sms = pl->num_sms;
+  return GE_OK;
+}
+
+int gemm_epi_run(gemm_epi_plan *pl, const void *A, const void *B, const void *const *aux,
+                 const float *scalars, void *const *outs, void *stream) {
+  if (!pl) return GE_ERR_INVALID;
+  int st = check_run_args(pl, A, B, aux, scalars, outs);
+  if (st != GE_OK) return st;
+  KParams &kp = pl->kp;
+  const EpiProgram &P = pl->prog;
+  // re-encode tensor maps only when a pointer changed
+  bool same = pl->maps_ok && pl->mA == A && pl->mB == B;
+  for (int t = 0; same && t < P.n_tma_aux; ++t) same = pl->mAux[t] == aux[P.tma_aux_slot[t]];
+  for (int o = 0; same && o < pl->dt.n_out; ++o) same = pl->mOut[o] == outs[o];
+  if (!same) {
+    pl->maps_ok = false;
+    if (!encode_operands(pl, &kp, A, B)) return GE_ERR_CUDA;
+    for (int t = 0; t < P.n_tma_aux; ++t)
+      if (!encode_epilogue_map(pl, &kp.tmAux[t], P.tma_aux_dtype[t], aux[P.tma_aux_slot[t]]))
+        return GE_ERR_CUDA;
+    for (int o = 0; o < pl->dt.n_out; ++o)
+      if (!encode_epilogue_map(pl, &kp.tmOut[o], P.out_dtype[o], outs[o])) return GE_ERR_CUDA;
+    pl->mA = A;
+    pl->mB = B;
+    for (int t = 0; t < P.n_tma_aux; ++t) pl->mAux[t] = aux[P.tma_aux_slot[t]];
+    for (int o = 0; o < pl->dt.n_out; ++o) pl->mOut[o] = outs[o];
+    pl->maps_ok = true;
+  }
+  for (int b = 0; b < P.n_bcast; ++b) kp.bcast_ptr[b] = aux[P.bcast_slot[b]];
+  for (int s = 0; s < pl->dt.n_scalar; ++s) kp.prog.scalars[s] = scalars[s];
+  const cudaError_t e = gemm_launch(pl->lay.cg, pl->lay.bn, kp, pl->lay.grid, pl->lay.smem,
+                                    static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? GE_OK : GE_ERR_CUDA;
+}
+
+size_t gemm_epi_unfused_workspace_bytes(const gemm_epi_plan *pl) {
+  if (!pl) return 0;
+  return static_cast<size_t>(pl->L) * static_cast<size_t>(pl->M) * static_cast<size_t>(pl->N) * 4u;
+}
+
+int gemm_epi_run_unfused(gemm_epi_plan *pl, const void *A, const void *B, const void *const *aux,
+                         const float *scalars, void *const *outs, void *workspace,
+                         size_t workspace_bytes, void *stream) {
+  if (!pl) return GE_ERR_INVALID;
+  int st = check_run_args(pl, A, B, aux, scalars, outs);
+  if (st != GE_OK) return st;
+  if (!workspace || !aligned16(workspace) || workspace_bytes < gemm_epi_unfused_workspace_bytes(pl))
+    return GE_ERR_WORKSPACE;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  // launch 1: GEMM, accumulator stored as fp32
+  KParams &ka = pl->kp_acc;
+  if (!(pl->acc_maps_ok && pl->aA == A && pl->aB == B && pl->aWs == workspace)) {
+    pl->acc_maps_ok = false;
+    if (!encode_operands(pl, &ka, A, B)) return GE_ERR_CUDA;
+    if (!encode_epilogue_map(pl, &ka.tmOut[0], GE_F32, workspace)) return GE_ERR_CUDA;
+    pl->aA = A;
+    pl->aB = B;
+    pl->aWs = workspace;
+    pl->acc_maps_ok = true;
+  }
+  cudaError_t e = gemm_launch(pl->lay_acc.cg, pl->lay_acc.bn, ka, pl->lay_acc.grid,
+                              pl->lay_acc.smem, s);
+  if (e != cudaSuccess) return GE_ERR_CUDA;
+  // launch 2: the epilogue program, elementwise
+  EwParams ep;
+  std::memset(static_cast<void *>(&ep), 0, sizeof(ep));
+  const EpiProgram &P = pl->prog;
+  ep.acc = static_cast<const float *>(workspace);
+  for (int t = 0; t < P.n_tma_aux; ++t) ep.aux_ptr[t] = aux[P.tma_aux_slot[t]];
+  for (int b = 0; b < P.n_bcast; ++b) ep.bcast_ptr[b] = aux[P.bcast_slot[b]];
+  for (int o = 0; o < pl->dt.n_out; ++o) ep.out_ptr[o] = outs[o];
+  ep.prog = P;
+  for (int i = 0; i < pl->dt.n_scalar; ++i) ep.prog.scalars[i] = scalars[i];
+  ep.rows = pl->L * pl->M;
+  ep.N = static_cast<int32_t>(pl->N);
+  ep.chunks_per_row = static_cast<int32_t>((pl->N + CH - 1) / CH);
+  const int64_t units = ep.rows * ep.chunks_per_row;
+  const int64_t blocks = (units + kEwThreads - 1) / kEwThreads;
+  const int grid = static_cast<int>(std::min<int64_t>(blocks, int64_t(pl->num_sms) * 16));
+  e = ew_launch(ep, std::max(grid, 1), s);
+  return e == cudaSuccess ? GE_OK : GE_ERR_CUDA;
+}
+
+const char *gemm_epi_status_string(int status) {
+  switch (status) {
+    case GE_OK: return "GE_OK";
+    case GE_ERR_NO_ACCUM: return "GE_ERR_NO_ACCUM";
+    case GE_ERR_NO_D: return "GE_ERR_NO_D";
+    case GE_ERR_SSA: return "GE_ERR_SSA";
+    case GE_ERR_MISSING_ARG: return "GE_ERR_MISSING_ARG";
+    case GE_ERR_UNSUPPORTED: return "GE_ERR_UNSUPPORTED";
+    case GE_ERR_MISALIGNED: return "GE_ERR_MISALIGNED";
+    case GE_ERR_ARCH: return "GE_ERR_ARCH";
+    case GE_ERR_SHAPE: return "GE_ERR_SHAPE";
+    case GE_ERR_TIMEOUT: return "GE_ERR_TIMEOUT";
+    case GE_ERR_CUDA: return "GE_ERR_CUDA";
+    case GE_ERR_INVALID: return "GE_ERR_INVALID";
+    case GE_ERR_SMEM: return "GE_ERR_SMEM";
+    case GE_ERR_WORKSPACE: return "GE_ERR_WORKSPACE";
+    default: return "GE_ERR_UNKNOWN";
+  }
+}
+
+int gemm_epi_last_error(gemm_epi_plan *plan) {
+  (void)plan;
+  uint32_t st[4] = {0, 0, 0, 0};
+  if (cudaMemcpyFromSymbol(st, g_ge_status, sizeof(st)) != cudaSuccess) {
+    cudaGetLastError();
+    return GE_ERR_CUDA;
+  }
+  if (st[0] != 0) {
+    const uint32_t zero[4] = {0, 0, 0, 0};
+    if (log_enabled())
+      std::fprintf(stderr, "[gemm_epi] device status %u (wait site %u, block %u)\n", st[0], st[1],
+                   st[2]);
+    if (cudaMemcpyToSymbol(g_ge_status, zero, sizeof(zero)) != cudaSuccess) {
+      cudaGetLastError();
+      return GE_ERR_CUDA;
+    }
+  }
+  return static_cast<int>(st[0]);
+}
+
+}  // extern "C"

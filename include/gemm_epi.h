@@ -1,0 +1,216 @@
+/*
+ * gemm_epi.h -- C ABI of libgemm_epi.so: a batched dense GEMM on one GB300
+ * (sm_103a) whose elementwise epilogue is fused into the same kernel.
+ *
+ *   accum[l] = A[l] @ B[l]                         fp16/bf16 operands, fp32 accumulate
+ *   outs     = epilogue DAG (accum, aux tensors, row-broadcast vectors, scalars)
+ *
+ * What the operation is: "CUTLASS Operator API: Custom epilogue fusions for
+ * GEMMs", sections "Custom epilogue fusions for GEMMs" (a GEMM whose result,
+ * accum, is transformed by a user epilogue before it is stored; outputs D and
+ * Aux, cells [2]-[5]) and "How the epilogue fusion API works" (the epilogue
+ * as a DAG of AccFetch, Load, compute and Store nodes).  The node set here is
+ * that figure's plus Scalar, row Broadcast (section "Row and column
+ * broadcasts") and ReLU (section "Defining an epilogue via a Python
+ * function": predefined activations; "Custom Epilogue Example", section
+ * "Activation Functions").
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  * Layouts are row-major and packed:
+ *      A      (L, M, K)   K contiguous
+ *      B      (L, K, N)   N contiguous
+ *      aux tensors and outputs (L, M, N), N contiguous
+ *      row-broadcast vectors (N,), one vector for every row of every batch.
+ *  * Every device pointer must be 16-byte aligned and every row of a 2-D/3-D
+ *    operand must be a multiple of 16 bytes long ("Custom Epilogue Example",
+ *    section "Constraints": contiguous dimensions 16-byte aligned).
+ *  * The caller owns all device memory (A, B, aux, outputs, the unfused
+ *    workspace).  A plan owns only host state; creating one allocates no
+ *    device memory.  Plans are not thread-safe: use one plan per host thread.
+ *  * `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *    stream).  Runs are asynchronous on that stream; nothing synchronises.
+ *  * The epilogue runs in fp32: every intermediate stays fp32 and only a
+ *    store rounds (round to nearest even) to its output type ("Custom
+ *    Epilogue Example", "Running the Example": --acc_dtype Float32,
+ *    --epi_dtype Float32).  ReLU returns +0 for inputs <= 0.
+ *  * Return values are GE_* status codes; gemm_epi_status_string names them.
+ */
+#ifndef GEMM_EPI_H
+#define GEMM_EPI_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define GE_MAX_NODES 16   /* nodes in one epilogue DAG */
+#define GE_MAX_AUX 8      /* aux slots (Load tensors and Broadcast vectors) */
+#define GE_MAX_TMA_AUX 4  /* of which Load tensors */
+#define GE_MAX_OUT 4      /* output slots */
+#define GE_MAX_SCALARS 16 /* scalar slots */
+
+/* element types */
+typedef enum { GE_F16 = 0, GE_BF16 = 1, GE_F32 = 2 } ge_dtype;
+
+/* DAG node kinds.  `a`, `b` name earlier nodes; `slot` picks the operand. */
+typedef enum {
+  GE_ACCFETCH = 0,  /* the fp32 accumulator accum[l,i,j]                     */
+  GE_LOAD = 1,      /* aux slot `slot`, an (L,M,N) tensor: aux[l,i,j]        */
+  GE_SCALAR = 2,    /* scalar slot `slot`                                    */
+  GE_BROADCAST = 3, /* aux slot `slot`, an (N,) row vector: aux[j]           */
+  GE_MUL = 4,       /* v[a] * v[b]                                           */
+  GE_ADD = 5,       /* v[a] + v[b]                                           */
+  GE_RELU = 6,      /* v[a] > 0 ? v[a] : +0                                  */
+  GE_STORE = 7      /* out slot `slot` = round(v[a]); slot 0 is D            */
+} ge_op;
+
+typedef struct {
+  int32_t op;   /* ge_op */
+  int32_t a;    /* first operand (node index) */
+  int32_t b;    /* second operand (GE_MUL, GE_ADD) */
+  int32_t slot; /* aux / scalar / output slot */
+} ge_node;
+
+/* The epilogue function as a DAG in single assignment, topological order:
+ * every operand refers to an earlier node, every output slot is stored
+ * exactly once (the pages' SSA rule: a variable is assigned once). */
+typedef struct {
+  int32_t n;
+  ge_node node[GE_MAX_NODES];
+} ge_dag;
+
+typedef struct {
+  int32_t ab;                   /* GE_F16 or GE_BF16: type of A and B          */
+  int32_t acc;                  /* must be GE_F32                              */
+  int32_t n_aux;                /* aux slots used (<= GE_MAX_AUX)              */
+  int32_t n_scalar;             /* scalar slots (<= GE_MAX_SCALARS)            */
+  int32_t n_out;                /* output slots (1..GE_MAX_OUT); out[0] is D   */
+  int32_t aux[GE_MAX_AUX];      /* type of each aux slot                       */
+  int32_t out[GE_MAX_OUT];      /* type of each output slot                    */
+} ge_dtypes;
+
+/* Optional tuning knobs; zero-initialise for automatic choices. */
+typedef struct {
+  int32_t cta_group;    /* 0 auto, 1 = one CTA per MMA tile, 2 = CTA pair (2x1 cluster) */
+  int32_t tile_n;       /* 0 auto, else the MMA N: 64, 128 or 256                       */
+  int32_t stages;       /* 0 auto (as many as fit), else 2..8 shared-memory stages      */
+  int32_t max_ctas;     /* 0 = one CTA per SM, else a cap on the persistent grid        */
+  int32_t raster_group; /* 0 auto, else M tiles per raster group (L2 reuse of B)        */
+  int32_t timeout_ms;   /* 0 = 1000; bound on every device-side wait                    */
+  uint32_t debug_flags; /* 0; GE_DEBUG_* below, for tests only                          */
+} ge_options;
+
+/* Test hook: the producer never loads the first k-block, so the MMA warp's
+ * wait on it runs out after timeout_ms and the run reports GE_ERR_TIMEOUT.
+ * Nothing faults or hangs: every wait in the kernel is bounded. */
+#define GE_DEBUG_SKIP_FIRST_LOAD 1u
+
+/* What a plan chose (for logs, tests and the benchmark). */
+typedef struct {
+  int32_t cta_group, tile_m, tile_n, tile_k;  /* tile_m/tile_n: output tile of one MMA */
+  int32_t stages, epi_chunk, aux_stages;
+  int32_t grid, num_tiles, smem_bytes;
+  int32_t n_instr, n_regs;                    /* compiled epilogue program             */
+  int32_t num_sms;
+} ge_plan_info;
+
+typedef struct gemm_epi_plan gemm_epi_plan;
+
+/* status codes */
+enum {
+  GE_OK = 0,
+  GE_ERR_NO_ACCUM = 1,    /* DAG has no GE_ACCFETCH ("accum must be an input to the epilogue") */
+  GE_ERR_NO_D = 2,        /* no GE_STORE to slot 0 ("Output node D is not found")               */
+  GE_ERR_SSA = 3,         /* operand is not an earlier value node, or a slot is stored twice   */
+  GE_ERR_MISSING_ARG = 4, /* slot beyond n_aux/n_scalar/n_out, or a NULL operand at run time   */
+  GE_ERR_UNSUPPORTED = 5, /* unknown op or type, too many nodes/slots, program too large       */
+  GE_ERR_MISALIGNED = 6,  /* pointer or row length not a multiple of 16 bytes                  */
+  GE_ERR_ARCH = 7,        /* no compute-capability 10.3 device current                         */
+  GE_ERR_SHAPE = 8,       /* L, M, N or K <= 0 or too large                                    */
+  GE_ERR_TIMEOUT = 9,     /* a device-side wait ran out (read with gemm_epi_last_error)        */
+  GE_ERR_CUDA = 10,       /* a CUDA runtime / driver call failed                               */
+  GE_ERR_INVALID = 11,    /* NULL plan or struct, bad option, output slot never stored         */
+  GE_ERR_SMEM = 12,       /* the requested tile/stages do not fit in shared memory             */
+  GE_ERR_WORKSPACE = 13   /* unfused workspace missing, misaligned or too small                */
+};
+
+/*
+ * Validate the epilogue and the problem and build a plan.  Host only: checks
+ * the DAG and the types first (no device needed for those errors), then the
+ * current device (compute capability 10.3) and the shared-memory budget,
+ * then compiles the DAG into the kernel's epilogue program and picks the
+ * tile, the stage count and the persistent grid.
+ *   plan   out: the new plan (NULL on failure)
+ *   L,M,N,K   batch count and GEMM sizes, all > 0
+ * Errors: GE_ERR_INVALID, _SHAPE, _UNSUPPORTED, _NO_ACCUM, _NO_D, _SSA,
+ * _MISSING_ARG, _MISALIGNED (row lengths), _ARCH, _SMEM, _CUDA.
+ */
+int gemm_epi_plan_create(gemm_epi_plan **plan, int64_t L, int64_t M, int64_t N, int64_t K,
+                         const ge_dtypes *dtypes, const ge_dag *dag);
+
+/* Same with tuning options (opts may be NULL). */
+int gemm_epi_plan_create_ex(gemm_epi_plan **plan, int64_t L, int64_t M, int64_t N, int64_t K,
+                            const ge_dtypes *dtypes, const ge_dag *dag, const ge_options *opts);
+
+/*
+ * Host-only check of a DAG against its types, with the same codes as
+ * gemm_epi_plan_create; touches no device.
+ */
+int gemm_epi_validate(const ge_dtypes *dtypes, const ge_dag *dag);
+
+/*
+ * Run the fused GEMM + epilogue: one persistent kernel launch on `stream`.
+ *   A, B      device pointers (layouts above)
+ *   aux       n_aux device pointers; entries for slots the DAG never reads may be NULL
+ *   scalars   n_scalar host floats (read during the call; may be NULL if n_scalar == 0)
+ *   outs      n_out device pointers, each (L,M,N) of its output type
+ * Errors: GE_ERR_INVALID, _MISSING_ARG, _MISALIGNED, _CUDA (launch failed).
+ * A device-side timeout is reported later by gemm_epi_last_error.
+ */
+int gemm_epi_run(gemm_epi_plan *plan, const void *A, const void *B, const void *const *aux,
+                 const float *scalars, void *const *outs, void *stream);
+
+/* Bytes of fp32 workspace gemm_epi_run_unfused needs: L*M*N*4. */
+size_t gemm_epi_unfused_workspace_bytes(const gemm_epi_plan *plan);
+
+/*
+ * The unfused comparison path ("Custom Epilogue Example", section
+ * "Overview": the GEMM in one kernel, the elementwise work in another).
+ * Launch 1: the same GEMM kernel stores the fp32 accumulator into
+ * `workspace`; launch 2: a vectorised elementwise kernel reads it back with
+ * the aux operands and evaluates the same epilogue program, so results are
+ * bit-identical to gemm_epi_run.
+ *   workspace        caller-owned device buffer of >= gemm_epi_unfused_workspace_bytes
+ * Errors: as gemm_epi_run, plus GE_ERR_WORKSPACE.
+ */
+int gemm_epi_run_unfused(gemm_epi_plan *plan, const void *A, const void *B,
+                         const void *const *aux, const float *scalars, void *const *outs,
+                         void *workspace, size_t workspace_bytes, void *stream);
+
+/* Free a plan (NULL is ignored).  Does not synchronise. */
+void gemm_epi_plan_destroy(gemm_epi_plan *plan);
+
+/* Fill `info` with the plan's choices.  Errors: GE_ERR_INVALID. */
+int gemm_epi_plan_info(const gemm_epi_plan *plan, ge_plan_info *info);
+
+/* Static name of a status code ("GE_OK", ...); never NULL. */
+const char *gemm_epi_status_string(int status);
+
+/*
+ * Read and clear the sticky device-side status of the current device:
+ * GE_OK, or GE_ERR_TIMEOUT when some wait in a kernel of this library gave
+ * up (the kernel then stopped early and its outputs are undefined).  The
+ * status word is shared by all plans on a device.  Call it after the runs
+ * of interest have completed (e.g. after synchronising their stream); it
+ * performs a synchronous device-to-host copy.  plan may be NULL.
+ */
+int gemm_epi_last_error(gemm_epi_plan *plan);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GEMM_EPI_H */

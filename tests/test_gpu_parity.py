@@ -1,0 +1,181 @@
+"""GPU parity: the CUDA path (through the C ABI) against the fp64 oracle,
+element by element, on the same seeded inputs."""
+import dataclasses
+
+import numpy as np
+import pytest
+import torch
+
+pytestmark = pytest.mark.gpu
+
+import _gpu  # noqa: E402
+from _gpu import B, W  # noqa: E402
+
+
+def small(w, L, M, N, K, **kw):
+    return dataclasses.replace(w, L=L, M=M, N=N, K=K, sample_rows=None, **kw)
+
+
+# --------------------------------------------------- the five workloads --
+
+@pytest.mark.parametrize("w", W.CONFIGS, ids=lambda w: w.name)
+def test_workload_parity(w):
+    """cfg1-3 on every element; cfg4/5 (the full 8192^3 and L=8 sizes, in the
+    launch configuration the benchmark times) on 64 seeded rows per batch,
+    including each batch's first and last row."""
+    inputs = W.make_inputs(w)
+    gpu, info = _gpu.run_gpu(w, inputs)
+    rows = None if w.sample_rows is None else W.sample_rows(w)
+    ref = _gpu.oracle_rows(w, inputs, rows)
+    _gpu.compare(w, gpu, ref, rows)
+
+
+def test_plan_choices_for_headline_sizes():
+    w = W.BY_NAME["cfg4_alpha_beta_x_8192"]
+    plan = B.gemm_epi_plan_create(w.L, w.M, w.N, w.K, _gpu.dtypes_of(w), B.make_dag(w.dag))
+    try:
+        info = B.gemm_epi_plan_info(plan)
+    finally:
+        B.gemm_epi_plan_destroy(plan)
+    assert info["cta_group"] == 2 and info["tile_m"] == 256 and info["tile_n"] == 256
+    assert info["stages"] >= 4 and info["grid"] % 2 == 0
+
+
+# ------------------------------------------------------ page examples --
+
+@pytest.mark.parametrize("w", W.page_examples(L=2, M=256, N=256, K=320), ids=lambda w: w.name)
+def test_page_examples(w):
+    inputs = W.make_inputs(w)
+    gpu, _ = _gpu.run_gpu(w, inputs)
+    _gpu.compare(w, gpu, _gpu.oracle_rows(w, inputs))
+
+
+# ------------------------------------------------ shapes and variants --
+
+SHAPES = [(1, 1, 8, 8), (1, 8, 8, 8), (1, 129, 136, 72), (3, 200, 264, 200),
+          (2, 257, 520, 1000), (1, 300, 24, 64), (1, 64, 1032, 136), (2, 513, 392, 8)]
+VARIANTS = [(1, 64), (1, 128), (1, 256), (2, 128), (2, 256)]
+
+
+@pytest.mark.parametrize("shape", SHAPES, ids=lambda s: "x".join(map(str, s)))
+@pytest.mark.parametrize("variant", VARIANTS, ids=lambda v: "cg%d_n%d" % v)
+def test_ragged_shapes_exact(shape, variant):
+    """Integer inputs: every (cta_group, tile N) variant must be bit-exact on
+    ragged M, N, K (TMA zero-fills loads and clips stores at the edges)."""
+    w = small(W.CONFIGS[0], *shape)
+    inputs = W.make_inputs(w)
+    opt = B.ge_options(cta_group=variant[0], tile_n=variant[1])
+    gpu, info = _gpu.run_gpu(w, inputs, options=opt)
+    assert (info["cta_group"], info["tile_n"]) == variant
+    _gpu.compare(w, gpu, _gpu.oracle_rows(w, inputs))
+
+
+@pytest.mark.parametrize("variant", VARIANTS, ids=lambda v: "cg%d_n%d" % v)
+def test_bf16_bias_relu_square_variants(variant):
+    w = small(W.CONFIGS[4], 2, 384, 520, 264)
+    inputs = W.make_inputs(w)
+    opt = B.ge_options(cta_group=variant[0], tile_n=variant[1])
+    gpu, _ = _gpu.run_gpu(w, inputs, options=opt)
+    _gpu.compare(w, gpu, _gpu.oracle_rows(w, inputs))
+
+
+@pytest.mark.parametrize("stages", [2, 3, 4])
+def test_few_stages(stages):
+    """Short rings wrap the stage/phase bookkeeping many times per tile."""
+    w = small(W.CONFIGS[3], 1, 512, 512, 1024)
+    inputs = W.make_inputs(w)
+    gpu, info = _gpu.run_gpu(w, inputs, options=B.ge_options(stages=stages))
+    assert info["stages"] == stages
+    _gpu.compare(w, gpu, _gpu.oracle_rows(w, inputs))
+
+
+def test_small_grid_many_tiles_per_cta():
+    """Two CTA pairs loop over many tiles: both TMEM accumulators, the aux
+    prefetch across tile boundaries and the raster order all wrap."""
+    w = small(W.CONFIGS[3], 2, 1024, 768, 256)
+    inputs = W.make_inputs(w)
+    gpu, info = _gpu.run_gpu(w, inputs, options=B.ge_options(max_ctas=4, raster_group=3))
+    assert info["grid"] <= 4
+    _gpu.compare(w, gpu, _gpu.oracle_rows(w, inputs))
+
+
+# ------------------------------------------------------------ unfused --
+
+@pytest.mark.parametrize("w", [W.CONFIGS[1], small(W.CONFIGS[4], 2, 256, 392, 520),
+                               small(W.CONFIGS[3], 1, 300, 264, 200)], ids=lambda w: w.name)
+def test_unfused_matches_fused_bitwise(w):
+    """Same compiled program on the same fp32 accumulator: identical bits."""
+    inputs = W.make_inputs(w)
+    fused, _ = _gpu.run_gpu(w, inputs)
+    unfused, _ = _gpu.run_gpu(w, inputs, unfused=True)
+    _gpu.bitwise_equal(fused, unfused)
+    _gpu.compare(w, unfused, _gpu.oracle_rows(w, inputs))
+
+
+def test_variants_agree_on_normal_inputs():
+    w = small(W.CONFIGS[3], 1, 512, 512, 2048)
+    inputs = W.make_inputs(w)
+    base, _ = _gpu.run_gpu(w, inputs, options=B.ge_options(cta_group=2, tile_n=256))
+    for cg, bn in VARIANTS[:-1]:
+        other, _ = _gpu.run_gpu(w, inputs, options=B.ge_options(cta_group=cg, tile_n=bn))
+        for a, b in zip(base, other):
+            assert torch.allclose(a.float(), b.float(), rtol=1e-3, atol=1e-2)
+
+
+def test_repeated_runs_and_side_stream():
+    w = small(W.CONFIGS[0], 1, 384, 256, 512)
+    inputs = W.make_inputs(w)
+    s = torch.cuda.Stream()
+    gpu, _ = _gpu.run_gpu(w, inputs, stream=s, repeat=3)
+    _gpu.compare(w, gpu, _gpu.oracle_rows(w, inputs))
+
+
+# ------------------------------------------------------ error behaviour --
+
+def test_run_argument_errors():
+    w = small(W.CONFIGS[0], 1, 128, 128, 128)
+    A, Bm, aux, sc = [x for x in W.make_inputs(w)]
+    dev = torch.device("cuda")
+    Ad, Bd, Cd = A.cuda(), Bm.cuda(), aux[0].cuda()
+    D = torch.empty(1, 128, 128, dtype=torch.float16, device=dev)
+    X = torch.empty(1, 128, 128, dtype=torch.float16, device=dev)
+    plan = B.gemm_epi_plan_create(1, 128, 128, 128, _gpu.dtypes_of(w), B.make_dag(w.dag))
+    try:
+        assert B.gemm_epi_run(plan, Ad, Bd, [Cd], sc, [D, None], check=False) == \
+            B.GE_ERR_MISSING_ARG
+        assert B.gemm_epi_run(plan, Ad, Bd, [None], sc, [D, X], check=False) == \
+            B.GE_ERR_MISSING_ARG
+        mis = Ad.data_ptr() + 2
+        assert B.gemm_epi_run(plan, mis, Bd, [Cd], sc, [D, X], check=False) == \
+            B.GE_ERR_MISALIGNED
+        ws = torch.empty(16, dtype=torch.float32, device=dev)
+        assert B.gemm_epi_run_unfused(plan, Ad, Bd, [Cd], sc, [D, X], ws, check=False) == \
+            B.GE_ERR_WORKSPACE
+        # nothing was launched by the rejected calls; a good call still works
+        assert B.gemm_epi_run(plan, Ad, Bd, [Cd], sc, [D, X]) == B.GE_OK
+        torch.cuda.synchronize()
+        assert B.gemm_epi_last_error(plan) == B.GE_OK
+    finally:
+        B.gemm_epi_plan_destroy(plan)
+
+
+def test_device_wait_timeout_is_reported():
+    """A k-block that is never loaded: the MMA warp's bounded wait runs out,
+    the kernel records GE_ERR_TIMEOUT, drains and exits; the context stays
+    usable and the next run is correct."""
+    w = small(W.CONFIGS[0], 1, 256, 256, 256)
+    inputs = W.make_inputs(w)
+    opt = B.ge_options(timeout_ms=50, debug_flags=B.GE_DEBUG_SKIP_FIRST_LOAD, max_ctas=2)
+    A, Bm, aux, sc = inputs
+    dev = torch.device("cuda")
+    outs = [torch.empty(1, 256, 256, dtype=torch.float16, device=dev) for _ in range(2)]
+    plan = B.gemm_epi_plan_create(1, 256, 256, 256, _gpu.dtypes_of(w), B.make_dag(w.dag), opt)
+    try:
+        assert B.gemm_epi_run(plan, A.cuda(), Bm.cuda(), [aux[0].cuda()], sc, outs) == B.GE_OK
+        torch.cuda.synchronize()
+        assert B.gemm_epi_last_error(plan) == B.GE_ERR_TIMEOUT
+        assert B.gemm_epi_last_error(plan) == B.GE_OK  # read-and-clear
+    finally:
+        B.gemm_epi_plan_destroy(plan)
+    gpu, _ = _gpu.run_gpu(w, inputs)
+    _gpu.compare(w, gpu, _gpu.oracle_rows(w, inputs))
