@@ -48,6 +48,8 @@ def parse():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--mnk", default=None,
+                    help="M,N,K override of the workload's sizes (profiling on a smaller case)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-unfused", action="store_true")
@@ -375,6 +377,10 @@ def main():
     args = parse()
     from dense_gemm_elementwise_gb300 import workloads as W
     w = W.BY_NAME[args.workload]
+    if args.mnk:
+        import dataclasses
+        m, n, k = (int(x) for x in args.mnk.split(","))
+        w = dataclasses.replace(w, M=m, N=n, K=k, name="%s@%dx%dx%d" % (w.name, m, n, k))
     if args.impl == "reference":
         run_reference(args, w)
     else:

@@ -15,6 +15,7 @@ GE_F16, GE_BF16, GE_F32 = 0, 1, 2
 GE_ACCFETCH, GE_LOAD, GE_SCALAR, GE_BROADCAST, GE_MUL, GE_ADD, GE_RELU, GE_STORE = range(8)
 GE_MAX_NODES, GE_MAX_AUX, GE_MAX_TMA_AUX, GE_MAX_OUT, GE_MAX_SCALARS = 16, 8, 4, 4, 16
 GE_DEBUG_SKIP_FIRST_LOAD = 1
+GE_DEBUG_FORCE_INTERPRETER = 2
 
 STATUS = ["GE_OK", "GE_ERR_NO_ACCUM", "GE_ERR_NO_D", "GE_ERR_SSA", "GE_ERR_MISSING_ARG",
           "GE_ERR_UNSUPPORTED", "GE_ERR_MISALIGNED", "GE_ERR_ARCH", "GE_ERR_SHAPE",
@@ -57,7 +58,8 @@ class ge_options(ctypes.Structure):
 class ge_plan_info(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in
                 ("cta_group", "tile_m", "tile_n", "tile_k", "stages", "epi_chunk", "aux_stages",
-                 "grid", "num_tiles", "smem_bytes", "n_instr", "n_regs", "num_sms")]
+                 "grid", "num_tiles", "smem_bytes", "n_instr", "n_regs", "num_sms",
+                 "epi_variant")]
 
 
 class GemmEpiError(RuntimeError):

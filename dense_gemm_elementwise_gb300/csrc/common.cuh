@@ -5,7 +5,7 @@
 #include <cuda.h>  // CUtensorMap (type only; the driver is reached through cudart)
 #include <stdint.h>
 
-#include "../../include/gemm_epi.h"
+#include "gemm_epi.h"
 
 namespace ge {
 
@@ -21,7 +21,8 @@ namespace ge {
 // instructions outside and over the CH columns inside: dispatch is paid once
 // per instruction per chunk, not per element.
 // ---------------------------------------------------------------------------
-constexpr int CH = 16;        // epilogue chunk: columns per thread per step
+constexpr int CH = 16;        // columns one program evaluation covers per thread
+constexpr int EW = 32;        // columns of one fused-epilogue step (TMA box width)
 constexpr int kRegs = 4;      // vector registers of the epilogue program
 constexpr int kMaxIns = 48;   // instructions in one program
 
@@ -73,11 +74,11 @@ constexpr int kThreads = 64 + 32 * kEpiWarps;  // producer warp, MMA warp, epilo
 constexpr int kMaxStages = 8;
 constexpr int kMaxAuxStages = 4;
 
-struct alignas(64) KParams {
+struct KParams {
   CUtensorMap tmA;                    // (K, M, L) box (64, 128, 1), 128B swizzle
   CUtensorMap tmB;                    // (N, K, L) box (64, 64, 1), 128B swizzle
-  CUtensorMap tmAux[GE_MAX_TMA_AUX];  // (N, M, L) box (CH, 32, 1)
-  CUtensorMap tmOut[GE_MAX_OUT];      // (N, M, L) box (CH, 32, 1)
+  CUtensorMap tmAux[GE_MAX_TMA_AUX];  // (N, M, L) box (EW, 32, 1)
+  CUtensorMap tmOut[GE_MAX_OUT];      // (N, M, L) box (EW, 32, 1)
   const void *bcast_ptr[GE_MAX_AUX];
   uint32_t *status;                   // device status word (timeouts)
   EpiProgram prog;
@@ -105,7 +106,7 @@ struct EwParams {
   EpiProgram prog;
   int64_t rows;                       // L*M
   int32_t N;
-  int32_t chunks_per_row;             // ceil(N / CH)
+  int32_t chunks_per_row;             // ceil(N / 8): one thread per 8 columns
 };
 
 // Where a device-side wait gave up (second word of the status block).

@@ -1,17 +1,22 @@
-// epilogue.cuh -- device interpreter of the compiled epilogue program.
+// epilogue.cuh -- evaluation of the compiled epilogue program.
 //
-// One call evaluates the whole program for one chunk: CH consecutive columns
-// of one output row, held by one thread.  Instruction dispatch is uniform
-// across the warp (every lane runs the same program), values stay in
-// registers (all register-array indices are compile-time constants inside
-// the switch cases), and every operation is plain fp32: multiply, add,
-// max-with-zero.  A store rounds once, to nearest even, to its output type.
+// A program (program.cuh) is evaluated for CH consecutive columns of one
+// output row per thread.  Two executors evaluate the same instruction list:
 //
-// The memory policy `Mem` supplies the leaves (aux tensors, broadcast
-// vectors) and takes the stores: the fused kernel reads/writes swizzled
-// shared-memory staging boxes moved by TMA; the unfused elementwise kernel
-// reads/writes global memory directly.  The arithmetic is the same code in
-// both, so the two paths agree bit for bit.
+//   run_program<CH>          the interpreter: one uniform dispatch per
+//                            instruction per CH columns (any DAG the plan
+//                            compiler accepts);
+//   run_static_from<SP,..>   the catalog executor: the instruction list is a
+//                            compile-time constant, every dispatch is resolved
+//                            by `if constexpr`, leaving straight-line fp32 code.
+//
+// All register-array indices are compile-time constants, so values stay in
+// registers.  Multiplies and adds are __fmul_rn/__fadd_rn (never contracted
+// into an FMA); ReLU returns +0 for x <= 0; a store rounds once to nearest
+// even.  The memory policy `Mem` supplies aux tensors and broadcast vectors
+// and takes the stores: swizzled shared-memory TMA boxes in the fused kernel,
+// global memory in the unfused elementwise kernel.  Same arithmetic, same
+// order, so every executor and kernel agrees bit for bit.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -49,88 +54,93 @@ __device__ __forceinline__ uint32_t f32x2_to_bf16x2(float a, float b) {
   return *reinterpret_cast<uint32_t *>(&h);
 }
 
-// 8 16-bit values in a uint4 -> 8 floats
-__device__ __forceinline__ void unpack8(const uint4 &v, int dtype, float *t) {
+template <int DT>
+__device__ __forceinline__ void unpack8(const uint4 &v, float *t) {
   const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
-    float2 f = (dtype == GE_BF16) ? bf16x2_to_f32x2(w[i]) : f16x2_to_f32x2(w[i]);
+    const float2 f = DT == GE_BF16 ? bf16x2_to_f32x2(w[i]) : f16x2_to_f32x2(w[i]);
     t[2 * i] = f.x;
     t[2 * i + 1] = f.y;
   }
 }
 
-__device__ __forceinline__ uint4 pack8(const float *t, int dtype) {
+template <int DT>
+__device__ __forceinline__ uint4 pack8(const float *t) {
   uint32_t w[4];
 #pragma unroll
   for (int i = 0; i < 4; ++i)
-    w[i] = (dtype == GE_BF16) ? f32x2_to_bf16x2(t[2 * i], t[2 * i + 1])
-                              : f32x2_to_f16x2(t[2 * i], t[2 * i + 1]);
+    w[i] = DT == GE_BF16 ? f32x2_to_bf16x2(t[2 * i], t[2 * i + 1])
+                         : f32x2_to_f16x2(t[2 * i], t[2 * i + 1]);
   return make_uint4(w[0], w[1], w[2], w[3]);
 }
 
 // ----------------------------------------------------- swizzled staging box --
-// A TMA box of 32 rows x CH columns.  Rows are 32 bytes (16-bit types, 32-byte
-// swizzle) or 64 bytes (fp32, 64-byte swizzle); the swizzle XORs the 16-byte
-// chunk index with address bits 7.. (row >> 2 or row >> 1), so a warp's 16-byte
-// accesses to one chunk column touch every bank once per 8 threads.
-__device__ __forceinline__ uint32_t box_off16(int row, int j) {
-  return row * 32 + ((j ^ ((row >> 2) & 1)) << 4);
-}
-__device__ __forceinline__ uint32_t box_off32(int row, int j) {
-  return row * 64 + ((j ^ ((row >> 1) & 3)) << 4);
-}
-
-__device__ __forceinline__ void box_load(const uint8_t *box, int dtype, int row, float (&t)[CH]) {
-  if (dtype == GE_F32) {
+// One TMA box: 32 rows x EW (32) columns, row = lane.  16-bit rows are 64 bytes
+// (64-byte swizzle: 16-byte chunk j of row r at r*64 + ((j ^ ((r>>1)&3))*16));
+// fp32 rows are 128 bytes (128-byte swizzle: chunk j at r*128 + ((j ^ (r&7))*16)).
+// Either way the 8 lanes of a 16-byte access phase hit 8 different bank
+// groups.  `half` selects columns [16*half, 16*half + 16) of the box.
+template <int DT>
+__device__ __forceinline__ void box_load(const uint8_t *box, int row, int half, float (&t)[16]) {
+  if constexpr (DT == GE_F32) {
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      float4 v = *reinterpret_cast<const float4 *>(box + box_off32(row, j));
-      t[4 * j] = v.x;
-      t[4 * j + 1] = v.y;
-      t[4 * j + 2] = v.z;
-      t[4 * j + 3] = v.w;
+    for (int k = 0; k < 4; ++k) {
+      const int j = 4 * half + k;
+      const float4 v = *reinterpret_cast<const float4 *>(box + row * 128 + ((j ^ (row & 7)) << 4));
+      t[4 * k] = v.x;
+      t[4 * k + 1] = v.y;
+      t[4 * k + 2] = v.z;
+      t[4 * k + 3] = v.w;
     }
   } else {
 #pragma unroll
-    for (int j = 0; j < 2; ++j) {
-      uint4 v = *reinterpret_cast<const uint4 *>(box + box_off16(row, j));
-      unpack8(v, dtype, t + 8 * j);
+    for (int k = 0; k < 2; ++k) {
+      const int j = 2 * half + k;
+      const uint4 v =
+          *reinterpret_cast<const uint4 *>(box + row * 64 + ((j ^ ((row >> 1) & 3)) << 4));
+      unpack8<DT>(v, t + 8 * k);
     }
   }
 }
 
-__device__ __forceinline__ void box_store(uint8_t *box, int dtype, int row, const float (&t)[CH]) {
-  if (dtype == GE_F32) {
+template <int DT>
+__device__ __forceinline__ void box_store(uint8_t *box, int row, int half, const float (&t)[16]) {
+  if constexpr (DT == GE_F32) {
 #pragma unroll
-    for (int j = 0; j < 4; ++j)
-      *reinterpret_cast<float4 *>(box + box_off32(row, j)) =
-          make_float4(t[4 * j], t[4 * j + 1], t[4 * j + 2], t[4 * j + 3]);
+    for (int k = 0; k < 4; ++k) {
+      const int j = 4 * half + k;
+      *reinterpret_cast<float4 *>(box + row * 128 + ((j ^ (row & 7)) << 4)) =
+          make_float4(t[4 * k], t[4 * k + 1], t[4 * k + 2], t[4 * k + 3]);
+    }
   } else {
 #pragma unroll
-    for (int j = 0; j < 2; ++j)
-      *reinterpret_cast<uint4 *>(box + box_off16(row, j)) = pack8(t + 8 * j, dtype);
+    for (int k = 0; k < 2; ++k) {
+      const int j = 2 * half + k;
+      *reinterpret_cast<uint4 *>(box + row * 64 + ((j ^ ((row >> 1) & 3)) << 4)) =
+          pack8<DT>(t + 8 * k);
+    }
   }
 }
 
 // ------------------------------------------------------- global row access --
-// CH elements of a row starting at column col0 (a multiple of CH).  Rows are
-// multiples of 16 bytes and N is a multiple of 8, so each group of 8
+// C (8 or 16) elements of a row starting at column col0 (a multiple of 8).
+// Rows are multiples of 16 bytes and N is a multiple of 8, so each group of 8
 // columns is entirely inside or entirely outside the row.
-__device__ __forceinline__ void row_load(const void *row, int dtype, int col0, int N,
-                                         float (&t)[CH]) {
+template <int DT, int C>
+__device__ __forceinline__ void row_load(const void *row, int col0, int N, float (&t)[C]) {
 #pragma unroll
-  for (int h = 0; h < 2; ++h) {
+  for (int h = 0; h < C / 8; ++h) {
     const int c = col0 + 8 * h;
     if (c < N) {
-      if (dtype == GE_F32) {
+      if constexpr (DT == GE_F32) {
         const float4 *p = reinterpret_cast<const float4 *>(static_cast<const float *>(row) + c);
-        float4 a = __ldg(p), b = __ldg(p + 1);
+        const float4 a = __ldg(p), b = __ldg(p + 1);
         t[8 * h] = a.x; t[8 * h + 1] = a.y; t[8 * h + 2] = a.z; t[8 * h + 3] = a.w;
         t[8 * h + 4] = b.x; t[8 * h + 5] = b.y; t[8 * h + 6] = b.z; t[8 * h + 7] = b.w;
       } else {
-        uint4 v = __ldg(reinterpret_cast<const uint4 *>(static_cast<const uint16_t *>(row) + c));
-        unpack8(v, dtype, t + 8 * h);
+        const uint4 v = __ldg(reinterpret_cast<const uint4 *>(static_cast<const uint16_t *>(row) + c));
+        unpack8<DT>(v, t + 8 * h);
       }
     } else {
 #pragma unroll
@@ -139,37 +149,52 @@ __device__ __forceinline__ void row_load(const void *row, int dtype, int col0, i
   }
 }
 
-__device__ __forceinline__ void row_store(void *row, int dtype, int col0, int N,
-                                          const float (&t)[CH]) {
+template <int DT, int C>
+__device__ __forceinline__ void row_store(void *row, int col0, int N, const float (&t)[C]) {
 #pragma unroll
-  for (int h = 0; h < 2; ++h) {
+  for (int h = 0; h < C / 8; ++h) {
     const int c = col0 + 8 * h;
     if (c < N) {
-      if (dtype == GE_F32) {
+      if constexpr (DT == GE_F32) {
         float4 *p = reinterpret_cast<float4 *>(static_cast<float *>(row) + c);
         p[0] = make_float4(t[8 * h], t[8 * h + 1], t[8 * h + 2], t[8 * h + 3]);
         p[1] = make_float4(t[8 * h + 4], t[8 * h + 5], t[8 * h + 6], t[8 * h + 7]);
       } else {
-        *reinterpret_cast<uint4 *>(static_cast<uint16_t *>(row) + c) = pack8(t + 8 * h, dtype);
+        *reinterpret_cast<uint4 *>(static_cast<uint16_t *>(row) + c) = pack8<DT>(t + 8 * h);
       }
     }
   }
 }
 
+// run-time element type -> compile-time instantiation
+#define GE_DISPATCH_DTYPE(dt, CALL) \
+  do {                              \
+    if ((dt) == GE_F32) {           \
+      constexpr int DT_ = GE_F32;   \
+      CALL;                         \
+    } else if ((dt) == GE_BF16) {   \
+      constexpr int DT_ = GE_BF16;  \
+      CALL;                         \
+    } else {                        \
+      constexpr int DT_ = GE_F16;   \
+      CALL;                         \
+    }                               \
+  } while (0)
+
 // ------------------------------------------------------------ interpreter --
-template <class Mem>
-__device__ __forceinline__ void run_program(const EpiProgram &P, const float (&acc)[CH], Mem &mem) {
-  float r[kRegs][CH];
+template <int C, class Mem>
+__device__ __forceinline__ void run_program(const EpiProgram &P, const float (&acc)[C], const Mem &mem) {
+  float r[kRegs][C];
 #pragma unroll
   for (int i = 0; i < kRegs; ++i)
 #pragma unroll
-    for (int e = 0; e < CH; ++e) r[i][e] = 0.f;
+    for (int e = 0; e < C; ++e) r[i][e] = 0.f;
 
 #pragma unroll 1
   for (int pc = 0; pc < P.n_ins; ++pc) {
     const uint32_t w = P.ins[pc];
     const uint32_t op = w & 0xFFu, dst = (w >> 8) & 0xFFu, src = (w >> 16) & 0xFFu, idx = w >> 24;
-    float t[CH];
+    float t[C];
     switch (src) {
       case SRC_REG:
         switch (idx) {
@@ -180,25 +205,25 @@ __device__ __forceinline__ void run_program(const EpiProgram &P, const float (&a
         }
         break;
       case SRC_ACC: vcopy(t, acc); break;
-      case SRC_AUX: mem.aux(idx, t); break;
-      case SRC_BCAST: mem.bcast(idx, t); break;
+      case SRC_AUX: GE_DISPATCH_DTYPE(P.tma_aux_dtype[idx], mem.template aux<DT_>(idx, t)); break;
+      case SRC_BCAST: GE_DISPATCH_DTYPE(P.bcast_dtype[idx], mem.template bcast<DT_>(idx, t)); break;
       case SRC_SCALAR: {
         const float s = P.scalars[idx];
 #pragma unroll
-        for (int e = 0; e < CH; ++e) t[e] = s;
+        for (int e = 0; e < C; ++e) t[e] = s;
       } break;
       default:
 #pragma unroll
-        for (int e = 0; e < CH; ++e) t[e] = 0.f;
+        for (int e = 0; e < C; ++e) t[e] = 0.f;
         break;
     }
-#define GE_APPLY(D, EXPR)                     \
-  case D: {                                   \
-    _Pragma("unroll") for (int e = 0; e < CH; ++e) { \
-      const float x = r[D][e];                \
-      (void)x;                                \
-      r[D][e] = (EXPR);                       \
-    }                                         \
+#define GE_APPLY(D, EXPR)                             \
+  case D: {                                           \
+    _Pragma("unroll") for (int e = 0; e < C; ++e) {   \
+      const float x = r[D][e];                        \
+      (void)x;                                        \
+      r[D][e] = (EXPR);                               \
+    }                                                 \
   } break;
     switch (op) {
       case OP_MOV:
@@ -223,11 +248,70 @@ __device__ __forceinline__ void run_program(const EpiProgram &P, const float (&a
         }
         break;
       default:  // OP_STORE
-        mem.store(dst, t);
+        GE_DISPATCH_DTYPE(P.out_dtype[dst], mem.template store<DT_>(dst, t));
         break;
     }
 #undef GE_APPLY
   }
 }
+
+// ---------------------------------------------------- catalog (static) --
+template <class SP, int PC, int C, class Mem>
+__device__ __forceinline__ void run_static_from(float (&r)[kRegs][C], const float (&acc)[C],
+                                                const Mem &mem, const float *scalars) {
+  if constexpr (PC < SP::P.n_ins) {
+    constexpr uint32_t w = SP::P.ins[PC];
+    constexpr uint32_t op = w & 0xFFu, dst = (w >> 8) & 0xFFu, src = (w >> 16) & 0xFFu,
+                       idx = w >> 24;
+    if constexpr (op == OP_RELU) {
+#pragma unroll
+      for (int e = 0; e < C; ++e) r[dst][e] = r[dst][e] > 0.f ? r[dst][e] : 0.f;
+    } else {
+      float t[C];
+      if constexpr (src == SRC_REG) {
+        vcopy(t, r[idx]);
+      } else if constexpr (src == SRC_ACC) {
+        vcopy(t, acc);
+      } else if constexpr (src == SRC_AUX) {
+        mem.template aux<SP::P.tma_aux_dtype[idx]>(idx, t);
+      } else if constexpr (src == SRC_BCAST) {
+        mem.template bcast<SP::P.bcast_dtype[idx]>(idx, t);
+      } else {
+        const float s = scalars[idx];
+#pragma unroll
+        for (int e = 0; e < C; ++e) t[e] = s;
+      }
+      if constexpr (op == OP_MOV) {
+        vcopy(r[dst], t);
+      } else if constexpr (op == OP_MUL) {
+#pragma unroll
+        for (int e = 0; e < C; ++e) r[dst][e] = __fmul_rn(r[dst][e], t[e]);
+      } else if constexpr (op == OP_ADD) {
+#pragma unroll
+        for (int e = 0; e < C; ++e) r[dst][e] = __fadd_rn(r[dst][e], t[e]);
+      } else {
+        mem.template store<SP::P.out_dtype[dst]>(dst, t);
+      }
+    }
+    run_static_from<SP, PC + 1, C>(r, acc, mem, scalars);
+  }
+}
+
+// Epilogue selectors used as kernel template arguments.
+struct EpiInterp {
+  template <int C, class Mem>
+  __device__ __forceinline__ static void run(const EpiProgram &P, const float (&acc)[C], const Mem &mem) {
+    run_program<C>(P, acc, mem);
+  }
+};
+
+template <class SP>
+struct EpiStatic {
+  template <int C, class Mem>
+  __device__ __forceinline__ static void run(const EpiProgram &P, const float (&acc)[C], const Mem &mem) {
+    float r[kRegs][C] = {};
+    run_static_from<SP, 0, C>(r, acc, mem, P.scalars);
+  }
+};
 
 }  // namespace ge

@@ -8,9 +8,10 @@
 //               tcgen05.mma (fp16/bf16 -> fp32) into one of two TMEM
 //               accumulators; tcgen05.commit frees ring stages and publishes
 //               finished accumulators.
-//   warps 2-5   epilogue: tcgen05.ld of 16-column chunks, aux tensors staged
-//               per warp by TMA (prefetched ahead, across tiles), the DAG
-//               program in fp32, rounding, TMA stores from swizzled staging.
+//   warps 2-5   epilogue: tcgen05.ld of 32-column steps, aux tensors staged
+//               per warp by TMA (prefetched ahead, across tiles), the epilogue
+//               program in fp32 (interpreted, or straight-line for catalog
+//               entries), rounding, TMA stores from swizzled staging.
 // The two TMEM accumulators let the epilogue of tile i overlap the mainloop of
 // tile i+1.  Ragged M/N/K edges are handled by TMA: out-of-range loads read
 // zeros, out-of-range stores are dropped.
@@ -39,7 +40,7 @@ struct TileCfg {
   static constexpr int kABytes = BM * BK * 2;      // one A stage
   static constexpr int kBBytes = kBnLocal * BK * 2;
   static constexpr int kBAtoms = kBnLocal / 64;    // 64-column swizzle atoms of B
-  static constexpr int kChunks = BN / CH;
+  static constexpr int kSteps = BN / EW;          // epilogue steps per tile
   static constexpr int kTmemCols = 2 * BN;         // two accumulators
   static_assert(kBnLocal % 64 == 0, "B half-tile must be whole 128-byte atoms");
   static_assert(kTmemCols == 128 || kTmemCols == 256 || kTmemCols == 512, "TMEM alloc size");
@@ -114,26 +115,29 @@ struct Waiter {
 };
 
 // Epilogue leaves and stores for the fused kernel: aux tensors and outputs
-// live in this warp's swizzled TMA staging boxes (row = lane), broadcast
-// vectors are read from global memory (the same addresses for every lane).
+// live in this warp's swizzled TMA staging boxes (row = lane, `half` picks the
+// 16-column half of the 32-column box), broadcast vectors are read from
+// global memory (the same addresses for every lane).
 struct FusedMem {
   const KParams *p;
   const uint8_t *aux_stage;
   uint8_t *out_stage;
-  int row;
-  int col0;
+  int row, half, col0;
+  template <int DT>
   __device__ __forceinline__ void aux(uint32_t i, float (&t)[CH]) const {
-    box_load(aux_stage + p->aux_off[i], p->prog.tma_aux_dtype[i], row, t);
+    box_load<DT>(aux_stage + p->aux_off[i], row, half, t);
   }
+  template <int DT>
   __device__ __forceinline__ void bcast(uint32_t i, float (&t)[CH]) const {
-    row_load(p->bcast_ptr[i], p->prog.bcast_dtype[i], col0, p->N, t);
+    row_load<DT, CH>(p->bcast_ptr[i], col0, p->N, t);
   }
+  template <int DT>
   __device__ __forceinline__ void store(uint32_t o, const float (&t)[CH]) const {
-    box_store(out_stage + p->out_off[o], p->prog.out_dtype[o], row, t);
+    box_store<DT>(out_stage + p->out_off[o], row, half, t);
   }
 };
 
-template <int CG, int BN>
+template <int CG, int BN, class Epi>
 __global__ void __launch_bounds__(kThreads, 1) gemm_epi_kernel(const __grid_constant__ KParams p) {
   using T = TileCfg<CG, BN>;
   extern __shared__ uint8_t smem_raw[];
@@ -315,25 +319,30 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_epi_kernel(const __grid_cons
     const uint32_t auxbar_w = bar_aux + 8u * e * kMaxAuxStages;
     const bool has_aux = p.prog.n_tma_aux > 0;
     const int SA = p.aux_stages;
-    const int total = my_tiles * T::kChunks;
+    const int total = my_tiles * T::kSteps;
     int issued = 0, g = 0, abuf = 0, obuf = 0;
     uint32_t aphase = 0;
     bool ok = true;
+    int pf_tile = -1, pf_x0 = 0, pf_y = 0, pf_l = 0;  // prefetch: coordinates of tile pf_tile
 
-    // TMA loads of every Load tensor for this warp's 32 rows of chunk gi
+    // TMA loads of every Load tensor for this warp's 32 rows of step gi
     auto issue_aux = [&](int gi) {
-      const int ii = gi / T::kChunks, cc = gi - ii * T::kChunks;
-      int l2, mb2, nb2;
-      tile_coords(p, unit + ii * n_units, l2, mb2, nb2);
+      const int ii = gi / T::kSteps;
+      if (ii != pf_tile) {
+        int mb2, nb2;
+        tile_coords(p, unit + ii * n_units, pf_l, mb2, nb2);
+        pf_tile = ii;
+        pf_x0 = nb2 * BN;
+        pf_y = mb2 * T::kMmaM + static_cast<int>(rank) * BM + q * 32;
+      }
       const int as = gi % SA;
       const uint32_t ab = auxbar_w + 8u * as;
       uint8_t *dst = aux_w + as * p.aux_stage_bytes;
       fence_proxy_async_smem();
       mbar_arrive_expect_tx(ab, p.aux_tx_bytes);
-      const int x = nb2 * BN + cc * CH;
-      const int y = mb2 * T::kMmaM + static_cast<int>(rank) * BM + q * 32;
+      const int x = pf_x0 + (gi - ii * T::kSteps) * EW;
       for (int a = 0; a < p.prog.n_tma_aux; ++a)
-        tma_load_3d(smem_u32(dst + p.aux_off[a]), &p.tmAux[a], ab, x, y, l2);
+        tma_load_3d(smem_u32(dst + p.aux_off[a]), &p.tmAux[a], ab, x, pf_y, pf_l);
     };
 
     for (int i = 0; ok && i < my_tiles; ++i) {
@@ -352,15 +361,17 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_epi_kernel(const __grid_cons
         break;
       }
       tc_fence_after();
-      for (int c = 0; c < T::kChunks; ++c, ++g) {
+      for (int s = 0; s < T::kSteps; ++s, ++g) {
         if (has_aux && lane == 0) {
           while (issued < total && issued < g + SA) issue_aux(issued++);
         }
         __syncwarp();
-        float acc[CH];
-        tmem_ld16(tq + static_cast<uint32_t>(abuf * BN + c * CH), acc);
+        float acc0[CH], acc1[CH];
+        const uint32_t col = static_cast<uint32_t>(abuf * BN + s * EW);
+        tmem_ld16(tq + col, acc0);
+        tmem_ld16(tq + col + CH, acc1);
         tmem_wait_ld();
-        if (c == T::kChunks - 1) {
+        if (s == T::kSteps - 1) {
           // accumulator fully read: hand it back to the MMA warp
           tc_fence_before();
           __syncwarp();
@@ -378,17 +389,19 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_epi_kernel(const __grid_cons
             break;
           }
         }
-        // the staging buffer written two chunks ago has been read by its store
+        // the staging buffer written two steps ago has been read by its store
         if (lane == 0) bulk_wait_group_read<1>();
         __syncwarp();
         uint8_t *ostage = out_w + obuf * p.out_stage_bytes;
-        FusedMem mem{&p, aux_w + (g % SA) * p.aux_stage_bytes, ostage, lane, n0 + c * CH};
-        run_program(p.prog, acc, mem);
+        const uint8_t *astage = aux_w + (g % SA) * p.aux_stage_bytes;
+        const int c0 = n0 + s * EW;
+        Epi::template run<CH>(p.prog, acc0, FusedMem{&p, astage, ostage, lane, 0, c0});
+        Epi::template run<CH>(p.prog, acc1, FusedMem{&p, astage, ostage, lane, 1, c0 + CH});
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) {
           for (int o = 0; o < p.prog.n_out; ++o)
-            tma_store_3d(&p.tmOut[o], smem_u32(ostage + p.out_off[o]), n0 + c * CH, m0, l);
+            tma_store_3d(&p.tmOut[o], smem_u32(ostage + p.out_off[o]), c0, m0, l);
           bulk_commit_group();
         }
         obuf ^= 1;

@@ -1,4 +1,8 @@
-// launch.h -- host-side entry points of the kernel translation units.
+// launch.h -- kernel handles exported by the kernel translation units.
+//
+// Every handle is a __global__ function usable with cudaFuncSetAttribute and
+// cudaLaunchKernelExC.  `epi` selects the epilogue executor: -1 the
+// interpreter, k >= 0 the straight-line kernel of catalog entry k.
 #pragma once
 
 #include <cuda_runtime_api.h>
@@ -7,23 +11,16 @@
 
 namespace ge {
 
-// GEMM + fused epilogue kernel, instantiated for (cta_group, BN) in
-// {(1, 64), (1, 128), (1, 256), (2, 128), (2, 256)}.
-bool gemm_variant_exists(int cg, int bn);
-cudaError_t gemm_prepare(int cg, int bn, int smem_bytes);  // opt in to the dynamic smem size
-cudaError_t gemm_launch(int cg, int bn, const KParams &p, int grid, int smem_bytes,
-                        cudaStream_t stream);
-cudaError_t gemm_max_active_clusters(int cg, int bn, int smem_bytes, int *clusters);
-
-// per-translation-unit halves of the above
-cudaError_t gemm_prepare_cg1(int bn, int smem_bytes);
-cudaError_t gemm_launch_cg1(int bn, const KParams &p, int grid, int smem_bytes, cudaStream_t s);
-cudaError_t gemm_prepare_cg2(int bn, int smem_bytes);
-cudaError_t gemm_launch_cg2(int bn, const KParams &p, int grid, int smem_bytes, cudaStream_t s);
-cudaError_t gemm_max_active_clusters_cg2(int bn, int smem_bytes, int *clusters);
+// fused GEMM + epilogue, (cta_group, BN) in {(1,64), (1,128), (1,256), (2,128), (2,256)}
+const void *gemm_kernel_cg1_n64(int epi);
+const void *gemm_kernel_cg1_n128(int epi);
+const void *gemm_kernel_cg1_n256(int epi);
+const void *gemm_kernel_cg2_n128(int epi);
+const void *gemm_kernel_cg2_n256(int epi);
 
 // unfused comparison path: elementwise epilogue over an fp32 accumulator
-cudaError_t ew_launch(const EwParams &p, int grid, cudaStream_t stream);
+const void *ew_kernel(int epi);
 constexpr int kEwThreads = 256;
+constexpr int kEwCols = 8;  // columns per thread
 
 }  // namespace ge

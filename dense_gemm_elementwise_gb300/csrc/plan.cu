@@ -14,8 +14,10 @@
 #include <mutex>
 #include <new>
 
+#include "catalog.cuh"
 #include "common.cuh"
 #include "launch.h"
+#include "program.cuh"
 
 using namespace ge;
 
@@ -92,139 +94,19 @@ int validate_impl(const ge_dtypes *dt, const ge_dag *dag) {
   return GE_OK;
 }
 
-// -------------------------------------------------------------- compiler --
-// Greedy register allocation in node order.  Leaves are never copied into a
-// register unless an operation needs a destination for them; an operation
-// reuses an operand's register in place when this is the operand's last use.
-int compile_dag(const ge_dtypes *dt, const ge_dag *dag, EpiProgram *P) {
-  std::memset(P, 0, sizeof(*P));
-  const int n = dag->n;
-  int last_use[GE_MAX_NODES];
-  for (int i = 0; i < n; ++i) last_use[i] = -1;
-  for (int i = 0; i < n; ++i) {
-    const ge_node &nd = dag->node[i];
-    if (nd.op == GE_MUL || nd.op == GE_ADD) {
-      last_use[nd.a] = i;
-      last_use[nd.b] = i;
-    } else if (nd.op == GE_RELU || nd.op == GE_STORE) {
-      last_use[nd.a] = i;
-    }
-  }
-  int tma_of_slot[GE_MAX_AUX], bc_of_slot[GE_MAX_AUX];
-  for (int s = 0; s < GE_MAX_AUX; ++s) tma_of_slot[s] = bc_of_slot[s] = -1;
-  struct Loc {
-    uint32_t src, idx;
-  } loc[GE_MAX_NODES];
-  bool busy[kRegs] = {false, false, false, false};
-  int max_regs = 0;
-  bool overflow = false;
-
-  auto emit = [&](uint32_t op, uint32_t dst, Loc s) {
-    if (P->n_ins >= kMaxIns) {
-      overflow = true;
-      return;
-    }
-    P->ins[P->n_ins++] = pack_ins(op, dst, s.src, s.idx);
-  };
-  auto alloc = [&]() -> int {
-    for (int r = 0; r < kRegs; ++r)
-      if (!busy[r]) {
-        busy[r] = true;
-        max_regs = std::max(max_regs, r + 1);
-        return r;
-      }
+// catalog entry whose program equals P, or -1
+template <int K = 0>
+int match_catalog(const EpiProgram &P) {
+  if constexpr (K < catalog::kCount) {
+    if (same_program(P, catalog::Prog<K>::P)) return K;
+    return match_catalog<K + 1>(P);
+  } else {
     return -1;
-  };
-  auto in_reg_dying = [&](int ref, int at) { return loc[ref].src == SRC_REG && last_use[ref] == at; };
-
-  for (int i = 0; i < n; ++i) {
-    const ge_node &nd = dag->node[i];
-    switch (nd.op) {
-      case GE_ACCFETCH: loc[i] = {SRC_ACC, 0}; break;
-      case GE_LOAD: {
-        int &t = tma_of_slot[nd.slot];
-        if (t < 0) {
-          if (P->n_tma_aux >= GE_MAX_TMA_AUX) return GE_ERR_UNSUPPORTED;
-          t = P->n_tma_aux++;
-          P->tma_aux_slot[t] = nd.slot;
-          P->tma_aux_dtype[t] = dt->aux[nd.slot];
-        }
-        loc[i] = {SRC_AUX, static_cast<uint32_t>(t)};
-        break;
-      }
-      case GE_BROADCAST: {
-        int &b = bc_of_slot[nd.slot];
-        if (b < 0) {
-          b = P->n_bcast++;
-          P->bcast_slot[b] = nd.slot;
-          P->bcast_dtype[b] = dt->aux[nd.slot];
-        }
-        loc[i] = {SRC_BCAST, static_cast<uint32_t>(b)};
-        break;
-      }
-      case GE_SCALAR: loc[i] = {SRC_SCALAR, static_cast<uint32_t>(nd.slot)}; break;
-      case GE_MUL:
-      case GE_ADD: {
-        const uint32_t op = nd.op == GE_MUL ? OP_MUL : OP_ADD;
-        int d, other;
-        if (in_reg_dying(nd.a, i)) {
-          d = static_cast<int>(loc[nd.a].idx);
-          other = nd.b;
-        } else if (in_reg_dying(nd.b, i)) {
-          d = static_cast<int>(loc[nd.b].idx);
-          other = nd.a;
-        } else {
-          d = alloc();
-          if (d < 0) return GE_ERR_UNSUPPORTED;
-          emit(OP_MOV, d, loc[nd.a]);
-          other = nd.b;
-        }
-        emit(op, d, loc[other]);
-        // free operand registers whose last use this was (other than d)
-        for (int ref : {nd.a, nd.b})
-          if (loc[ref].src == SRC_REG && last_use[ref] == i && static_cast<int>(loc[ref].idx) != d)
-            busy[loc[ref].idx] = false;
-        loc[i] = {SRC_REG, static_cast<uint32_t>(d)};
-        if (last_use[i] < 0) busy[d] = false;  // dead value
-        break;
-      }
-      case GE_RELU: {
-        int d;
-        if (in_reg_dying(nd.a, i)) {
-          d = static_cast<int>(loc[nd.a].idx);
-        } else {
-          d = alloc();
-          if (d < 0) return GE_ERR_UNSUPPORTED;
-          emit(OP_MOV, d, loc[nd.a]);
-        }
-        emit(OP_RELU, d, Loc{SRC_NONE, 0});
-        loc[i] = {SRC_REG, static_cast<uint32_t>(d)};
-        if (last_use[i] < 0) busy[d] = false;
-        break;
-      }
-      case GE_STORE: {
-        emit(OP_STORE, static_cast<uint32_t>(nd.slot), loc[nd.a]);
-        if (loc[nd.a].src == SRC_REG && last_use[nd.a] == i) busy[loc[nd.a].idx] = false;
-        break;
-      }
-      default: return GE_ERR_UNSUPPORTED;
-    }
-    if (overflow) return GE_ERR_UNSUPPORTED;
   }
-  P->n_out = dt->n_out;
-  for (int o = 0; o < dt->n_out; ++o) P->out_dtype[o] = dt->out[o];
-  P->n_regs = max_regs;
-  return GE_OK;
 }
 
 // accumulator-only program of the unfused path's GEMM: out 0 (fp32) = accum
-void program_store_accum(EpiProgram *P) {
-  std::memset(P, 0, sizeof(*P));
-  P->n_ins = 1;
-  P->ins[0] = pack_ins(OP_STORE, 0, SRC_ACC, 0);
-  P->n_out = 1;
-  P->out_dtype[0] = GE_F32;
-}
+EpiProgram program_store_accum() { return catalog::Prog<0>::P; }
 
 // ---------------------------------------------------------- TMA encoding --
 typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
@@ -265,8 +147,9 @@ bool encode3d(CUtensorMap *m, int dt, const void *ptr, uint64_t d0, uint64_t d1,
             CU_TENSOR_MAP_INTERLEAVE_NONE, sw, l2, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// EW-column boxes: 16-bit rows are 64 bytes, fp32 rows 128 bytes
 CUtensorMapSwizzle epi_swizzle(int dt) {
-  return dt == GE_F32 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_32B;
+  return dt == GE_F32 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
 }
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -294,29 +177,29 @@ int make_layout(Layout *Lo, int cg, int bn, int want_stages, const EpiProgram &P
   uint32_t aux_stage = 0, out_stage = 0;
   for (int t = 0; t < P.n_tma_aux; ++t) {
     Lo->aux_off[t] = aux_stage;
-    aux_stage += 32u * CH * esize(P.tma_aux_dtype[t]);
+    aux_stage += 32u * EW * esize(P.tma_aux_dtype[t]);
   }
   for (int o = 0; o < P.n_out; ++o) {
     Lo->out_off[o] = out_stage;
-    out_stage += 32u * CH * esize(P.out_dtype[o]);
+    out_stage += 32u * EW * esize(P.out_dtype[o]);
   }
-  auto fits = [&](int sa, int *stages_out) {
+  auto stages_with = [&](int sa) {
     const int64_t epi = int64_t(kEpiWarps) * sa * aux_stage + int64_t(kEpiWarps) * 2 * out_stage;
     const int64_t room = int64_t(max_smem) - kAlignSlack - kBarBlock - epi;
-    int s = room > 0 ? static_cast<int>(room / (a_bytes + b_bytes)) : 0;
-    s = std::min(s, kMaxStages);
-    *stages_out = s;
+    const int s = room > 0 ? static_cast<int>(room / (a_bytes + b_bytes)) : 0;
+    return std::min(s, kMaxStages);
   };
-  int sa = P.n_tma_aux > 0 ? kMaxAuxStages : 1;
-  int stages = 0;
-  fits(sa, &stages);
-  if (P.n_tma_aux > 0 && stages < 4) {
-    int s2 = 0;
-    fits(2, &s2);
-    if (s2 > stages) {
-      sa = 2;
-      stages = s2;
-    }
+  // deepest aux prefetch that still leaves at least 5 mainloop stages
+  int sa = 1, stages = stages_with(1);
+  if (P.n_tma_aux > 0) {
+    sa = 2;
+    stages = stages_with(2);
+    for (int cand = kMaxAuxStages; cand > 2; --cand)
+      if (stages_with(cand) >= 5) {
+        sa = cand;
+        stages = stages_with(cand);
+        break;
+      }
   }
   if (want_stages > 0) {
     if (want_stages > stages || want_stages > kMaxStages) return GE_ERR_SMEM;
@@ -355,6 +238,7 @@ struct gemm_epi_plan {
   int device = 0, num_sms = 0, max_smem = 0;
   uint32_t *status = nullptr;
   EpiProgram prog{}, prog_acc{};
+  int epi = -1, epi_acc = -1;  // catalog entries (-1: interpreter)
   Layout lay, lay_acc;
   KParams kp{}, kp_acc{};
   // pointers the cached tensor maps were encoded for
@@ -369,8 +253,41 @@ struct gemm_epi_plan {
 
 namespace {
 
-bool variant_exists(int cg, int bn) {
-  return (cg == 1 && (bn == 64 || bn == 128 || bn == 256)) || (cg == 2 && (bn == 128 || bn == 256));
+const void *gemm_kernel(int cg, int bn, int epi) {
+  if (cg == 1 && bn == 64) return gemm_kernel_cg1_n64(epi);
+  if (cg == 1 && bn == 128) return gemm_kernel_cg1_n128(epi);
+  if (cg == 1 && bn == 256) return gemm_kernel_cg1_n256(epi);
+  if (cg == 2 && bn == 128) return gemm_kernel_cg2_n128(epi);
+  if (cg == 2 && bn == 256) return gemm_kernel_cg2_n256(epi);
+  return nullptr;
+}
+
+cudaLaunchConfig_t launch_config(const Layout &Lo, cudaStream_t s, cudaLaunchAttribute *attr) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(Lo.grid));
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = static_cast<size_t>(Lo.smem);
+  cfg.stream = s;
+  cfg.attrs = nullptr;
+  cfg.numAttrs = 0;
+  if (Lo.cg == 2) {
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+  }
+  return cfg;
+}
+
+cudaError_t launch_gemm(const Layout &Lo, int epi, const KParams &kp, cudaStream_t s) {
+  const void *fn = gemm_kernel(Lo.cg, Lo.bn, epi);
+  if (!fn) return cudaErrorInvalidDeviceFunction;
+  cudaLaunchAttribute attr[1];
+  cudaLaunchConfig_t cfg = launch_config(Lo, s, attr);
+  void *args[] = {const_cast<KParams *>(&kp)};
+  return cudaLaunchKernelExC(&cfg, fn, args);
 }
 
 // Rough cost model in SM clocks: waves x per-tile mainloop, where a k-block
@@ -430,15 +347,21 @@ int configure(gemm_epi_plan *pl) {
     int sms = pl->num_sms;
     if (o.max_ctas) sms = std::min(sms, o.max_ctas);
     int units = std::max(1, sms / cg);
+    const void *fn = gemm_kernel(cg, bn, Lo == &pl->lay ? pl->epi : pl->epi_acc);
+    if (!fn) return GE_ERR_INVALID;
+    if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, Lo->smem) != cudaSuccess)
+      return GE_ERR_CUDA;
     if (cg == 2) {
       int clusters = 0;
-      if (gemm_prepare(cg, bn, Lo->smem) != cudaSuccess) return GE_ERR_CUDA;
-      if (gemm_max_active_clusters(cg, bn, Lo->smem, &clusters) == cudaSuccess && clusters > 0)
+      cudaLaunchAttribute attr[1];
+      cudaLaunchConfig_t cfg = launch_config(*Lo, nullptr, attr);
+      cfg.gridDim = dim3(2);
+      if (cudaOccupancyMaxActiveClusters(&clusters, fn, &cfg) == cudaSuccess && clusters > 0)
         units = std::min(units, clusters);
+      cudaGetLastError();
     }
     units = static_cast<int>(std::min<int64_t>(units, tiles));
     Lo->grid = units * cg;
-    if (gemm_prepare(cg, bn, Lo->smem) != cudaSuccess) return GE_ERR_CUDA;
   }
   return GE_OK;
 }
@@ -489,7 +412,7 @@ bool encode_operands(const gemm_epi_plan *pl, KParams *kp, const void *A, const 
 }
 
 bool encode_epilogue_map(const gemm_epi_plan *pl, CUtensorMap *m, int dt, const void *ptr) {
-  return encode3d(m, dt, ptr, pl->N, pl->M, pl->L, CH, 32, epi_swizzle(dt),
+  return encode3d(m, dt, ptr, pl->N, pl->M, pl->L, EW, 32, epi_swizzle(dt),
                   CU_TENSOR_MAP_L2_PROMOTION_L2_128B);
 }
 
@@ -539,36 +462,22 @@ void log_plan(const gemm_epi_plan *pl) {
   const Layout &Lo = pl->lay;
   std::fprintf(stderr,
                "[gemm_epi] L=%lld M=%lld N=%lld K=%lld: cta_group=%d tile=%dx%dx%d stages=%d "
-               "aux_stages=%d grid=%d tiles=%d smem=%d program=%d ins/%d regs\n",
+               "aux_stages=%d grid=%d tiles=%d smem=%d program=%d ins/%d regs epilogue=%s\n",
                (long long)pl->L, (long long)pl->M, (long long)pl->N, (long long)pl->K, Lo.cg,
                BM * Lo.cg, Lo.bn, BK, Lo.stages, Lo.aux_stages, Lo.grid, Lo.num_tiles, Lo.smem_used,
-               pl->prog.n_ins, pl->prog.n_regs);
+               pl->prog.n_ins, pl->prog.n_regs,
+               pl->epi >= 0 ? catalog::kEntries[pl->epi].name : "interpreter");
 }
 
 }  // namespace
 
 // ------------------------------------------------------------- C ABI --
-namespace ge {
-bool gemm_variant_exists(int cg, int bn) { return variant_exists(cg, bn); }
-cudaError_t gemm_prepare(int cg, int bn, int smem) {
-  return cg == 2 ? gemm_prepare_cg2(bn, smem) : gemm_prepare_cg1(bn, smem);
-}
-cudaError_t gemm_launch(int cg, int bn, const KParams &p, int grid, int smem, cudaStream_t s) {
-  return cg == 2 ? gemm_launch_cg2(bn, p, grid, smem, s) : gemm_launch_cg1(bn, p, grid, smem, s);
-}
-cudaError_t gemm_max_active_clusters(int cg, int bn, int smem, int *n) {
-  if (cg != 2) return cudaErrorInvalidValue;
-  return gemm_max_active_clusters_cg2(bn, smem, n);
-}
-}  // namespace ge
-
 extern "C" {
 
 int gemm_epi_validate(const ge_dtypes *dtypes, const ge_dag *dag) {
   int st = validate_impl(dtypes, dag);
   if (st != GE_OK) return st;
-  EpiProgram P;
-  return compile_dag(dtypes, dag, &P);
+  return compile_program(*dtypes, *dag).status;
 }
 
 int gemm_epi_plan_create_ex(gemm_epi_plan **plan, int64_t L, int64_t M, int64_t N, int64_t K,
@@ -597,9 +506,16 @@ int gemm_epi_plan_create_ex(gemm_epi_plan **plan, int64_t L, int64_t M, int64_t 
   pl->dt = *dtypes;
   pl->dag = *dag;
   if (opts) pl->opt = *opts;
-  st = compile_dag(dtypes, dag, &pl->prog);
+  {
+    const CompileResult cr = compile_program(*dtypes, *dag);
+    st = cr.status;
+    pl->prog = cr.prog;
+  }
   if (st == GE_OK) {
-    program_store_accum(&pl->prog_acc);
+    pl->prog_acc = program_store_accum();
+    const bool interp = (pl->opt.debug_flags & GE_DEBUG_FORCE_INTERPRETER) != 0u;
+    pl->epi = interp ? -1 : match_catalog(pl->prog);
+    pl->epi_acc = interp ? -1 : match_catalog(pl->prog_acc);
     st = check_device(&pl->device, &pl->num_sms, &pl->max_smem);
   }
   if (st == GE_OK) {
@@ -643,6 +559,7 @@ int gemm_epi_plan_info(const gemm_epi_plan *pl, ge_plan_info *info) {
   info->n_instr = pl->prog.n_ins;
   info->n_regs = pl->prog.n_regs;
   info->num_sms = pl->num_sms;
+  info->epi_variant = pl->epi;
   return GE_OK;
 }
 
@@ -673,8 +590,7 @@ int gemm_epi_run(gemm_epi_plan *pl, const void *A, const void *B, const void *co
   }
   for (int b = 0; b < P.n_bcast; ++b) kp.bcast_ptr[b] = aux[P.bcast_slot[b]];
   for (int s = 0; s < pl->dt.n_scalar; ++s) kp.prog.scalars[s] = scalars[s];
-  const cudaError_t e = gemm_launch(pl->lay.cg, pl->lay.bn, kp, pl->lay.grid, pl->lay.smem,
-                                    static_cast<cudaStream_t>(stream));
+  const cudaError_t e = launch_gemm(pl->lay, pl->epi, kp, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? GE_OK : GE_ERR_CUDA;
 }
 
@@ -703,8 +619,7 @@ int gemm_epi_run_unfused(gemm_epi_plan *pl, const void *A, const void *B, const 
     pl->aWs = workspace;
     pl->acc_maps_ok = true;
   }
-  cudaError_t e = gemm_launch(pl->lay_acc.cg, pl->lay_acc.bn, ka, pl->lay_acc.grid,
-                              pl->lay_acc.smem, s);
+  cudaError_t e = launch_gemm(pl->lay_acc, pl->epi_acc, ka, s);
   if (e != cudaSuccess) return GE_ERR_CUDA;
   // launch 2: the epilogue program, elementwise
   EwParams ep;
@@ -718,11 +633,16 @@ int gemm_epi_run_unfused(gemm_epi_plan *pl, const void *A, const void *B, const 
   for (int i = 0; i < pl->dt.n_scalar; ++i) ep.prog.scalars[i] = scalars[i];
   ep.rows = pl->L * pl->M;
   ep.N = static_cast<int32_t>(pl->N);
-  ep.chunks_per_row = static_cast<int32_t>((pl->N + CH - 1) / CH);
+  ep.chunks_per_row = static_cast<int32_t>((pl->N + kEwCols - 1) / kEwCols);
   const int64_t units = ep.rows * ep.chunks_per_row;
   const int64_t blocks = (units + kEwThreads - 1) / kEwThreads;
   const int grid = static_cast<int>(std::min<int64_t>(blocks, int64_t(pl->num_sms) * 16));
-  e = ew_launch(ep, std::max(grid, 1), s);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(std::max(grid, 1)));
+  cfg.blockDim = dim3(kEwThreads);
+  cfg.stream = s;
+  void *args[] = {&ep};
+  e = cudaLaunchKernelExC(&cfg, ew_kernel(pl->epi), args);
   return e == cudaSuccess ? GE_OK : GE_ERR_CUDA;
 }
 

@@ -1,34 +1,38 @@
-// unfused.cu -- the unfused comparison path's second kernel: a vectorised,
-// grid-stride elementwise pass that reads the fp32 accumulator the GEMM wrote
-// to a workspace, evaluates the same compiled epilogue program as the fused
-// kernel, and writes the outputs.  One thread handles CH consecutive columns
-// of one row; consecutive threads take consecutive column chunks.
+// unfused.cu -- the unfused comparison path's second kernel: a grid-stride
+// elementwise pass that reads the fp32 accumulator the GEMM wrote to a
+// workspace, evaluates the same compiled epilogue program as the fused kernel
+// (interpreter or catalog executor), and writes the outputs.  One thread
+// handles 8 consecutive columns of one row (16-byte accesses); consecutive
+// threads take consecutive column groups, so every warp access is contiguous.
+#include <utility>
+
+#include "catalog.cuh"
 #include "epilogue.cuh"
 #include "launch.h"
 
 namespace ge {
 
-static __device__ __forceinline__ int esize(int dtype) { return dtype == GE_F32 ? 4 : 2; }
-
 struct GlobalMem {
   const EwParams *p;
   int64_t row;
   int col0;
-  __device__ __forceinline__ void aux(uint32_t i, float (&t)[CH]) const {
-    const int dt = p->prog.tma_aux_dtype[i];
-    const char *base = static_cast<const char *>(p->aux_ptr[i]) + row * p->N * esize(dt);
-    row_load(base, dt, col0, p->N, t);
+  template <int DT>
+  __device__ __forceinline__ void aux(uint32_t i, float (&t)[kEwCols]) const {
+    const char *base = static_cast<const char *>(p->aux_ptr[i]) + row * p->N * (DT == GE_F32 ? 4 : 2);
+    row_load<DT, kEwCols>(base, col0, p->N, t);
   }
-  __device__ __forceinline__ void bcast(uint32_t i, float (&t)[CH]) const {
-    row_load(p->bcast_ptr[i], p->prog.bcast_dtype[i], col0, p->N, t);
+  template <int DT>
+  __device__ __forceinline__ void bcast(uint32_t i, float (&t)[kEwCols]) const {
+    row_load<DT, kEwCols>(p->bcast_ptr[i], col0, p->N, t);
   }
-  __device__ __forceinline__ void store(uint32_t o, const float (&t)[CH]) const {
-    const int dt = p->prog.out_dtype[o];
-    char *base = static_cast<char *>(p->out_ptr[o]) + row * p->N * esize(dt);
-    row_store(base, dt, col0, p->N, t);
+  template <int DT>
+  __device__ __forceinline__ void store(uint32_t o, const float (&t)[kEwCols]) const {
+    char *base = static_cast<char *>(p->out_ptr[o]) + row * p->N * (DT == GE_F32 ? 4 : 2);
+    row_store<DT, kEwCols>(base, col0, p->N, t);
   }
 };
 
+template <class Epi>
 __global__ void __launch_bounds__(kEwThreads) epilogue_elementwise_kernel(
     const __grid_constant__ EwParams p) {
   const int64_t units = p.rows * p.chunks_per_row;
@@ -36,17 +40,21 @@ __global__ void __launch_bounds__(kEwThreads) epilogue_elementwise_kernel(
   for (int64_t u = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; u < units;
        u += stride) {
     const int64_t row = u / p.chunks_per_row;
-    const int col0 = static_cast<int>(u - row * p.chunks_per_row) * CH;
-    float acc[CH];
-    row_load(p.acc + row * p.N, GE_F32, col0, p.N, acc);
-    GlobalMem mem{&p, row, col0};
-    run_program(p.prog, acc, mem);
+    const int col0 = static_cast<int>(u - row * p.chunks_per_row) * kEwCols;
+    float acc[kEwCols];
+    row_load<GE_F32, kEwCols>(p.acc + row * p.N, col0, p.N, acc);
+    Epi::template run<kEwCols>(p.prog, acc, GlobalMem{&p, row, col0});
   }
 }
 
-cudaError_t ew_launch(const EwParams &p, int grid, cudaStream_t stream) {
-  epilogue_elementwise_kernel<<<grid, kEwThreads, 0, stream>>>(p);
-  return cudaGetLastError();
+template <size_t... K>
+static const void *pick_ew(int epi, std::index_sequence<K...>) {
+  static const void *const table[] = {reinterpret_cast<const void *>(
+      &epilogue_elementwise_kernel<EpiStatic<catalog::Prog<K>>>)...};
+  if (epi < 0) return reinterpret_cast<const void *>(&epilogue_elementwise_kernel<EpiInterp>);
+  return epi < static_cast<int>(sizeof...(K)) ? table[epi] : nullptr;
 }
+
+const void *ew_kernel(int epi) { return pick_ew(epi, std::make_index_sequence<catalog::kCount>{}); }
 
 }  // namespace ge

@@ -108,6 +108,11 @@ typedef struct {
  * Nothing faults or hangs: every wait in the kernel is bounded. */
 #define GE_DEBUG_SKIP_FIRST_LOAD 1u
 
+/* Run the epilogue through the general interpreter even when the DAG matches
+ * a built-in (precompiled, straight-line) epilogue.  Results are identical;
+ * used to test that the two executors agree. */
+#define GE_DEBUG_FORCE_INTERPRETER 2u
+
 /* What a plan chose (for logs, tests and the benchmark). */
 typedef struct {
   int32_t cta_group, tile_m, tile_n, tile_k;  /* tile_m/tile_n: output tile of one MMA */
@@ -115,6 +120,7 @@ typedef struct {
   int32_t grid, num_tiles, smem_bytes;
   int32_t n_instr, n_regs;                    /* compiled epilogue program             */
   int32_t num_sms;
+  int32_t epi_variant;                        /* built-in epilogue used, -1: interpreter */
 } ge_plan_info;
 
 typedef struct gemm_epi_plan gemm_epi_plan;

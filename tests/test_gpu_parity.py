@@ -179,3 +179,38 @@ def test_device_wait_timeout_is_reported():
         B.gemm_epi_plan_destroy(plan)
     gpu, _ = _gpu.run_gpu(w, inputs)
     _gpu.compare(w, gpu, _gpu.oracle_rows(w, inputs))
+
+
+# ------------------------------------------ catalog vs interpreter --
+
+def test_headline_workloads_use_builtin_epilogues():
+    for w in W.CONFIGS:
+        plan = B.gemm_epi_plan_create(w.L, w.M, w.N, w.K, _gpu.dtypes_of(w), B.make_dag(w.dag))
+        try:
+            info = B.gemm_epi_plan_info(plan)
+        finally:
+            B.gemm_epi_plan_destroy(plan)
+        assert info["epi_variant"] >= 0, w.name
+
+
+CATALOG_CASES = [small(W.CONFIGS[0], 2, 300, 392, 200), small(W.CONFIGS[2], 1, 264, 520, 136),
+                 small(W.CONFIGS[3], 1, 384, 264, 520), small(W.CONFIGS[4], 3, 200, 264, 200)] + \
+    [small(w, 2, 136, 264, 72) for w in W.page_examples()]
+
+
+@pytest.mark.parametrize("w", CATALOG_CASES, ids=lambda w: w.name)
+@pytest.mark.parametrize("variant", [(1, 64), (2, 256)], ids=lambda v: "cg%d_n%d" % v)
+def test_builtin_and_interpreter_agree_bitwise(w, variant):
+    """The straight-line kernels and the interpreter evaluate the same
+    compiled program in the same order: identical bits, fused and unfused."""
+    inputs = W.make_inputs(w)
+    base = dict(cta_group=variant[0], tile_n=variant[1])
+    fast, info = _gpu.run_gpu(w, inputs, options=B.ge_options(**base))
+    slow, info2 = _gpu.run_gpu(w, inputs, options=B.ge_options(
+        debug_flags=B.GE_DEBUG_FORCE_INTERPRETER, **base))
+    assert info2["epi_variant"] == -1
+    _gpu.bitwise_equal(fast, slow)
+    slow_unfused, _ = _gpu.run_gpu(w, inputs, unfused=True, options=B.ge_options(
+        debug_flags=B.GE_DEBUG_FORCE_INTERPRETER, **base))
+    _gpu.bitwise_equal(fast, slow_unfused)
+    _gpu.compare(w, fast, _gpu.oracle_rows(w, inputs))
