@@ -30,7 +30,9 @@ OP = {"accum": GE_ACCFETCH, "load": GE_LOAD, "scalar": GE_SCALAR, "broadcast": G
 # exported symbols of include/gemm_epi.h
 EXPORTS = ["gemm_epi_plan_create", "gemm_epi_plan_create_ex", "gemm_epi_validate", "gemm_epi_run",
            "gemm_epi_unfused_workspace_bytes", "gemm_epi_run_unfused", "gemm_epi_plan_destroy",
-           "gemm_epi_plan_info", "gemm_epi_status_string", "gemm_epi_last_error"]
+           "gemm_epi_plan_info", "gemm_epi_status_string", "gemm_epi_last_error",
+           "gemm_epi_run_unfused_noalloc"]
+GE_NOALLOC_SCRATCH_BYTES = 16 * 1024 * 1024
 
 
 class ge_node(ctypes.Structure):
@@ -96,6 +98,8 @@ def _load():
     L.gemm_epi_run_unfused.restype = ctypes.c_int
     L.gemm_epi_run_unfused.argtypes = [P, P, P, pp, ctypes.POINTER(ctypes.c_float), pp, P,
                                        ctypes.c_size_t, P]
+    L.gemm_epi_run_unfused_noalloc.restype = ctypes.c_int
+    L.gemm_epi_run_unfused_noalloc.argtypes = [P, P, P, pp, ctypes.POINTER(ctypes.c_float), pp, P]
     L.gemm_epi_plan_destroy.restype = None
     L.gemm_epi_plan_destroy.argtypes = [P]
     L.gemm_epi_plan_info.restype = ctypes.c_int
@@ -218,6 +222,16 @@ def gemm_epi_run_unfused(plan, A, B, aux, scalars, outs, workspace, workspace_by
                                   _stream(stream))
     if check and st != GE_OK:
         raise GemmEpiError(st, "gemm_epi_run_unfused")
+    return st
+
+
+def gemm_epi_run_unfused_noalloc(plan, A, B, aux, scalars, outs, stream=None, check=True):
+    """The unfused path on the library's built-in workspace: for callers that
+    cannot allocate device memory themselves (see include/gemm_epi.h)."""
+    st = lib.gemm_epi_run_unfused_noalloc(plan, _addr(A), _addr(B), _ptr_array(aux),
+                                          _scalars(scalars), _ptr_array(outs), _stream(stream))
+    if check and st != GE_OK:
+        raise GemmEpiError(st, "gemm_epi_run_unfused_noalloc")
     return st
 
 

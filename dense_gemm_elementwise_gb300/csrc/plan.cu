@@ -687,3 +687,46 @@ int gemm_epi_last_error(gemm_epi_plan *plan) {
 }
 
 }  // extern "C"
+
+// ------------------------------------------------- allocation-free variant --
+// The workspace of gemm_epi_run_unfused_noalloc: part of the library image, so
+// every device that loads it holds these GE_NOALLOC_SCRATCH_BYTES until exit.
+// In host code the name is only a stand-in for the symbol; the device address
+// comes from cudaGetSymbolAddress, looked up once per device.
+static __device__ __align__(256) float g_noalloc_scratch[GE_NOALLOC_SCRATCH_BYTES / sizeof(float)];
+
+namespace {
+constexpr int kMaxDevices = 128;
+std::mutex g_noalloc_mutex;
+void *g_noalloc_ptr[kMaxDevices] = {};
+}  // namespace
+
+extern "C" int gemm_epi_run_unfused_noalloc(gemm_epi_plan *pl, const void *A, const void *B,
+                                            const void *const *aux, const float *scalars,
+                                            void *const *outs, void *stream) {
+  if (!pl) return GE_ERR_INVALID;
+  if (gemm_epi_unfused_workspace_bytes(pl) > GE_NOALLOC_SCRATCH_BYTES) return GE_ERR_WORKSPACE;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    cudaGetLastError();
+    return GE_ERR_CUDA;
+  }
+  void *scratch = nullptr;
+  {
+    std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+    if (!g_noalloc_ptr[dev]) {
+      // first call on this device (which is current): find the array's address
+      void *p = nullptr;
+      if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) {
+        cudaGetLastError();
+        return GE_ERR_CUDA;
+      }
+      g_noalloc_ptr[dev] = p;
+    }
+    scratch = g_noalloc_ptr[dev];
+  }
+  // The GEMM writes every workspace element before the elementwise kernel
+  // reads it, so stale contents from an earlier call never leak through.
+  return gemm_epi_run_unfused(pl, A, B, aux, scalars, outs, scratch, GE_NOALLOC_SCRATCH_BYTES,
+                              stream);
+}

@@ -196,6 +196,39 @@ int gemm_epi_run_unfused(gemm_epi_plan *plan, const void *A, const void *B,
                          const void *const *aux, const float *scalars, void *const *outs,
                          void *workspace, size_t workspace_bytes, void *stream);
 
+/*
+ * Allocation-free variant of gemm_epi_run_unfused.  No counterpart on the
+ * pages: it exists for callers that cannot allocate device memory — code that
+ * runs where a cudaMalloc is not allowed or not wanted (inside an allocator or
+ * memory-pool callback, in a host application that reserves every byte of
+ * device memory up front and hands out nothing else, or in a deployment that
+ * forbids allocation after start-up) and so cannot provide the fp32
+ * workspace the unfused path needs.
+ *
+ * Instead of a caller buffer it uses one workspace compiled into the library:
+ * a device array of GE_NOALLOC_SCRATCH_BYTES that every GPU loading this
+ * library holds until the process exits.  The caller still passes A, B, aux,
+ * scalars and outputs exactly as for gemm_epi_run_unfused, and the results are
+ * the same bits.  The call itself allocates nothing.
+ *
+ *  * Problems needing more than GE_NOALLOC_SCRATCH_BYTES of workspace
+ *    (L*M*N*4 bytes) are rejected with GE_ERR_WORKSPACE before any launch.
+ *  * The first call on a device looks up that device's address of the array
+ *    (cudaGetSymbolAddress, with that device current); make the first call on
+ *    each device before any stream capture.
+ *  * All calls share the one array and it keeps whatever the last call left
+ *    in it.  Nothing in it needs to start at zero: the GEMM overwrites every
+ *    element it later reads.  Calls whose work overlaps on the GPU (different
+ *    streams, or different host threads, same device) race on the array: the
+ *    caller must order them.
+ * Errors: as gemm_epi_run_unfused, GE_ERR_WORKSPACE for oversized problems,
+ * GE_ERR_CUDA if the set-up lookup fails.
+ */
+#define GE_NOALLOC_SCRATCH_BYTES (16u * 1024u * 1024u)
+int gemm_epi_run_unfused_noalloc(gemm_epi_plan *plan, const void *A, const void *B,
+                                 const void *const *aux, const float *scalars, void *const *outs,
+                                 void *stream);
+
 /* Free a plan (NULL is ignored).  Does not synchronise. */
 void gemm_epi_plan_destroy(gemm_epi_plan *plan);
 
