@@ -44,12 +44,14 @@ FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_g
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--steps", type=int, default=500)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--mnk", default=None,
                     help="M,N,K override of the workload's sizes (profiling on a smaller case)")
+    ap.add_argument("--opt", default="",
+                    help="plan options, e.g. cta_group=2,tile_n=256,stages=5,raster_group=8")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-unfused", action="store_true")
@@ -254,7 +256,10 @@ def run_ours(args, w):
     outs = [torch.empty(w.L, w.M, w.N, dtype=W.TORCH_DTYPE[dt], device=dev) for _, dt in w.outs]
     dtypes = B.make_dtypes(w.ab, [dt for _, _, dt in w.aux], len(w.scalars),
                            [dt for _, dt in w.outs])
-    plan = B.gemm_epi_plan_create(w.L, w.M, w.N, w.K, dtypes, B.make_dag(w.dag))
+    opts = None
+    if args.opt:
+        opts = B.ge_options(**{k: int(v) for k, v in (kv.split("=") for kv in args.opt.split(","))})
+    plan = B.gemm_epi_plan_create(w.L, w.M, w.N, w.K, dtypes, B.make_dag(w.dag), opts)
     info = B.gemm_epi_plan_info(plan)
     flops = w.flops()
 
@@ -365,7 +370,8 @@ def run_ours(args, w):
                    "l2": "no flush: inputs (%d MiB) larger than L2" % (
                        (w.alg_bytes() - sum(w.L * w.M * w.N * W.ESIZE[dt]
                                             for _, dt in w.outs)) >> 20),
-                   "plan": info, "parallelism": "replicas" if world > 1 else "single"},
+                   "plan": info, "options": args.opt or "auto",
+                   "parallelism": "replicas" if world > 1 else "single"},
         "pct_of_peak": 100.0 * achieved / peak,
         "roofline": roofline, "gpu_launches": args.steps, "clocks": clk,
         "unfused": unfused, "e2e": e2e, "cpu_baseline": cpu,
