@@ -121,7 +121,7 @@ class ClockSampler:
         except subprocess.TimeoutExpired:
             self.proc.kill()
             out, _ = self.proc.communicate()
-        sm, smax, reasons = [], [], set()
+        sm, smax, power, reasons = [], [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for line in out.splitlines():
             parts = [p.strip() for p in line.split(",")]
@@ -130,6 +130,7 @@ class ClockSampler:
             try:
                 sm.append(float(parts[0]))
                 smax.append(float(parts[1]))
+                power.append(float(parts[2]))
             except ValueError:
                 continue
             for n, v in zip(names, parts[4:8]):
@@ -137,7 +138,9 @@ class ClockSampler:
                     reasons.add(n)
         return {"sm_mhz": statistics.median(sm) if sm else None,
                 "sm_max_mhz": max(smax) if smax else None,
-                "reasons": sorted(reasons), "samples": len(sm)}
+                "reasons": sorted(reasons), "samples": len(sm),
+                "power_w_median": statistics.median(power) if power else None,
+                "power_w_max": max(power) if power else None}
 
 
 # ------------------------------------------------------------ helpers ---
@@ -382,7 +385,9 @@ def run_ours(args, w):
 def main():
     args = parse()
     from dense_gemm_elementwise_gb300 import workloads as W
-    w = W.BY_NAME[args.workload]
+    table = dict(W.BY_NAME)
+    table.update({x.name: x for x in W.page_examples()})
+    w = table[args.workload]
     if args.mnk:
         import dataclasses
         m, n, k = (int(x) for x in args.mnk.split(","))

@@ -54,14 +54,14 @@ class ge_options(ctypes.Structure):
     _fields_ = [("cta_group", ctypes.c_int32), ("tile_n", ctypes.c_int32),
                 ("stages", ctypes.c_int32), ("max_ctas", ctypes.c_int32),
                 ("raster_group", ctypes.c_int32), ("timeout_ms", ctypes.c_int32),
-                ("debug_flags", ctypes.c_uint32)]
+                ("debug_flags", ctypes.c_uint32), ("cluster_n", ctypes.c_int32)]
 
 
 class ge_plan_info(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in
                 ("cta_group", "tile_m", "tile_n", "tile_k", "stages", "epi_chunk", "aux_stages",
                  "grid", "num_tiles", "smem_bytes", "n_instr", "n_regs", "num_sms",
-                 "epi_variant")]
+                 "epi_variant", "cluster_n")]
 
 
 class GemmEpiError(RuntimeError):

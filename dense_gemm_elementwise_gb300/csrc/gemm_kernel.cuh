@@ -16,6 +16,12 @@
 // tile i+1.  Ragged M/N/K edges are handled by TMA: out-of-range loads read
 // zeros, out-of-range stores are dropped.
 //
+// MC = 2: two CTA pairs of a 4-CTA cluster compute adjacent N tiles with the
+// same A rows; each CTA fetches half of its A rows and multicasts them to its
+// counterpart in the other pair (25% less L2->SM traffic).  A stage is free
+// only when both pairs' MMAs have read it, so empty barriers count one commit
+// per pair and the commits multicast to the whole cluster.
+//
 // cta_group::2: the CTA pair computes a (256 x BN) tile.  Each CTA loads its
 // 128 rows of A and its BN/2 columns of B into its own shared memory; the
 // leader's MMA thread issues the pair MMA, which reads both CTAs' halves and
@@ -33,11 +39,14 @@
 
 namespace ge {
 
-template <int CG, int BN>
+template <int CG, int BN, int MC>
 struct TileCfg {
+  static constexpr int kCluster = CG * MC;         // CTAs per cluster
   static constexpr int kMmaM = BM * CG;            // rows of one MMA tile
   static constexpr int kBnLocal = BN / CG;         // B columns loaded per CTA
   static constexpr int kABytes = BM * BK * 2;      // one A stage
+  static constexpr int kALoadRows = BM / MC;       // A rows this CTA fetches per stage
+  static_assert(MC == 1 || CG == 2, "A multicast is built on CTA pairs");
   static constexpr int kBBytes = kBnLocal * BK * 2;
   static constexpr int kBAtoms = kBnLocal / 64;    // 64-column swizzle atoms of B
   static constexpr int kSteps = BN / EW;          // epilogue steps per tile
@@ -137,9 +146,9 @@ struct FusedMem {
   }
 };
 
-template <int CG, int BN, class Epi>
+template <int CG, int BN, int MC, class Epi>
 __global__ void __launch_bounds__(kThreads, 1) gemm_epi_kernel(const __grid_constant__ KParams p) {
-  using T = TileCfg<CG, BN>;
+  using T = TileCfg<CG, BN, MC>;
   extern __shared__ uint8_t smem_raw[];
   // 1024-byte alignment of the shared-window address (swizzle atoms)
   uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
@@ -147,9 +156,14 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_epi_kernel(const __grid_cons
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const uint32_t rank = (CG == 2) ? cluster_ctarank() : 0u;
-  const int unit = blockIdx.x / CG;    // this CTA's cluster (or CTA) index
-  const int n_units = gridDim.x / CG;
+  const uint32_t crank = (T::kCluster > 1) ? cluster_ctarank() : 0u;
+  const uint32_t rank = crank % CG;          // rank within the CTA pair
+  const int pair = static_cast<int>(crank / CG);  // pair within the cluster (MC > 1)
+  const uint32_t leader = crank - rank;      // cluster rank of this pair's leader
+  const int unit = blockIdx.x / T::kCluster;  // this CTA's cluster (or CTA) index
+  const int n_units = gridDim.x / T::kCluster;
+  constexpr uint16_t kAllMask = static_cast<uint16_t>((1u << T::kCluster) - 1u);
+  const uint16_t pair_mask = static_cast<uint16_t>(0x3u << (CG * pair));
 
   const uint32_t bar = sb + p.off_bar;
   const uint32_t bar_aux = bar + kBarAux;
@@ -159,7 +173,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_epi_kernel(const __grid_cons
   if (threadIdx.x == 0) {
     for (int s = 0; s < p.stages; ++s) {
       mbar_init(bar + kBarFull + 8 * s, 1);
-      mbar_init(bar + kBarEmpty + 8 * s, 1);
+      mbar_init(bar + kBarEmpty + 8 * s, MC);  // released by every pair sharing the stage
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(bar + kBarTmemFull + 8 * b, 1);
@@ -180,7 +194,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_epi_kernel(const __grid_cons
   }
   __syncwarp();
   tc_fence_before();
-  if constexpr (CG == 2) cluster_sync_all(); else __syncthreads();
+  if constexpr (T::kCluster > 1) cluster_sync_all(); else __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t *>(tmem_slot);
   const Waiter wt{abort_flag, p.status, p.timeout_ns};
@@ -197,6 +211,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_epi_kernel(const __grid_cons
       for (int i = 0; ok && i < my_tiles; ++i) {
         int l, mb, nb;
         tile_coords(p, unit + i * n_units, l, mb, nb);
+        nb = nb * MC + pair;
         const int m0 = mb * T::kMmaM + static_cast<int>(rank) * BM;
         const int n0 = nb * BN + static_cast<int>(rank) * T::kBnLocal;
         for (int kb = 0; kb < p.num_kb; ++kb) {
@@ -212,9 +227,19 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_epi_kernel(const __grid_cons
             const uint32_t sa = sb + p.off_A + stage * T::kABytes;
             const uint32_t sbb = sb + p.off_B + stage * T::kBBytes;
             if constexpr (CG == 2) {
-              const uint32_t fb = mapa_shared(fb_local, 0);
+              const uint32_t fb = mapa_shared(fb_local, leader);
               if (rank == 0) mbar_arrive_expect_tx(fb_local, p.tx_bytes);
-              tma_load_3d_pair(sa, &p.tmA, fb, kb * BK, m0, l);
+              if constexpr (MC == 1) {
+                tma_load_3d_pair(sa, &p.tmA, fb, kb * BK, m0, l);
+              } else {
+                // this pair fetches its share of the A rows and multicasts it to
+                // the CTA with the same rank in every pair of the cluster
+                uint16_t mask = 0;
+#pragma unroll
+                for (int pp = 0; pp < MC; ++pp) mask |= static_cast<uint16_t>(1u << (pp * CG + rank));
+                tma_load_3d_pair_mc(sa + pair * T::kALoadRows * 128, &p.tmA, fb, kb * BK,
+                                    m0 + pair * T::kALoadRows, l, mask);
+              }
 #pragma unroll
               for (int j = 0; j < T::kBAtoms; ++j)
                 tma_load_3d_pair(sbb + j * 8192, &p.tmB, fb, n0 + 64 * j, kb * BK, l);
@@ -284,14 +309,14 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_epi_kernel(const __grid_cons
             const uint64_t bd = smem_desc_sw128(sbb + 2048u * k, p.b_lbo, p.b_sbo);
             umma_f16<CG>(d, ad, bd, id, (kb | k) != 0 ? 1u : 0u);
           }
-          umma_commit<CG>(bar + kBarEmpty + 8 * stage);
+          umma_commit<CG>(bar + kBarEmpty + 8 * stage, kAllMask);
           if (++stage == p.stages) {
             stage = 0;
             phase ^= 1u;
           }
         }
         if (!ok) break;
-        umma_commit<CG>(bar + kBarTmemFull + 8 * abuf);
+        umma_commit<CG>(bar + kBarTmemFull + 8 * abuf, pair_mask);
         abuf ^= 1;
         if (abuf == 0) aphase ^= 1u;
       }
@@ -305,7 +330,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_epi_kernel(const __grid_cons
         }
       } else {
         // abort: let the MMAs already issued finish before TMEM is freed
-        umma_commit<CG>(bar + kBarDrain);
+        umma_commit<CG>(bar + kBarDrain, pair_mask);
         wt.drain(bar + kBarDrain, 0u);
       }
     }
@@ -331,6 +356,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_epi_kernel(const __grid_cons
       if (ii != pf_tile) {
         int mb2, nb2;
         tile_coords(p, unit + ii * n_units, pf_l, mb2, nb2);
+        nb2 = nb2 * MC + pair;
         pf_tile = ii;
         pf_x0 = nb2 * BN;
         pf_y = mb2 * T::kMmaM + static_cast<int>(rank) * BM + q * 32;
@@ -348,6 +374,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_epi_kernel(const __grid_cons
     for (int i = 0; ok && i < my_tiles; ++i) {
       int l, mb, nb;
       tile_coords(p, unit + i * n_units, l, mb, nb);
+      nb = nb * MC + pair;
       const int m0 = mb * T::kMmaM + static_cast<int>(rank) * BM + q * 32;
       const int n0 = nb * BN;
       // start this tile's aux loads before its accumulator is ready
@@ -377,7 +404,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_epi_kernel(const __grid_cons
           __syncwarp();
           if (lane == 0) {
             const uint32_t tb = bar + kBarTmemEmpty + 8 * abuf;
-            if constexpr (CG == 2) mbar_arrive_remote(mapa_shared(tb, 0));
+            if constexpr (CG == 2) mbar_arrive_remote(mapa_shared(tb, leader));
             else mbar_arrive(tb);
           }
         }
@@ -421,7 +448,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_epi_kernel(const __grid_cons
   // ------------------------------------------------------------ teardown --
   __syncwarp();
   tc_fence_before();
-  if constexpr (CG == 2) cluster_sync_all(); else __syncthreads();
+  if constexpr (T::kCluster > 1) cluster_sync_all(); else __syncthreads();
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc<CG>(tmem_base, T::kTmemCols);

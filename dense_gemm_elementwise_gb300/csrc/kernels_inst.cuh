@@ -10,19 +10,19 @@
 
 namespace ge {
 
-template <int CG, int BN, size_t... K>
+template <int CG, int BN, int MC, size_t... K>
 const void *pick_gemm_kernel(int epi, std::index_sequence<K...>) {
   static const void *const table[] = {
-      reinterpret_cast<const void *>(&gemm_epi_kernel<CG, BN, EpiStatic<catalog::Prog<K>>>)...};
-  if (epi < 0) return reinterpret_cast<const void *>(&gemm_epi_kernel<CG, BN, EpiInterp>);
+      reinterpret_cast<const void *>(&gemm_epi_kernel<CG, BN, MC, EpiStatic<catalog::Prog<K>>>)...};
+  if (epi < 0) return reinterpret_cast<const void *>(&gemm_epi_kernel<CG, BN, MC, EpiInterp>);
   return epi < static_cast<int>(sizeof...(K)) ? table[epi] : nullptr;
 }
 
 }  // namespace ge
 
-#define GE_INSTANTIATE_GEMM(CG, BN)                                                    \
-  namespace ge {                                                                       \
-  const void *gemm_kernel_cg##CG##_n##BN(int epi) {                                    \
-    return pick_gemm_kernel<CG, BN>(epi, std::make_index_sequence<catalog::kCount>{}); \
-  }                                                                                    \
+#define GE_INSTANTIATE_GEMM(CG, BN, MC, NAME)                                              \
+  namespace ge {                                                                           \
+  const void *NAME(int epi) {                                                              \
+    return pick_gemm_kernel<CG, BN, MC>(epi, std::make_index_sequence<catalog::kCount>{}); \
+  }                                                                                        \
   }

@@ -17,6 +17,7 @@ const void *gemm_kernel_cg1_n128(int epi);
 const void *gemm_kernel_cg1_n256(int epi);
 const void *gemm_kernel_cg2_n128(int epi);
 const void *gemm_kernel_cg2_n256(int epi);
+const void *gemm_kernel_cg2_n256_mc2(int epi);  // 4-CTA cluster, A multicast across 2 pairs
 
 // unfused comparison path: elementwise epilogue over an fp32 accumulator
 const void *ew_kernel(int epi);

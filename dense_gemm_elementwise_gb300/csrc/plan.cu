@@ -157,6 +157,7 @@ bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 // ------------------------------------------------------------ configuration --
 struct Layout {
   int cg = 0, bn = 0, stages = 0, aux_stages = 0, grid = 0, num_tiles = 0;
+  int mc = 1;         // CTA pairs per cluster sharing A (multicast)
   int smem = 0;       // dynamic smem requested at launch
   int smem_used = 0;  // bytes the layout occupies
   int num_m_blk = 0, num_n_blk = 0, num_kb = 0, raster_group = 0;
@@ -253,7 +254,8 @@ struct gemm_epi_plan {
 
 namespace {
 
-const void *gemm_kernel(int cg, int bn, int epi) {
+const void *gemm_kernel(int cg, int bn, int mc, int epi) {
+  if (mc == 2) return (cg == 2 && bn == 256) ? gemm_kernel_cg2_n256_mc2(epi) : nullptr;
   if (cg == 1 && bn == 64) return gemm_kernel_cg1_n64(epi);
   if (cg == 1 && bn == 128) return gemm_kernel_cg1_n128(epi);
   if (cg == 1 && bn == 256) return gemm_kernel_cg1_n256(epi);
@@ -270,9 +272,9 @@ cudaLaunchConfig_t launch_config(const Layout &Lo, cudaStream_t s, cudaLaunchAtt
   cfg.stream = s;
   cfg.attrs = nullptr;
   cfg.numAttrs = 0;
-  if (Lo.cg == 2) {
+  if (Lo.cg * Lo.mc > 1) {
     attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.x = static_cast<unsigned>(Lo.cg * Lo.mc);
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
@@ -282,7 +284,7 @@ cudaLaunchConfig_t launch_config(const Layout &Lo, cudaStream_t s, cudaLaunchAtt
 }
 
 cudaError_t launch_gemm(const Layout &Lo, int epi, const KParams &kp, cudaStream_t s) {
-  const void *fn = gemm_kernel(Lo.cg, Lo.bn, epi);
+  const void *fn = gemm_kernel(Lo.cg, Lo.bn, Lo.mc, epi);
   if (!fn) return cudaErrorInvalidDeviceFunction;
   cudaLaunchAttribute attr[1];
   cudaLaunchConfig_t cfg = launch_config(Lo, s, attr);
@@ -292,14 +294,17 @@ cudaError_t launch_gemm(const Layout &Lo, int epi, const KParams &kp, cudaStream
 
 // Rough cost model in SM clocks: waves x per-tile mainloop, where a k-block
 // costs the larger of its tensor-core time (2*BN clocks for 128 x BN x 64 at
-// 8192 flop/clk/SM) and its operand fill time at ~64 B/clk/SM of L2 bandwidth.
-double est_cycles(const gemm_epi_plan *pl, int cg, int bn, int units) {
+// 8192 flop/clk/SM) and its operand fill time at ~48 B/clk/SM of L2 bandwidth
+// when every SM is busy (measured: per-SM throughput drops by a third from
+// 38 to 152 active SMs with 32 KiB per k-block).  With A multicast (mc = 2)
+// a CTA fetches only half of its A rows.
+double est_cycles(const gemm_epi_plan *pl, int cg, int bn, int mc, int units) {
   const int64_t mt = (pl->M + BM * cg - 1) / (BM * cg);
-  const int64_t nt = (pl->N + bn - 1) / bn;
+  const int64_t nt = (pl->N + int64_t(bn) * mc - 1) / (int64_t(bn) * mc);
   const int64_t tiles = pl->L * mt * nt;
   const int64_t kb = (pl->K + BK - 1) / BK;
   const double mma = 2.0 * bn;
-  const double fill = double((BM + bn / cg) * BK * 2) / 64.0;
+  const double fill = double((BM / mc + bn / cg) * BK * 2) / 48.0;
   const double per_tile = kb * std::max(mma, fill);
   const int64_t waves = (tiles + units - 1) / units;
   return waves * per_tile + (bn / CH) * 300.0;
@@ -310,26 +315,28 @@ int configure(gemm_epi_plan *pl) {
   if (o.cta_group != 0 && o.cta_group != 1 && o.cta_group != 2) return GE_ERR_INVALID;
   if (o.tile_n != 0 && o.tile_n != 64 && o.tile_n != 128 && o.tile_n != 256) return GE_ERR_INVALID;
   if (o.stages < 0 || o.stages > kMaxStages || o.max_ctas < 0 || o.raster_group < 0 ||
-      o.timeout_ms < 0)
+      o.timeout_ms < 0 || (o.cluster_n != 0 && o.cluster_n != 1 && o.cluster_n != 2))
     return GE_ERR_INVALID;
-  const int cand[5][2] = {{2, 256}, {2, 128}, {1, 256}, {1, 128}, {1, 64}};
+  const int cand[6][3] = {{2, 256, 2}, {2, 256, 1}, {2, 128, 1}, {1, 256, 1}, {1, 128, 1}, {1, 64, 1}};
   int best = -1;
   double best_c = 0;
-  for (int c = 0; c < 5; ++c) {
-    const int cg = cand[c][0], bn = cand[c][1];
+  for (int c = 0; c < 6; ++c) {
+    const int cg = cand[c][0], bn = cand[c][1], mc = cand[c][2];
     if (o.cta_group && o.cta_group != cg) continue;
     if (o.tile_n && o.tile_n != bn) continue;
+    if (o.cluster_n ? o.cluster_n != mc : mc != 1) continue;  // multicast: opt-in
     int sms = pl->num_sms;
     if (o.max_ctas) sms = std::min(sms, o.max_ctas);
-    const int units = std::max(1, sms / cg);
-    const double cost = est_cycles(pl, cg, bn, units);
+    if (sms < cg * mc) continue;
+    const int units = sms / (cg * mc);
+    const double cost = est_cycles(pl, cg, bn, mc, units);
     if (best < 0 || cost < best_c * 0.98) {
       best = c;
       best_c = cost;
     }
   }
   if (best < 0) return GE_ERR_INVALID;  // e.g. cta_group 2 with tile_n 64
-  const int cg = cand[best][0], bn = cand[best][1];
+  const int cg = cand[best][0], bn = cand[best][1], mc = cand[best][2];
 
   int st = make_layout(&pl->lay, cg, bn, o.stages, pl->prog, pl->max_smem);
   if (st != GE_OK) return st;
@@ -337,8 +344,10 @@ int configure(gemm_epi_plan *pl) {
   if (st != GE_OK) return st;
 
   for (Layout *Lo : {&pl->lay, &pl->lay_acc}) {
+    Lo->mc = mc;
     Lo->num_m_blk = static_cast<int>((pl->M + BM * cg - 1) / (BM * cg));
-    Lo->num_n_blk = static_cast<int>((pl->N + bn - 1) / bn);
+    // with A multicast a tile index covers mc adjacent N tiles (one per pair)
+    Lo->num_n_blk = static_cast<int>((pl->N + int64_t(bn) * mc - 1) / (int64_t(bn) * mc));
     Lo->num_kb = static_cast<int>((pl->K + BK - 1) / BK);
     const int64_t tiles = pl->L * Lo->num_m_blk * int64_t(Lo->num_n_blk);
     if (tiles > (int64_t(1) << 30)) return GE_ERR_SHAPE;
@@ -346,22 +355,22 @@ int configure(gemm_epi_plan *pl) {
     Lo->raster_group = o.raster_group ? o.raster_group : 8;
     int sms = pl->num_sms;
     if (o.max_ctas) sms = std::min(sms, o.max_ctas);
-    int units = std::max(1, sms / cg);
-    const void *fn = gemm_kernel(cg, bn, Lo == &pl->lay ? pl->epi : pl->epi_acc);
+    int units = std::max(1, sms / (cg * mc));
+    const void *fn = gemm_kernel(cg, bn, mc, Lo == &pl->lay ? pl->epi : pl->epi_acc);
     if (!fn) return GE_ERR_INVALID;
     if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, Lo->smem) != cudaSuccess)
       return GE_ERR_CUDA;
-    if (cg == 2) {
+    if (cg * mc > 1) {
       int clusters = 0;
       cudaLaunchAttribute attr[1];
       cudaLaunchConfig_t cfg = launch_config(*Lo, nullptr, attr);
-      cfg.gridDim = dim3(2);
+      cfg.gridDim = dim3(static_cast<unsigned>(cg * mc));
       if (cudaOccupancyMaxActiveClusters(&clusters, fn, &cfg) == cudaSuccess && clusters > 0)
         units = std::min(units, clusters);
       cudaGetLastError();
     }
     units = static_cast<int>(std::min<int64_t>(units, tiles));
-    Lo->grid = units * cg;
+    Lo->grid = units * cg * mc;
   }
   return GE_OK;
 }
@@ -402,10 +411,12 @@ void fill_params(const gemm_epi_plan *pl, const Layout &Lo, const EpiProgram &P,
   kp->debug_flags = pl->opt.debug_flags;
 }
 
+// A box: the rows one CTA fetches per stage (all 128, or its share under multicast)
 bool encode_operands(const gemm_epi_plan *pl, KParams *kp, const void *A, const void *B) {
   const uint64_t L = pl->L, M = pl->M, N = pl->N, K = pl->K;
   const int ab = pl->dt.ab;
-  return encode3d(&kp->tmA, ab, A, K, M, L, BK, BM, CU_TENSOR_MAP_SWIZZLE_128B,
+  const uint32_t a_rows = static_cast<uint32_t>(BM / pl->lay.mc);
+  return encode3d(&kp->tmA, ab, A, K, M, L, BK, a_rows, CU_TENSOR_MAP_SWIZZLE_128B,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B) &&
          encode3d(&kp->tmB, ab, B, N, K, L, 64, BK, CU_TENSOR_MAP_SWIZZLE_128B,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
@@ -461,9 +472,9 @@ int check_run_args(const gemm_epi_plan *pl, const void *A, const void *B, const 
 void log_plan(const gemm_epi_plan *pl) {
   const Layout &Lo = pl->lay;
   std::fprintf(stderr,
-               "[gemm_epi] L=%lld M=%lld N=%lld K=%lld: cta_group=%d tile=%dx%dx%d stages=%d "
+               "[gemm_epi] L=%lld M=%lld N=%lld K=%lld: cta_group=%d x%d tile=%dx%dx%d stages=%d "
                "aux_stages=%d grid=%d tiles=%d smem=%d program=%d ins/%d regs epilogue=%s\n",
-               (long long)pl->L, (long long)pl->M, (long long)pl->N, (long long)pl->K, Lo.cg,
+               (long long)pl->L, (long long)pl->M, (long long)pl->N, (long long)pl->K, Lo.cg, Lo.mc,
                BM * Lo.cg, Lo.bn, BK, Lo.stages, Lo.aux_stages, Lo.grid, Lo.num_tiles, Lo.smem_used,
                pl->prog.n_ins, pl->prog.n_regs,
                pl->epi >= 0 ? catalog::kEntries[pl->epi].name : "interpreter");
@@ -560,6 +571,7 @@ int gemm_epi_plan_info(const gemm_epi_plan *pl, ge_plan_info *info) {
   info->n_regs = pl->prog.n_regs;
   info->num_sms = pl->num_sms;
   info->epi_variant = pl->epi;
+  info->cluster_n = pl->lay.mc;
   return GE_OK;
 }
 

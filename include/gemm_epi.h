@@ -101,6 +101,10 @@ typedef struct {
   int32_t raster_group; /* 0 auto, else M tiles per raster group (L2 reuse of B)        */
   int32_t timeout_ms;   /* 0 = 1000; bound on every device-side wait                    */
   uint32_t debug_flags; /* 0; GE_DEBUG_* below, for tests only                          */
+  int32_t cluster_n;    /* 0 or 1: no multicast; 2 = two CTA pairs per 4-CTA cluster
+                           computing adjacent N tiles and sharing A by TMA multicast
+                           (cta_group 2, tile_n 256).  Opt-in: on GB300 only 36 such
+                           clusters fit (144 SMs), which offsets the traffic saved.     */
 } ge_options;
 
 /* Test hook: the producer never loads the first k-block, so the MMA warp's
@@ -121,6 +125,7 @@ typedef struct {
   int32_t n_instr, n_regs;                    /* compiled epilogue program             */
   int32_t num_sms;
   int32_t epi_variant;                        /* built-in epilogue used, -1: interpreter */
+  int32_t cluster_n;                          /* CTA pairs sharing A per cluster         */
 } ge_plan_info;
 
 typedef struct gemm_epi_plan gemm_epi_plan;

@@ -54,48 +54,60 @@ def test_page_examples(w):
 
 SHAPES = [(1, 1, 8, 8), (1, 8, 8, 8), (1, 129, 136, 72), (3, 200, 264, 200),
           (2, 257, 520, 1000), (1, 300, 24, 64), (1, 64, 1032, 136), (2, 513, 392, 8)]
-VARIANTS = [(1, 64), (1, 128), (1, 256), (2, 128), (2, 256)]
+# (cta_group, tile N, CTA pairs per cluster sharing A by multicast)
+VARIANTS = [(1, 64, 1), (1, 128, 1), (1, 256, 1), (2, 128, 1), (2, 256, 1), (2, 256, 2)]
+
+
+def opts(variant, **kw):
+    return B.ge_options(cta_group=variant[0], tile_n=variant[1], cluster_n=variant[2], **kw)
+
+
+def vid(v):
+    return "cg%d_n%d_x%d" % v
 
 
 @pytest.mark.parametrize("shape", SHAPES, ids=lambda s: "x".join(map(str, s)))
-@pytest.mark.parametrize("variant", VARIANTS, ids=lambda v: "cg%d_n%d" % v)
+@pytest.mark.parametrize("variant", VARIANTS, ids=vid)
 def test_ragged_shapes_exact(shape, variant):
-    """Integer inputs: every (cta_group, tile N) variant must be bit-exact on
-    ragged M, N, K (TMA zero-fills loads and clips stores at the edges)."""
+    """Integer inputs: every kernel variant must be bit-exact on ragged M, N,
+    K (TMA zero-fills loads and clips stores at the edges; with multicast an
+    odd number of N tiles leaves the second pair's tile out of range)."""
     w = small(W.CONFIGS[0], *shape)
     inputs = W.make_inputs(w)
-    opt = B.ge_options(cta_group=variant[0], tile_n=variant[1])
-    gpu, info = _gpu.run_gpu(w, inputs, options=opt)
-    assert (info["cta_group"], info["tile_n"]) == variant
+    gpu, info = _gpu.run_gpu(w, inputs, options=opts(variant))
+    assert (info["cta_group"], info["tile_n"], info["cluster_n"]) == variant
     _gpu.compare(w, gpu, _gpu.oracle_rows(w, inputs))
 
 
-@pytest.mark.parametrize("variant", VARIANTS, ids=lambda v: "cg%d_n%d" % v)
+@pytest.mark.parametrize("variant", VARIANTS, ids=vid)
 def test_bf16_bias_relu_square_variants(variant):
     w = small(W.CONFIGS[4], 2, 384, 520, 264)
     inputs = W.make_inputs(w)
-    opt = B.ge_options(cta_group=variant[0], tile_n=variant[1])
-    gpu, _ = _gpu.run_gpu(w, inputs, options=opt)
+    gpu, _ = _gpu.run_gpu(w, inputs, options=opts(variant))
     _gpu.compare(w, gpu, _gpu.oracle_rows(w, inputs))
 
 
 @pytest.mark.parametrize("stages", [2, 3, 4])
-def test_few_stages(stages):
+@pytest.mark.parametrize("cluster_n", [1, 2])
+def test_few_stages(stages, cluster_n):
     """Short rings wrap the stage/phase bookkeeping many times per tile."""
-    w = small(W.CONFIGS[3], 1, 512, 512, 1024)
+    w = small(W.CONFIGS[3], 1, 512, 1024, 1024)
     inputs = W.make_inputs(w)
-    gpu, info = _gpu.run_gpu(w, inputs, options=B.ge_options(stages=stages))
+    gpu, info = _gpu.run_gpu(w, inputs, options=B.ge_options(
+        stages=stages, cta_group=2, tile_n=256, cluster_n=cluster_n))
     assert info["stages"] == stages
     _gpu.compare(w, gpu, _gpu.oracle_rows(w, inputs))
 
 
-def test_small_grid_many_tiles_per_cta():
-    """Two CTA pairs loop over many tiles: both TMEM accumulators, the aux
+@pytest.mark.parametrize("cluster_n", [1, 2])
+def test_small_grid_many_tiles_per_cta(cluster_n):
+    """Four CTAs loop over many tiles: both TMEM accumulators, the aux
     prefetch across tile boundaries and the raster order all wrap."""
     w = small(W.CONFIGS[3], 2, 1024, 768, 256)
     inputs = W.make_inputs(w)
-    gpu, info = _gpu.run_gpu(w, inputs, options=B.ge_options(max_ctas=4, raster_group=3))
-    assert info["grid"] <= 4
+    gpu, info = _gpu.run_gpu(w, inputs, options=B.ge_options(
+        max_ctas=4, raster_group=3, cta_group=2, tile_n=256, cluster_n=cluster_n))
+    assert info["grid"] <= 4 and info["cluster_n"] == cluster_n
     _gpu.compare(w, gpu, _gpu.oracle_rows(w, inputs))
 
 
@@ -115,9 +127,9 @@ def test_unfused_matches_fused_bitwise(w):
 def test_variants_agree_on_normal_inputs():
     w = small(W.CONFIGS[3], 1, 512, 512, 2048)
     inputs = W.make_inputs(w)
-    base, _ = _gpu.run_gpu(w, inputs, options=B.ge_options(cta_group=2, tile_n=256))
-    for cg, bn in VARIANTS[:-1]:
-        other, _ = _gpu.run_gpu(w, inputs, options=B.ge_options(cta_group=cg, tile_n=bn))
+    base, _ = _gpu.run_gpu(w, inputs, options=opts(VARIANTS[4]))
+    for v in VARIANTS[:4] + VARIANTS[5:]:
+        other, _ = _gpu.run_gpu(w, inputs, options=opts(v))
         for a, b in zip(base, other):
             assert torch.allclose(a.float(), b.float(), rtol=1e-3, atol=1e-2)
 
@@ -159,13 +171,15 @@ def test_run_argument_errors():
         B.gemm_epi_plan_destroy(plan)
 
 
-def test_device_wait_timeout_is_reported():
+@pytest.mark.parametrize("cluster_n", [1, 2])
+def test_device_wait_timeout_is_reported(cluster_n):
     """A k-block that is never loaded: the MMA warp's bounded wait runs out,
     the kernel records GE_ERR_TIMEOUT, drains and exits; the context stays
     usable and the next run is correct."""
     w = small(W.CONFIGS[0], 1, 256, 256, 256)
     inputs = W.make_inputs(w)
-    opt = B.ge_options(timeout_ms=50, debug_flags=B.GE_DEBUG_SKIP_FIRST_LOAD, max_ctas=2)
+    opt = B.ge_options(timeout_ms=50, debug_flags=B.GE_DEBUG_SKIP_FIRST_LOAD,
+                       max_ctas=2 * cluster_n, cta_group=2, tile_n=256, cluster_n=cluster_n)
     A, Bm, aux, sc = inputs
     dev = torch.device("cuda")
     outs = [torch.empty(1, 256, 256, dtype=torch.float16, device=dev) for _ in range(2)]
@@ -199,12 +213,12 @@ CATALOG_CASES = [small(W.CONFIGS[0], 2, 300, 392, 200), small(W.CONFIGS[2], 1, 2
 
 
 @pytest.mark.parametrize("w", CATALOG_CASES, ids=lambda w: w.name)
-@pytest.mark.parametrize("variant", [(1, 64), (2, 256)], ids=lambda v: "cg%d_n%d" % v)
+@pytest.mark.parametrize("variant", [(1, 64, 1), (2, 256, 2)], ids=vid)
 def test_builtin_and_interpreter_agree_bitwise(w, variant):
     """The straight-line kernels and the interpreter evaluate the same
     compiled program in the same order: identical bits, fused and unfused."""
     inputs = W.make_inputs(w)
-    base = dict(cta_group=variant[0], tile_n=variant[1])
+    base = dict(cta_group=variant[0], tile_n=variant[1], cluster_n=variant[2])
     fast, info = _gpu.run_gpu(w, inputs, options=B.ge_options(**base))
     slow, info2 = _gpu.run_gpu(w, inputs, options=B.ge_options(
         debug_flags=B.GE_DEBUG_FORCE_INTERPRETER, **base))
