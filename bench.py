@@ -179,7 +179,7 @@ def oracle_sample(w, A, Bm, aux, scalars, rows, threads):
     from dense_gemm_elementwise_gb300 import workloads as W
     t0 = time.perf_counter()
     oracle.gemm_epilogue(w.L, w.M, w.N, w.K, w.ab, W.to_codes(A), W.to_codes(Bm),
-                         [W.to_codes(a) for a in aux], [dt for _, _, dt in w.aux], scalars, w.dag,
+                         [W.to_codes(a) for a in aux], [s[2] for s in w.aux], scalars, w.dag,
                          [dt for _, dt in w.outs], rows=np.asarray(rows, dtype=np.int64),
                          threads=threads)
     return time.perf_counter() - t0
@@ -257,7 +257,7 @@ def run_ours(args, w):
     Ad, Bd = A.to(dev), Bm.to(dev)
     auxd = [a.to(dev) for a in aux]
     outs = [torch.empty(w.L, w.M, w.N, dtype=W.TORCH_DTYPE[dt], device=dev) for _, dt in w.outs]
-    dtypes = B.make_dtypes(w.ab, [dt for _, _, dt in w.aux], len(w.scalars),
+    dtypes = B.make_dtypes(w.ab, [s[2] for s in w.aux], len(w.scalars),
                            [dt for _, dt in w.outs])
     opts = None
     if args.opt:

@@ -90,6 +90,14 @@ constexpr ge_dag dag_row_bias() {
                  nd(GE_ADD, 2, 3), nd(GE_STORE, 4, 0, 0)}};
 }
 
+// D = alpha*accum + row_bias + col_bias
+constexpr ge_dag dag_row_col_bias() {
+  return ge_dag{8,
+                {nd(GE_ACCFETCH), nd(GE_SCALAR, 0, 0, 0), nd(GE_MUL, 0, 1), nd(GE_BROADCAST, 0, 0, 0),
+                 nd(GE_ADD, 2, 3), nd(GE_COL_BROADCAST, 0, 0, 1), nd(GE_ADD, 4, 5),
+                 nd(GE_STORE, 6, 0, 0)}};
+}
+
 constexpr Entry kEntries[] = {
     {"store_accum_f32", types(0, 0, 0, 0, 1, GE_F32, 0), dag_store_accum()},
     {"store_accum_f16", types(0, 0, 0, 0, 1, GE_F16, 0), dag_store_accum()},
@@ -101,6 +109,7 @@ constexpr Entry kEntries[] = {
     {"bias_relu_square_bf16", types(2, GE_BF16, GE_F32, 2, 2, GE_BF16, GE_BF16),
      dag_bias_relu_square()},
     {"row_bias_f16", types(1, GE_F16, 0, 1, 1, GE_F16, 0), dag_row_bias()},
+    {"row_col_bias_f16", types(2, GE_F16, GE_F16, 1, 1, GE_F16, 0), dag_row_col_bias()},
 };
 
 constexpr int kCount = static_cast<int>(sizeof(kEntries) / sizeof(kEntries[0]));

@@ -32,6 +32,12 @@ enum EpiOp : uint32_t {
   OP_ADD = 2,    // r[dst] += src
   OP_RELU = 3,   // r[dst]  = r[dst] > 0 ? r[dst] : +0
   OP_STORE = 4,  // out[dst] = round(src)
+  OP_SUB = 5,    // r[dst] -= src
+  OP_RSUB = 6,   // r[dst]  = src - r[dst]
+  OP_DIV = 7,    // r[dst] /= src
+  OP_RDIV = 8,   // r[dst]  = src / r[dst]
+  OP_MIN = 9,    // r[dst]  = min(r[dst], src)
+  OP_MAX = 10,   // r[dst]  = max(r[dst], src)
 };
 
 enum EpiSrc : uint32_t {
@@ -41,6 +47,7 @@ enum EpiSrc : uint32_t {
   SRC_BCAST = 3,   // row-broadcast vector number idx
   SRC_SCALAR = 4,  // scalar idx
   SRC_NONE = 5,
+  SRC_CBCAST = 6,  // column-broadcast vector number idx (one value per row)
 };
 
 __host__ __device__ constexpr uint32_t pack_ins(uint32_t op, uint32_t dst, uint32_t src,
@@ -58,6 +65,9 @@ struct EpiProgram {
   int32_t n_bcast;                        // Broadcast vectors
   int32_t bcast_slot[GE_MAX_AUX];
   int32_t bcast_dtype[GE_MAX_AUX];
+  int32_t n_cbcast;                       // column-broadcast vectors
+  int32_t cbcast_slot[GE_MAX_AUX];
+  int32_t cbcast_dtype[GE_MAX_AUX];
   int32_t n_out;
   int32_t out_dtype[GE_MAX_OUT];
   int32_t n_regs;                         // registers the program uses
@@ -80,6 +90,7 @@ struct KParams {
   CUtensorMap tmAux[GE_MAX_TMA_AUX];  // (N, M, L) box (EW, 32, 1)
   CUtensorMap tmOut[GE_MAX_OUT];      // (N, M, L) box (EW, 32, 1)
   const void *bcast_ptr[GE_MAX_AUX];
+  const void *cbcast_ptr[GE_MAX_AUX];
   uint32_t *status;                   // device status word (timeouts)
   EpiProgram prog;
   int32_t L, M, N, K;
@@ -102,9 +113,11 @@ struct EwParams {
   const float *acc;                   // (L, M, N) fp32 workspace
   const void *aux_ptr[GE_MAX_TMA_AUX];
   const void *bcast_ptr[GE_MAX_AUX];
+  const void *cbcast_ptr[GE_MAX_AUX];
   void *out_ptr[GE_MAX_OUT];
   EpiProgram prog;
   int64_t rows;                       // L*M
+  int32_t M;
   int32_t N;
   int32_t chunks_per_row;             // ceil(N / 8): one thread per 8 columns
 };

@@ -166,6 +166,17 @@ __device__ __forceinline__ void row_store(void *row, int col0, int N, const floa
   }
 }
 
+// one element of a vector, widened to fp32 (column-broadcast values)
+template <int DT>
+__device__ __forceinline__ float load_one(const void *base, int64_t i) {
+  if constexpr (DT == GE_F32) {
+    return __ldg(static_cast<const float *>(base) + i);
+  } else {
+    const uint32_t u = __ldg(static_cast<const uint16_t *>(base) + i);
+    return DT == GE_BF16 ? __uint_as_float(u << 16) : __half2float(__ushort_as_half(static_cast<unsigned short>(u)));
+  }
+}
+
 // run-time element type -> compile-time instantiation
 #define GE_DISPATCH_DTYPE(dt, CALL) \
   do {                              \
@@ -207,6 +218,7 @@ __device__ __forceinline__ void run_program(const EpiProgram &P, const float (&a
       case SRC_ACC: vcopy(t, acc); break;
       case SRC_AUX: GE_DISPATCH_DTYPE(P.tma_aux_dtype[idx], mem.template aux<DT_>(idx, t)); break;
       case SRC_BCAST: GE_DISPATCH_DTYPE(P.bcast_dtype[idx], mem.template bcast<DT_>(idx, t)); break;
+      case SRC_CBCAST: GE_DISPATCH_DTYPE(P.cbcast_dtype[idx], mem.template cbcast<DT_>(idx, t)); break;
       case SRC_SCALAR: {
         const float s = P.scalars[idx];
 #pragma unroll
@@ -247,6 +259,42 @@ __device__ __forceinline__ void run_program(const EpiProgram &P, const float (&a
           GE_APPLY(2, x > 0.f ? x : 0.f) GE_APPLY(3, x > 0.f ? x : 0.f)
         }
         break;
+      case OP_SUB:
+        switch (dst) {
+          GE_APPLY(0, __fsub_rn(x, t[e])) GE_APPLY(1, __fsub_rn(x, t[e]))
+          GE_APPLY(2, __fsub_rn(x, t[e])) GE_APPLY(3, __fsub_rn(x, t[e]))
+        }
+        break;
+      case OP_RSUB:
+        switch (dst) {
+          GE_APPLY(0, __fsub_rn(t[e], x)) GE_APPLY(1, __fsub_rn(t[e], x))
+          GE_APPLY(2, __fsub_rn(t[e], x)) GE_APPLY(3, __fsub_rn(t[e], x))
+        }
+        break;
+      case OP_DIV:
+        switch (dst) {
+          GE_APPLY(0, __fdiv_rn(x, t[e])) GE_APPLY(1, __fdiv_rn(x, t[e]))
+          GE_APPLY(2, __fdiv_rn(x, t[e])) GE_APPLY(3, __fdiv_rn(x, t[e]))
+        }
+        break;
+      case OP_RDIV:
+        switch (dst) {
+          GE_APPLY(0, __fdiv_rn(t[e], x)) GE_APPLY(1, __fdiv_rn(t[e], x))
+          GE_APPLY(2, __fdiv_rn(t[e], x)) GE_APPLY(3, __fdiv_rn(t[e], x))
+        }
+        break;
+      case OP_MIN:
+        switch (dst) {
+          GE_APPLY(0, fminf(x, t[e])) GE_APPLY(1, fminf(x, t[e]))
+          GE_APPLY(2, fminf(x, t[e])) GE_APPLY(3, fminf(x, t[e]))
+        }
+        break;
+      case OP_MAX:
+        switch (dst) {
+          GE_APPLY(0, fmaxf(x, t[e])) GE_APPLY(1, fmaxf(x, t[e]))
+          GE_APPLY(2, fmaxf(x, t[e])) GE_APPLY(3, fmaxf(x, t[e]))
+        }
+        break;
       default:  // OP_STORE
         GE_DISPATCH_DTYPE(P.out_dtype[dst], mem.template store<DT_>(dst, t));
         break;
@@ -276,6 +324,8 @@ __device__ __forceinline__ void run_static_from(float (&r)[kRegs][C], const floa
         mem.template aux<SP::P.tma_aux_dtype[idx]>(idx, t);
       } else if constexpr (src == SRC_BCAST) {
         mem.template bcast<SP::P.bcast_dtype[idx]>(idx, t);
+      } else if constexpr (src == SRC_CBCAST) {
+        mem.template cbcast<SP::P.cbcast_dtype[idx]>(idx, t);
       } else {
         const float s = scalars[idx];
 #pragma unroll
@@ -289,6 +339,24 @@ __device__ __forceinline__ void run_static_from(float (&r)[kRegs][C], const floa
       } else if constexpr (op == OP_ADD) {
 #pragma unroll
         for (int e = 0; e < C; ++e) r[dst][e] = __fadd_rn(r[dst][e], t[e]);
+      } else if constexpr (op == OP_SUB) {
+#pragma unroll
+        for (int e = 0; e < C; ++e) r[dst][e] = __fsub_rn(r[dst][e], t[e]);
+      } else if constexpr (op == OP_RSUB) {
+#pragma unroll
+        for (int e = 0; e < C; ++e) r[dst][e] = __fsub_rn(t[e], r[dst][e]);
+      } else if constexpr (op == OP_DIV) {
+#pragma unroll
+        for (int e = 0; e < C; ++e) r[dst][e] = __fdiv_rn(r[dst][e], t[e]);
+      } else if constexpr (op == OP_RDIV) {
+#pragma unroll
+        for (int e = 0; e < C; ++e) r[dst][e] = __fdiv_rn(t[e], r[dst][e]);
+      } else if constexpr (op == OP_MIN) {
+#pragma unroll
+        for (int e = 0; e < C; ++e) r[dst][e] = fminf(r[dst][e], t[e]);
+      } else if constexpr (op == OP_MAX) {
+#pragma unroll
+        for (int e = 0; e < C; ++e) r[dst][e] = fmaxf(r[dst][e], t[e]);
       } else {
         mem.template store<SP::P.out_dtype[dst]>(dst, t);
       }

@@ -99,7 +99,9 @@ struct Waiter {
     if (kCluster ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
     for (uint32_t it = 1;; ++it) {
-      if (kCluster ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity)) return true;
+      if (kCluster ? mbar_try_wait_cluster(bar, parity)
+                   : mbar_try_wait_sleep(bar, parity, 20000u))
+        return true;
       if ((it & 3u) == 0u) {
         if (*abort_flag) return false;
         if (globaltimer_ns() - t0 > timeout_ns) {
@@ -132,6 +134,7 @@ struct FusedMem {
   const uint8_t *aux_stage;
   uint8_t *out_stage;
   int row, half, col0;
+  int grow;  // this lane's row within its batch (column-broadcast index)
   template <int DT>
   __device__ __forceinline__ void aux(uint32_t i, float (&t)[CH]) const {
     box_load<DT>(aux_stage + p->aux_off[i], row, half, t);
@@ -139,6 +142,12 @@ struct FusedMem {
   template <int DT>
   __device__ __forceinline__ void bcast(uint32_t i, float (&t)[CH]) const {
     row_load<DT, CH>(p->bcast_ptr[i], col0, p->N, t);
+  }
+  template <int DT>
+  __device__ __forceinline__ void cbcast(uint32_t i, float (&t)[CH]) const {
+    const float v = grow < p->M ? load_one<DT>(p->cbcast_ptr[i], grow) : 0.f;
+#pragma unroll
+    for (int e = 0; e < CH; ++e) t[e] = v;
   }
   template <int DT>
   __device__ __forceinline__ void store(uint32_t o, const float (&t)[CH]) const {
@@ -422,8 +431,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_epi_kernel(const __grid_cons
         uint8_t *ostage = out_w + obuf * p.out_stage_bytes;
         const uint8_t *astage = aux_w + (g % SA) * p.aux_stage_bytes;
         const int c0 = n0 + s * EW;
-        Epi::template run<CH>(p.prog, acc0, FusedMem{&p, astage, ostage, lane, 0, c0});
-        Epi::template run<CH>(p.prog, acc1, FusedMem{&p, astage, ostage, lane, 1, c0 + CH});
+        Epi::template run<CH>(p.prog, acc0, FusedMem{&p, astage, ostage, lane, 0, c0, m0 + lane});
+        Epi::template run<CH>(p.prog, acc1,
+                              FusedMem{&p, astage, ostage, lane, 1, c0 + CH, m0 + lane});
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) {

@@ -55,15 +55,16 @@ int validate_impl(const ge_dtypes *dt, const ge_dag *dag) {
 
   bool has_acc = false;
   int stored[GE_MAX_OUT] = {0};
-  int aux_kind[GE_MAX_AUX] = {0};  // 1 Load tensor, 2 Broadcast vector
+  int aux_kind[GE_MAX_AUX] = {0};  // 1 Load tensor, 2 row vector, 3 column vector
   for (int i = 0; i < dag->n; ++i) {
     const ge_node &nd = dag->node[i];
     switch (nd.op) {
       case GE_ACCFETCH: has_acc = true; break;
       case GE_LOAD:
-      case GE_BROADCAST: {
+      case GE_BROADCAST:
+      case GE_COL_BROADCAST: {
         if (nd.slot < 0 || nd.slot >= dt->n_aux) return GE_ERR_MISSING_ARG;
-        const int kind = nd.op == GE_LOAD ? 1 : 2;
+        const int kind = nd.op == GE_LOAD ? 1 : nd.op == GE_BROADCAST ? 2 : 3;
         if (aux_kind[nd.slot] && aux_kind[nd.slot] != kind) return GE_ERR_UNSUPPORTED;
         aux_kind[nd.slot] = kind;
         break;
@@ -73,6 +74,10 @@ int validate_impl(const ge_dtypes *dt, const ge_dag *dag) {
         break;
       case GE_MUL:
       case GE_ADD:
+      case GE_SUB:
+      case GE_DIV:
+      case GE_MIN:
+      case GE_MAX:
         if (!is_value_node(dag, nd.b, i)) return GE_ERR_SSA;
         if (!is_value_node(dag, nd.a, i)) return GE_ERR_SSA;
         break;
@@ -451,7 +456,7 @@ int check_run_args(const gemm_epi_plan *pl, const void *A, const void *B, const 
   if (pl->dt.n_scalar > 0 && !scalars) return GE_ERR_MISSING_ARG;
   if (!aligned16(A) || !aligned16(B)) return GE_ERR_MISALIGNED;
   const EpiProgram &P = pl->prog;
-  if ((P.n_tma_aux + P.n_bcast) > 0 && !aux) return GE_ERR_MISSING_ARG;
+  if ((P.n_tma_aux + P.n_bcast + P.n_cbcast) > 0 && !aux) return GE_ERR_MISSING_ARG;
   for (int t = 0; t < P.n_tma_aux; ++t) {
     const void *p = aux[P.tma_aux_slot[t]];
     if (!p) return GE_ERR_MISSING_ARG;
@@ -459,6 +464,11 @@ int check_run_args(const gemm_epi_plan *pl, const void *A, const void *B, const 
   }
   for (int b = 0; b < P.n_bcast; ++b) {
     const void *p = aux[P.bcast_slot[b]];
+    if (!p) return GE_ERR_MISSING_ARG;
+    if (!aligned16(p)) return GE_ERR_MISALIGNED;
+  }
+  for (int b = 0; b < P.n_cbcast; ++b) {
+    const void *p = aux[P.cbcast_slot[b]];
     if (!p) return GE_ERR_MISSING_ARG;
     if (!aligned16(p)) return GE_ERR_MISALIGNED;
   }
@@ -601,6 +611,7 @@ int gemm_epi_run(gemm_epi_plan *pl, const void *A, const void *B, const void *co
     pl->maps_ok = true;
   }
   for (int b = 0; b < P.n_bcast; ++b) kp.bcast_ptr[b] = aux[P.bcast_slot[b]];
+  for (int b = 0; b < P.n_cbcast; ++b) kp.cbcast_ptr[b] = aux[P.cbcast_slot[b]];
   for (int s = 0; s < pl->dt.n_scalar; ++s) kp.prog.scalars[s] = scalars[s];
   const cudaError_t e = launch_gemm(pl->lay, pl->epi, kp, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? GE_OK : GE_ERR_CUDA;
@@ -640,6 +651,8 @@ int gemm_epi_run_unfused(gemm_epi_plan *pl, const void *A, const void *B, const 
   ep.acc = static_cast<const float *>(workspace);
   for (int t = 0; t < P.n_tma_aux; ++t) ep.aux_ptr[t] = aux[P.tma_aux_slot[t]];
   for (int b = 0; b < P.n_bcast; ++b) ep.bcast_ptr[b] = aux[P.bcast_slot[b]];
+  for (int b = 0; b < P.n_cbcast; ++b) ep.cbcast_ptr[b] = aux[P.cbcast_slot[b]];
+  ep.M = static_cast<int32_t>(pl->M);
   for (int o = 0; o < pl->dt.n_out; ++o) ep.out_ptr[o] = outs[o];
   ep.prog = P;
   for (int i = 0; i < pl->dt.n_scalar; ++i) ep.prog.scalars[i] = scalars[i];

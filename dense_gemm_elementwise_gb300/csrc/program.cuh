@@ -18,7 +18,17 @@ namespace ge {
 // mul(alpha, accum) and mul(accum, alpha) compile to the same program
 // (fp32 multiply and add are commutative bit for bit).
 __host__ __device__ constexpr int src_rank(uint32_t src) {
-  return src == SRC_ACC ? 0 : src == SRC_AUX ? 1 : src == SRC_BCAST ? 2 : src == SRC_REG ? 3 : 4;
+  return src == SRC_ACC      ? 0
+         : src == SRC_AUX    ? 1
+         : src == SRC_BCAST  ? 2
+         : src == SRC_CBCAST ? 3
+         : src == SRC_REG    ? 4
+                             : 5;
+}
+
+__host__ __device__ constexpr bool is_binary(int op) {
+  return op == GE_MUL || op == GE_ADD || op == GE_SUB || op == GE_DIV || op == GE_MIN ||
+         op == GE_MAX;
 }
 
 struct CompileResult {
@@ -38,7 +48,7 @@ __host__ __device__ constexpr CompileResult compile_program(const ge_dtypes &dt,
   for (int i = 0; i < GE_MAX_NODES; ++i) last_use[i] = -1;
   for (int i = 0; i < n; ++i) {
     const ge_node &nd = dag.node[i];
-    if (nd.op == GE_MUL || nd.op == GE_ADD) {
+    if (is_binary(nd.op)) {
       last_use[nd.a] = i;
       last_use[nd.b] = i;
     } else if (nd.op == GE_RELU || nd.op == GE_STORE) {
@@ -47,7 +57,8 @@ __host__ __device__ constexpr CompileResult compile_program(const ge_dtypes &dt,
   }
   int tma_of_slot[GE_MAX_AUX] = {};
   int bc_of_slot[GE_MAX_AUX] = {};
-  for (int s = 0; s < GE_MAX_AUX; ++s) tma_of_slot[s] = bc_of_slot[s] = -1;
+  int cb_of_slot[GE_MAX_AUX] = {};
+  for (int s = 0; s < GE_MAX_AUX; ++s) tma_of_slot[s] = bc_of_slot[s] = cb_of_slot[s] = -1;
   uint32_t loc_src[GE_MAX_NODES] = {};
   uint32_t loc_idx[GE_MAX_NODES] = {};
   bool busy[kRegs] = {};
@@ -90,22 +101,49 @@ __host__ __device__ constexpr CompileResult compile_program(const ge_dtypes &dt,
         loc_idx[i] = static_cast<uint32_t>(bc_of_slot[nd.slot]);
         break;
       }
+      case GE_COL_BROADCAST: {
+        if (cb_of_slot[nd.slot] < 0) {
+          cb_of_slot[nd.slot] = P.n_cbcast;
+          P.cbcast_slot[P.n_cbcast] = nd.slot;
+          P.cbcast_dtype[P.n_cbcast] = dt.aux[nd.slot];
+          ++P.n_cbcast;
+        }
+        loc_src[i] = SRC_CBCAST;
+        loc_idx[i] = static_cast<uint32_t>(cb_of_slot[nd.slot]);
+        break;
+      }
       case GE_SCALAR:
         loc_src[i] = SRC_SCALAR;
         loc_idx[i] = static_cast<uint32_t>(nd.slot);
         break;
       case GE_MUL:
-      case GE_ADD: {
-        const uint32_t op = nd.op == GE_MUL ? OP_MUL : OP_ADD;
+      case GE_ADD:
+      case GE_SUB:
+      case GE_DIV:
+      case GE_MIN:
+      case GE_MAX: {
+        // two-address forms; subtraction and division have a reversed form
+        // for when the second operand's register is the one reused
+        const bool commutes = nd.op == GE_MUL || nd.op == GE_ADD || nd.op == GE_MIN ||
+                              nd.op == GE_MAX;
+        const uint32_t op = nd.op == GE_MUL   ? OP_MUL
+                            : nd.op == GE_ADD ? OP_ADD
+                            : nd.op == GE_SUB ? OP_SUB
+                            : nd.op == GE_DIV ? OP_DIV
+                            : nd.op == GE_MIN ? OP_MIN
+                                              : OP_MAX;
+        const uint32_t rop = nd.op == GE_SUB ? OP_RSUB : nd.op == GE_DIV ? OP_RDIV : op;
         const bool a_dies = loc_src[nd.a] == SRC_REG && last_use[nd.a] == i;
         const bool b_dies = loc_src[nd.b] == SRC_REG && last_use[nd.b] == i;
         int d = -1, other = -1;
-        if (a_dies && (!b_dies || loc_idx[nd.a] <= loc_idx[nd.b])) {
+        uint32_t emit_op = op;
+        if (a_dies && (!b_dies || loc_idx[nd.a] <= loc_idx[nd.b] || !commutes)) {
           d = static_cast<int>(loc_idx[nd.a]);
           other = nd.b;
         } else if (b_dies) {
           d = static_cast<int>(loc_idx[nd.b]);
           other = nd.a;
+          emit_op = rop;
         } else {
           for (int r = 0; r < kRegs; ++r)
             if (!busy[r]) {
@@ -121,13 +159,14 @@ __host__ __device__ constexpr CompileResult compile_program(const ge_dtypes &dt,
           int first = nd.a;
           other = nd.b;
           const int ra = src_rank(loc_src[nd.a]), rb = src_rank(loc_src[nd.b]);
-          if (rb < ra || (rb == ra && loc_idx[nd.b] < loc_idx[nd.a])) {
+          if (commutes && (rb < ra || (rb == ra && loc_idx[nd.b] < loc_idx[nd.a]))) {
             first = nd.b;
             other = nd.a;
           }
           P.ins[P.n_ins++] = pack_ins(OP_MOV, static_cast<uint32_t>(d), loc_src[first], loc_idx[first]);
         }
-        P.ins[P.n_ins++] = pack_ins(op, static_cast<uint32_t>(d), loc_src[other], loc_idx[other]);
+        P.ins[P.n_ins++] =
+            pack_ins(emit_op, static_cast<uint32_t>(d), loc_src[other], loc_idx[other]);
         const int refs[2] = {nd.a, nd.b};
         for (int k = 0; k < 2; ++k) {
           const int ref = refs[k];
@@ -182,8 +221,10 @@ __host__ __device__ constexpr CompileResult compile_program(const ge_dtypes &dt,
 // Same program (instructions and operand types); scalar values are run-time.
 __host__ __device__ constexpr bool same_program(const EpiProgram &a, const EpiProgram &b) {
   if (a.n_ins != b.n_ins || a.n_tma_aux != b.n_tma_aux || a.n_bcast != b.n_bcast ||
-      a.n_out != b.n_out)
+      a.n_cbcast != b.n_cbcast || a.n_out != b.n_out)
     return false;
+  for (int t = 0; t < a.n_cbcast; ++t)
+    if (a.cbcast_dtype[t] != b.cbcast_dtype[t]) return false;
   for (int i = 0; i < a.n_ins; ++i)
     if (a.ins[i] != b.ins[i]) return false;
   for (int t = 0; t < a.n_tma_aux; ++t)

@@ -26,6 +26,12 @@ struct GlobalMem {
     row_load<DT, kEwCols>(p->bcast_ptr[i], col0, p->N, t);
   }
   template <int DT>
+  __device__ __forceinline__ void cbcast(uint32_t i, float (&t)[kEwCols]) const {
+    const float v = load_one<DT>(p->cbcast_ptr[i], row % p->M);
+#pragma unroll
+    for (int e = 0; e < kEwCols; ++e) t[e] = v;
+  }
+  template <int DT>
   __device__ __forceinline__ void store(uint32_t o, const float (&t)[kEwCols]) const {
     char *base = static_cast<char *>(p->out_ptr[o]) + row * p->N * (DT == GE_F32 ? 4 : 2);
     row_store<DT, kEwCols>(base, col0, p->N, t);

@@ -7,9 +7,10 @@ GEMM or epilogue arithmetic; both the CUDA path (through the C-ABI binding)
 and the CPU oracle consume what it produces.
 
 DAG tuples are ``(op, a, b, slot)`` with ``op`` one of ``accum, load, scalar,
-broadcast, mul, add, relu, store``; ``a``/``b`` index earlier nodes; ``slot``
-selects the aux tensor (load, broadcast), the scalar (scalar) or the output
-(store).  Output slot 0 is D.
+broadcast, col_broadcast, mul, add, sub, div, min, max, relu, store``;
+``a``/``b`` index earlier nodes; ``slot`` selects the aux tensor (load, row or
+column broadcast), the scalar (scalar) or the output (store).  Output slot 0
+is D.
 """
 from dataclasses import dataclass, field
 from typing import List, Optional, Tuple
@@ -40,6 +41,21 @@ class Dag:
     def broadcast(self, slot):
         return self._add("broadcast", slot=slot)
 
+    def col_broadcast(self, slot):
+        return self._add("col_broadcast", slot=slot)
+
+    def sub(self, a, b):
+        return self._add("sub", a, b)
+
+    def div(self, a, b):
+        return self._add("div", a, b)
+
+    def minimum(self, a, b):
+        return self._add("min", a, b)
+
+    def maximum(self, a, b):
+        return self._add("max", a, b)
+
     def scalar(self, slot):
         return self._add("scalar", slot=slot)
 
@@ -64,7 +80,8 @@ class Workload:
     N: int
     K: int
     ab: str                                   # element type of A and B
-    aux: List[Tuple[str, str, str]]           # (name, "tensor" (L,M,N) | "row" (N,), dtype)
+    aux: List[tuple]                          # (name, "tensor" (L,M,N) | "row" (N,) |
+                                              #  "col" (M,), dtype[, "pow2"])
     scalars: List[Tuple[str, float]]          # (name, value)
     outs: List[Tuple[str, str]]               # (name, dtype); outs[0] is D
     dag: List[Tuple[str, int, int, int]]
@@ -82,8 +99,9 @@ class Workload:
         """Read A, B and each aux once; write each output once."""
         L, M, N, K = self.L, self.M, self.N, self.K
         b = (L * M * K + L * K * N) * ESIZE[self.ab]
-        for _, kind, dt in self.aux:
-            b += (L * M * N if kind == "tensor" else N) * ESIZE[dt]
+        for spec in self.aux:
+            kind, dt = spec[1], spec[2]
+            b += {"tensor": L * M * N, "row": N, "col": M}[kind] * ESIZE[dt]
         for _, dt in self.outs:
             b += L * M * N * ESIZE[dt]
         return b
@@ -202,6 +220,46 @@ def dag_identity():
     return g.nodes
 
 
+def dag_row_col_bias():
+    """D = (accum*alpha) + row_bias + col_bias ("Custom epilogue fusions for
+    GEMMs", cell [9]: row bias (N,) and column bias (M, 1) in one epilogue)."""
+    g = Dag()
+    acc = g.accum()
+    t = g.add(g.mul(acc, g.scalar(0)), g.broadcast(0))
+    g.store(g.add(t, g.col_broadcast(1)), 0)
+    return g.nodes
+
+
+def dag_aux_normalize():
+    """D = accum / aux ("Defining an epilogue via a Python function",
+    aux_normalize)."""
+    g = Dag()
+    g.store(g.div(g.accum(), g.load(0)), 0)
+    return g.nodes
+
+
+def dag_scale_shift():
+    """tmp = accum*2.0 ; tmp2 = tmp - 1.0 ; D = tmp2 / 4.0 ; returns D, tmp
+    (the computation of the SSA failure example, cell [12], written with a new
+    name for the second assignment as single assignment requires)."""
+    g = Dag()
+    tmp = g.mul(g.accum(), g.scalar(0))
+    tmp2 = g.sub(tmp, g.scalar(1))
+    g.store(g.div(tmp2, g.scalar(2)), 0)
+    g.store(tmp, 1)
+    return g.nodes
+
+
+def dag_clamp():
+    """D = min(max(alpha*accum - C, lo), hi): subtraction and binary
+    maximum/minimum ("Defining an epilogue via a Python function")."""
+    g = Dag()
+    t = g.sub(g.mul(g.scalar(0), g.accum()), g.load(0))
+    t = g.maximum(t, g.scalar(1))
+    g.store(g.minimum(t, g.scalar(2)), 0)
+    return g.nodes
+
+
 # ----------------------------------------------------------- workloads ----
 
 def my_epilogue(L, M, N, K, seed=2025, name=None):
@@ -278,6 +336,24 @@ def page_examples(L=1, M=256, N=256, K=256):
         Workload(name="identity_f32_out", L=L, M=M, N=N, K=K, ab="f16", aux=[], scalars=[],
                  outs=[("D", "f32")], dag=dag_identity(), dist="ceil_uniform", seed=1234,
                  exact=True, cite="Python examples walkthrough: basic GEMM (f32 accumulate)"),
+        Workload(name="row_col_bias_f16", L=L, M=M, N=N, K=K, ab="f16",
+                 aux=[("row_bias", "row", "f16"), ("col_bias", "col", "f16")],
+                 scalars=[("alpha", 1.0)], outs=[("D", "f16")], dag=dag_row_col_bias(),
+                 dist="randint", seed=2025, exact=True,
+                 cite="Custom epilogue fusions for GEMMs, cell [9]"),
+        Workload(name="aux_normalize_f16", L=L, M=M, N=N, K=K, ab="f16",
+                 aux=[("aux", "tensor", "f16", "pow2")], scalars=[], outs=[("D", "f16")],
+                 dag=dag_aux_normalize(), dist="randint", seed=2025, exact=True,
+                 cite="Defining an epilogue via a Python function: aux_normalize"),
+        Workload(name="scale_shift_bf16", L=L, M=M, N=N, K=K, ab="bf16", aux=[],
+                 scalars=[("two", 2.0), ("one", 1.0), ("four", 4.0)],
+                 outs=[("D", "f32"), ("tmp", "bf16")], dag=dag_scale_shift(), dist="randint",
+                 seed=2025, exact=True,
+                 cite="Custom epilogue fusions for GEMMs, cell [12] (computation only)"),
+        Workload(name="clamp_f16", L=L, M=M, N=N, K=K, ab="f16", aux=[("C", "tensor", "f16")],
+                 scalars=[("alpha", 1.0), ("lo", -3.0), ("hi", 5.5)], outs=[("D", "f16")],
+                 dag=dag_clamp(), dist="randint", seed=2025, exact=True,
+                 cite="Defining an epilogue via a Python function: binary min and max"),
     ]
 
 
@@ -295,13 +371,14 @@ def make_inputs(w: Workload):
     * ``ceil_uniform``: numpy RandomState, ceil(uniform(-4, 4) cast to fp16),
       the basic-GEMM notebook's recipe;
     * ``normal``: N(0, 1) from torch's CPU generator, rounded to the type.
-    Operands are drawn in the order A, B, then the aux slots.
+    Operands are drawn in the order A, B, then the aux slots; aux slots marked
+    "pow2" (divisors) are then redrawn from +-{1, 2, 4}.
     """
     L, M, N, K = w.L, w.M, w.N, w.K
     shapes = [(L, M, K), (L, K, N)]
-    for _, kind, _dt in w.aux:
-        shapes.append((L, M, N) if kind == "tensor" else (N,))
-    dts = [w.ab, w.ab] + [dt for _, _, dt in w.aux]
+    for spec in w.aux:
+        shapes.append({"tensor": (L, M, N), "row": (N,), "col": (M,)}[spec[1]])
+    dts = [w.ab, w.ab] + [spec[2] for spec in w.aux]
     out = []
     if w.dist == "randint":
         g = torch.Generator().manual_seed(w.seed)
@@ -321,6 +398,14 @@ def make_inputs(w: Workload):
         raise ValueError(w.dist)
     A, B = out[0].contiguous(), out[1].contiguous()
     aux = [t.contiguous() for t in out[2:]]
+    # divisor operands ("pow2"): nonzero powers of two, +-{1, 2, 4}, so a
+    # division by them is exact in every precision
+    g2 = torch.Generator().manual_seed(w.seed + 1)
+    for k, spec in enumerate(w.aux):
+        if len(spec) > 3 and spec[3] == "pow2":
+            mag = torch.pow(2.0, torch.randint(0, 3, aux[k].shape, generator=g2).float())
+            sgn = torch.randint(0, 2, aux[k].shape, generator=g2).float() * 2 - 1
+            aux[k] = (mag * sgn).to(aux[k].dtype).contiguous()
     scalars = [float(v) for _, v in w.scalars]
     return A, B, aux, scalars
 

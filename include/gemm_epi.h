@@ -10,10 +10,10 @@
  * accum, is transformed by a user epilogue before it is stored; outputs D and
  * Aux, cells [2]-[5]) and "How the epilogue fusion API works" (the epilogue
  * as a DAG of AccFetch, Load, compute and Store nodes).  The node set here is
- * that figure's plus Scalar, row Broadcast (section "Row and column
- * broadcasts") and ReLU (section "Defining an epilogue via a Python
- * function": predefined activations; "Custom Epilogue Example", section
- * "Activation Functions").
+ * that figure's plus Scalar, row and column Broadcast (section "Row and
+ * column broadcasts"), subtraction, division, minimum and maximum, and ReLU
+ * (section "Defining an epilogue via a Python function": supported
+ * operations; "Custom Epilogue Example", section "Activation Functions").
  *
  * Conventions shared by every entry point
  * ---------------------------------------
@@ -21,7 +21,9 @@
  *      A      (L, M, K)   K contiguous
  *      B      (L, K, N)   N contiguous
  *      aux tensors and outputs (L, M, N), N contiguous
- *      row-broadcast vectors (N,), one vector for every row of every batch.
+ *      row-broadcast vectors (N,), one vector for every row of every batch;
+ *      column-broadcast vectors (M,) (the pages' (M, 1)), one value per row,
+ *      the same for every column and every batch.
  *  * Every device pointer must be 16-byte aligned and every row of a 2-D/3-D
  *    operand must be a multiple of 16 bytes long ("Custom Epilogue Example",
  *    section "Constraints": contiguous dimensions 16-byte aligned).
@@ -64,7 +66,12 @@ typedef enum {
   GE_MUL = 4,       /* v[a] * v[b]                                           */
   GE_ADD = 5,       /* v[a] + v[b]                                           */
   GE_RELU = 6,      /* v[a] > 0 ? v[a] : +0                                  */
-  GE_STORE = 7      /* out slot `slot` = round(v[a]); slot 0 is D            */
+  GE_STORE = 7,     /* out slot `slot` = round(v[a]); slot 0 is D            */
+  GE_SUB = 8,       /* v[a] - v[b]                                           */
+  GE_DIV = 9,       /* v[a] / v[b]  (fp32, correctly rounded)                */
+  GE_MIN = 10,      /* min(v[a], v[b])                                       */
+  GE_MAX = 11,      /* max(v[a], v[b])                                       */
+  GE_COL_BROADCAST = 12 /* aux slot `slot`, an (M,) column vector: aux[i]    */
 } ge_op;
 
 typedef struct {

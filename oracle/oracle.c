@@ -203,9 +203,14 @@ static void *row_worker(void *p) {
             v[n] = decode(jb->aux_type[nd->slot], jb->aux[nd->slot], (l * M + i) * N + j);
             break;
           case ORC_BCAST: v[n] = decode(jb->aux_type[nd->slot], jb->aux[nd->slot], j); break;
+          case ORC_COLBCAST: v[n] = decode(jb->aux_type[nd->slot], jb->aux[nd->slot], i); break;
           case ORC_SCALAR: v[n] = jb->scalars[nd->slot]; break;
           case ORC_MUL: v[n] = v[nd->a] * v[nd->b]; break;
           case ORC_ADD: v[n] = v[nd->a] + v[nd->b]; break;
+          case ORC_SUB: v[n] = v[nd->a] - v[nd->b]; break;
+          case ORC_DIV: v[n] = v[nd->a] / v[nd->b]; break;
+          case ORC_MIN: v[n] = v[nd->b] < v[nd->a] ? v[nd->b] : v[nd->a]; break;
+          case ORC_MAX: v[n] = v[nd->b] > v[nd->a] ? v[nd->b] : v[nd->a]; break;
           case ORC_RELU: v[n] = v[nd->a] > 0.0 ? v[nd->a] : 0.0; break;
           case ORC_STORE:
             encode(jb->out_type[nd->slot], jb->outs[nd->slot], out_row * N + j, v[nd->a]);
@@ -233,6 +238,7 @@ static int validate_dag(int32_t n_nodes, const orc_node *nodes, int32_t n_aux, i
       case ORC_ACCUM: break;
       case ORC_LOAD:
       case ORC_BCAST:
+      case ORC_COLBCAST:
         if (nd->slot < 0 || nd->slot >= n_aux) return ORC_BAD_DAG;
         break;
       case ORC_SCALAR:
@@ -240,6 +246,10 @@ static int validate_dag(int32_t n_nodes, const orc_node *nodes, int32_t n_aux, i
         break;
       case ORC_MUL:
       case ORC_ADD:
+      case ORC_SUB:
+      case ORC_DIV:
+      case ORC_MIN:
+      case ORC_MAX:
         if (nd->b < 0 || nd->b >= n || nodes[nd->b].op == ORC_STORE) return ORC_BAD_DAG;
         /* fall through: operand a */
       case ORC_RELU:

@@ -30,6 +30,14 @@
  *   ORC_ADD a b    -> v[a] + v[b]
  *   ORC_RELU a     -> v[a] > 0 ? v[a] : +0    ("Custom Epilogue Example",
  *                                              section "Activation Functions")
+ *   ORC_SUB a b    -> v[a] - v[b]             (same page as the DAG, section
+ *   ORC_DIV a b    -> v[a] / v[b]              "Defining an epilogue via a Python
+ *   ORC_MIN a b    -> v[b] < v[a] ? v[b] : v[a]  function": tensor-tensor and
+ *   ORC_MAX a b    -> v[b] > v[a] ? v[b] : v[a]  scalar add/sub/mul/div, binary
+ *                                              minimum and maximum)
+ *   ORC_COLBCAST s -> aux_s[i]                (column broadcast: shape (M,) or
+ *                                              (M, 1), the same for every column
+ *                                              j and batch l)
  *   ORC_STORE a s  -> out_s[l,i,j] = round_to_nearest_even(type_s, v[a])
  *
  * Only a store rounds; every intermediate value stays in fp64 (the pages run
@@ -64,7 +72,12 @@ enum {
   ORC_MUL = 4,
   ORC_ADD = 5,
   ORC_RELU = 6,
-  ORC_STORE = 7
+  ORC_STORE = 7,
+  ORC_SUB = 8,
+  ORC_DIV = 9,
+  ORC_MIN = 10,
+  ORC_MAX = 11,
+  ORC_COLBCAST = 12
 };
 
 typedef struct {
@@ -97,7 +110,8 @@ uint16_t orc_f64_to_bf16(double x);
  *  B              L*K*N codes, row-major (l, k, j)
  *  n_aux          number of aux slots; aux_type[s] in {F16, BF16, F32}
  *  aux[s]         LOAD slots: L*M*N elements row-major (l, i, j);
- *                 BCAST slots: N elements; raw codes for F16/BF16, float for F32
+ *                 BCAST slots: N elements; COLBCAST slots: M elements;
+ *                 raw codes for F16/BF16, float for F32
  *  n_scalar       number of scalars; scalars[s] as double
  *  n_nodes,nodes  the DAG in topological (single assignment) order
  *  n_out          number of outputs; out_type[o] in {F16, BF16, F32}

@@ -17,7 +17,7 @@ SENTINEL32 = 0x7FC05A5A
 
 
 def dtypes_of(w):
-    return B.make_dtypes(w.ab, [dt for _, _, dt in w.aux], len(w.scalars),
+    return B.make_dtypes(w.ab, [s[2] for s in w.aux], len(w.scalars),
                          [dt for _, dt in w.outs])
 
 
@@ -75,7 +75,7 @@ def run_gpu(w, inputs, options=None, unfused=False, stream=None, repeat=1):
 def oracle_rows(w, inputs, rows=None):
     A, Bm, aux, scalars = inputs
     outs, _ = oracle.gemm_epilogue(w.L, w.M, w.N, w.K, w.ab, W.to_codes(A), W.to_codes(Bm),
-                                   [W.to_codes(a) for a in aux], [dt for _, _, dt in w.aux],
+                                   [W.to_codes(a) for a in aux], [s[2] for s in w.aux],
                                    scalars, w.dag, [dt for _, dt in w.outs], rows=rows,
                                    threads=oracle.threads_default())
     return outs

@@ -113,7 +113,7 @@ def eval_dag_exact(dag, acc, aux_vals, scalars, n_out):
     for n, (op, a, b, s) in enumerate(dag):
         if op == "accum":
             v[n] = acc
-        elif op in ("load", "broadcast"):
+        elif op in ("load", "broadcast", "col_broadcast"):
             v[n] = aux_vals[s]
         elif op == "scalar":
             v[n] = Fraction(scalars[s])
@@ -121,6 +121,14 @@ def eval_dag_exact(dag, acc, aux_vals, scalars, n_out):
             v[n] = v[a] * v[b]
         elif op == "add":
             v[n] = v[a] + v[b]
+        elif op == "sub":
+            v[n] = v[a] - v[b]
+        elif op == "div":
+            v[n] = v[a] / v[b]
+        elif op == "min":
+            v[n] = min(v[a], v[b])
+        elif op == "max":
+            v[n] = max(v[a], v[b])
         elif op == "relu":
             v[n] = v[a] if v[a] > 0 else Fraction(0)
         elif op == "store":
@@ -137,7 +145,7 @@ def zero_norm(codes):
 
 def run_oracle(L_, w, A, B, aux, scalars, rows=None, threads=0, want_pre=False):
     return oracle.gemm_epilogue(w.L, w.M, w.N, w.K, w.ab, W.to_codes(A), W.to_codes(B),
-                                [W.to_codes(a) for a in aux], [dt for _, _, dt in w.aux],
+                                [W.to_codes(a) for a in aux], [s[2] for s in w.aux],
                                 scalars, w.dag, [dt for _, dt in w.outs], rows=rows,
                                 threads=threads, want_pre=want_pre, lib_handle=L_)
 
@@ -228,6 +236,9 @@ def _golden_cases():
         "bias_relu_square_2x2x2x2.json": (W.dag_bias_relu_square(),
                                           [("C", "tensor", "bf16"), ("bias", "row", "f32")],
                                           [("D", "bf16"), ("E", "bf16")]),
+        "row_col_bias_2x2x2.json": (W.dag_row_col_bias(),
+                                    [("row_bias", "row", "f16"), ("col_bias", "col", "f16")],
+                                    [("D", "f16")]),
     }
     for fname, (dag, aux_spec, outs) in dags.items():
         with open(os.path.join(GOLDEN, fname)) as f:
@@ -282,6 +293,37 @@ def pin_integer_closed_form(L_):
     assert np.array_equal(np_decode(D, "f16"), ref.astype(np.float64))
 
 
+def pin_new_ops_closed_form(L_):
+    """Integer inputs through subtraction, division by powers of two, min,
+    max and row + column broadcasts: the exact results, computed in numpy."""
+    ex = {x.name: x for x in W.page_examples()}
+    w = small(ex["row_col_bias_f16"], L=2, M=12, N=24, K=40)
+    (A, B, aux, sc), Ai, Bi, (rb, cb) = _int_inputs(w)
+    acc = np.einsum("lik,lkj->lij", Ai, Bi)
+    ref = (acc + rb[None, None, :] + cb[None, :, None]).reshape(-1, w.N)
+    (D,), _ = run_oracle(L_, w, A, B, aux, sc)
+    assert np.array_equal(np_decode(D, "f16"), ref.astype(np.float64))
+    w = small(ex["clamp_f16"], L=2, M=10, N=16, K=24)
+    (A, B, aux, sc), Ai, Bi, (Ci,) = _int_inputs(w)
+    acc = np.einsum("lik,lkj->lij", Ai, Bi)
+    ref = np.minimum(np.maximum(acc - Ci, -3.0), 5.5).reshape(-1, w.N)
+    (D,), _ = run_oracle(L_, w, A, B, aux, sc)
+    assert np.array_equal(np_decode(D, "f16"), ref)
+    w = small(ex["aux_normalize_f16"], L=1, M=8, N=16, K=24)
+    A, B, aux, sc = W.make_inputs(w)
+    acc = np.einsum("lik,lkj->lij", A.double().numpy(), B.double().numpy())
+    ref = (acc / aux[0].double().numpy()).reshape(-1, w.N)
+    assert set(np.unique(np.abs(aux[0].double().numpy()))) <= {1.0, 2.0, 4.0}
+    (D,), _ = run_oracle(L_, w, A, B, aux, sc)
+    assert np.array_equal(np_decode(D, "f16"), ref)
+    w = small(ex["scale_shift_bf16"], L=1, M=8, N=16, K=24)
+    A, B, aux, sc = W.make_inputs(w)
+    acc = np.einsum("lik,lkj->lij", A.double().numpy(), B.double().numpy()).reshape(-1, w.N)
+    (D, T), _ = run_oracle(L_, w, A, B, aux, sc)
+    assert np.array_equal(D.astype(np.float64), (acc * 2 - 1) / 4)
+    assert np.array_equal(np_decode(T, "bf16"), acc * 2)
+
+
 def pin_broadcast_closed_form(L_):
     """Row-broadcast bias indexed by column j, same vector for every row and
     batch: integer inputs, D = relu(0.5*A@B + C + bias), E = D*D rounded."""
@@ -304,9 +346,9 @@ def _exact_case(L_, w, rs):
     A = torch.randn(L, M, K, generator=g).to(W.TORCH_DTYPE[w.ab])
     B = torch.randn(L, K, N, generator=g).to(W.TORCH_DTYPE[w.ab])
     aux = []
-    for _, kind, dt in w.aux:
-        shp = (L, M, N) if kind == "tensor" else (N,)
-        aux.append(torch.randn(shp, generator=g).to(W.TORCH_DTYPE[dt]))
+    for spec in w.aux:
+        shp = {"tensor": (L, M, N), "row": (N,), "col": (M,)}[spec[1]]
+        aux.append(torch.randn(shp, generator=g).to(W.TORCH_DTYPE[spec[2]]))
     scalars = [float(np.float32(v)) for v in rs.uniform(-3, 3, len(w.scalars))]
     outs, _ = run_oracle(L_, w, A, B, aux, scalars)
     Af = [[[Fraction(float(x)) for x in r] for r in m] for m in A.double().tolist()]
@@ -317,8 +359,10 @@ def _exact_case(L_, w, rs):
             for j in range(N):
                 acc = sum(Af[l][i][k] * Bf[l][k][j] for k in range(K))
                 av = []
-                for (_, kind, _dt), a in zip(w.aux, auxf):
-                    av.append(Fraction(float(a[l, i, j] if kind == "tensor" else a[j])))
+                for spec, a in zip(w.aux, auxf):
+                    sel = {"tensor": lambda: a[l, i, j], "row": lambda: a[j],
+                           "col": lambda: a[i]}[spec[1]]()
+                    av.append(Fraction(float(sel)))
                 want = eval_dag_exact(w.dag, acc, av, scalars, len(w.outs))
                 for o, (_, dt) in enumerate(w.outs):
                     got = outs[o][l * M + i, j]
@@ -398,7 +442,8 @@ def pin_rows_and_threads(L_):
 
 ALL_PINS = [pin_decode_exhaustive, pin_encode_roundtrip, pin_encode_midpoints,
             pin_encode_random_vs_table, pin_golden, pin_integer_closed_form,
-            pin_broadcast_closed_form, pin_fraction_brute_force, pin_special_cases,
+            pin_broadcast_closed_form, pin_new_ops_closed_form, pin_fraction_brute_force,
+            pin_special_cases,
             pin_relu_positive_zero, pin_rows_and_threads]
 
 

@@ -41,7 +41,7 @@ def test_status_strings():
 
 
 def _dt(w):
-    return B.make_dtypes(w.ab, [dt for _, _, dt in w.aux], len(w.scalars), [dt for _, dt in w.outs])
+    return B.make_dtypes(w.ab, [s[2] for s in w.aux], len(w.scalars), [dt for _, dt in w.outs])
 
 
 @pytest.mark.parametrize("w", W.CONFIGS + W.page_examples(), ids=lambda w: w.name)

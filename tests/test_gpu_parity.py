@@ -228,3 +228,43 @@ def test_builtin_and_interpreter_agree_bitwise(w, variant):
         debug_flags=B.GE_DEBUG_FORCE_INTERPRETER, **base))
     _gpu.bitwise_equal(fast, slow_unfused)
     _gpu.compare(w, fast, _gpu.oracle_rows(w, inputs))
+
+
+# ------------------------------------------------- wider node set --
+
+def _reverse_ops_workload():
+    """Exercises the two-address compiler's reversed forms: C - alpha*accum
+    and C / (beta*X) reuse the register of their second operand."""
+    g = W.Dag()
+    acc = g.accum()
+    t = g.mul(acc, g.scalar(0))
+    c = g.load(0)
+    u = g.sub(c, t)
+    v = g.mul(g.load(1), g.scalar(1))
+    w_ = g.div(c, v)
+    g.store(g.minimum(u, w_), 0)
+    g.store(u, 1)
+    return W.Workload(name="reverse_ops", L=2, M=264, N=392, K=200, ab="f16",
+                      aux=[("C", "tensor", "f16"), ("X", "tensor", "f16", "pow2")],
+                      scalars=[("alpha", 1.0), ("beta", 2.0)],
+                      outs=[("D", "f16"), ("U", "f16")], dag=g.nodes, dist="randint", seed=31,
+                      exact=True)
+
+
+@pytest.mark.parametrize("variant", [(1, 128, 1), (2, 256, 1)], ids=vid)
+def test_reversed_sub_div_and_min(variant):
+    w = _reverse_ops_workload()
+    inputs = W.make_inputs(w)
+    gpu, info = _gpu.run_gpu(w, inputs, options=opts(variant))
+    assert info["epi_variant"] == -1  # not a catalog entry: the interpreter
+    _gpu.compare(w, gpu, _gpu.oracle_rows(w, inputs))
+    unf, _ = _gpu.run_gpu(w, inputs, unfused=True, options=opts(variant))
+    _gpu.bitwise_equal(gpu, unf)
+
+
+def test_row_col_bias_uses_catalog():
+    w = [x for x in W.page_examples(L=2, M=300, N=264, K=136) if x.name == "row_col_bias_f16"][0]
+    inputs = W.make_inputs(w)
+    gpu, info = _gpu.run_gpu(w, inputs)
+    assert info["epi_variant"] >= 0
+    _gpu.compare(w, gpu, _gpu.oracle_rows(w, inputs))

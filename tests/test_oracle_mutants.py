@@ -43,6 +43,17 @@ MUTANTS = [
     ("subnormal_threshold", "if (ax < ldexp(1.0, emin)) {", "if (ax < ldexp(1.0, emin - 1)) {"),
     ("f32_store_via_f16", "default: ((float *)base)[idx] = (float)v; break;",
      "default: ((float *)base)[idx] = (float)orc_f16_to_f64(orc_f64_to_f16(v)); break;"),
+    ("sub_operands_swapped", "case ORC_SUB: v[n] = v[nd->a] - v[nd->b];",
+     "case ORC_SUB: v[n] = v[nd->b] - v[nd->a];"),
+    ("div_operands_swapped", "case ORC_DIV: v[n] = v[nd->a] / v[nd->b];",
+     "case ORC_DIV: v[n] = v[nd->b] / v[nd->a];"),
+    ("min_as_max", "case ORC_MIN: v[n] = v[nd->b] < v[nd->a] ? v[nd->b] : v[nd->a];",
+     "case ORC_MIN: v[n] = v[nd->b] > v[nd->a] ? v[nd->b] : v[nd->a];"),
+    ("max_returns_first", "case ORC_MAX: v[n] = v[nd->b] > v[nd->a] ? v[nd->b] : v[nd->a];",
+     "case ORC_MAX: v[n] = v[nd->a];"),
+    ("col_broadcast_by_column",
+     "case ORC_COLBCAST: v[n] = decode(jb->aux_type[nd->slot], jb->aux[nd->slot], i);",
+     "case ORC_COLBCAST: v[n] = decode(jb->aux_type[nd->slot], jb->aux[nd->slot], j % M);"),
 ]
 
 
