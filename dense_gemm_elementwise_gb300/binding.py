@@ -13,7 +13,8 @@ from . import build as _build
 
 GE_F16, GE_BF16, GE_F32 = 0, 1, 2
 (GE_ACCFETCH, GE_LOAD, GE_SCALAR, GE_BROADCAST, GE_MUL, GE_ADD, GE_RELU, GE_STORE, GE_SUB, GE_DIV,
- GE_MIN, GE_MAX, GE_COL_BROADCAST) = range(13)
+ GE_MIN, GE_MAX, GE_COL_BROADCAST, GE_SIGMOID, GE_TANH, GE_GELU, GE_SILU, GE_HARDSWISH,
+ GE_LEAKY_RELU) = range(19)
 GE_MAX_NODES, GE_MAX_AUX, GE_MAX_TMA_AUX, GE_MAX_OUT, GE_MAX_SCALARS = 16, 8, 4, 4, 16
 GE_DEBUG_SKIP_FIRST_LOAD = 1
 GE_DEBUG_FORCE_INTERPRETER = 2
@@ -27,7 +28,9 @@ for _i, _n in enumerate(STATUS):
 DTYPE = {"f16": GE_F16, "bf16": GE_BF16, "f32": GE_F32}
 OP = {"accum": GE_ACCFETCH, "load": GE_LOAD, "scalar": GE_SCALAR, "broadcast": GE_BROADCAST,
       "mul": GE_MUL, "add": GE_ADD, "relu": GE_RELU, "store": GE_STORE, "sub": GE_SUB,
-      "div": GE_DIV, "min": GE_MIN, "max": GE_MAX, "col_broadcast": GE_COL_BROADCAST}
+      "div": GE_DIV, "min": GE_MIN, "max": GE_MAX, "col_broadcast": GE_COL_BROADCAST,
+      "sigmoid": GE_SIGMOID, "tanh": GE_TANH, "gelu": GE_GELU, "silu": GE_SILU,
+      "hardswish": GE_HARDSWISH, "leaky_relu": GE_LEAKY_RELU}
 
 # exported symbols of include/gemm_epi.h
 EXPORTS = ["gemm_epi_plan_create", "gemm_epi_plan_create_ex", "gemm_epi_validate", "gemm_epi_run",

@@ -8,7 +8,8 @@
 // values are free) uses that entry's kernels, any other DAG the interpreter.
 // The entries cover the common fused epilogues of the pages: storing the
 // accumulator, linear combinations with an aux tensor, ReLU, row-broadcast
-// bias, auxiliary outputs and a squared second output.
+// bias, auxiliary outputs, a squared second output and GELU over a linear
+// combination.
 #pragma once
 
 #include "program.cuh"
@@ -24,7 +25,8 @@ struct Entry {
 
 constexpr ge_node nd(int op, int a = 0, int b = 0, int slot = 0) { return ge_node{op, a, b, slot}; }
 
-constexpr ge_dtypes types(int n_aux, int aux0, int aux1, int n_scalar, int n_out, int out0, int out1) {
+constexpr ge_dtypes types(int n_aux, int aux0, int aux1, int n_scalar, int n_out, int out0, int out1,
+                          int aux2 = 0) {
   ge_dtypes d{};
   d.ab = GE_F16;  // A/B type is a kernel parameter, not part of the program
   d.acc = GE_F32;
@@ -33,6 +35,7 @@ constexpr ge_dtypes types(int n_aux, int aux0, int aux1, int n_scalar, int n_out
   d.n_out = n_out;
   d.aux[0] = aux0;
   d.aux[1] = aux1;
+  d.aux[2] = aux2;
   d.out[0] = out0;
   d.out[1] = out1;
   return d;
@@ -98,6 +101,21 @@ constexpr ge_dag dag_row_col_bias() {
                  nd(GE_STORE, 6, 0, 0)}};
 }
 
+// D = gelu(alpha*accum + C)
+constexpr ge_dag dag_linear_gelu() {
+  return ge_dag{7,
+                {nd(GE_ACCFETCH), nd(GE_SCALAR, 0, 0, 0), nd(GE_MUL, 0, 1), nd(GE_LOAD, 0, 0, 0),
+                 nd(GE_ADD, 2, 3), nd(GE_GELU, 4), nd(GE_STORE, 5, 0, 0)}};
+}
+
+// D = gelu((accum + bias)*scale + c + tanh(x))
+constexpr ge_dag dag_complex_gelu_tanh() {
+  return ge_dag{12,
+                {nd(GE_ACCFETCH), nd(GE_BROADCAST, 0, 0, 2), nd(GE_ADD, 0, 1), nd(GE_SCALAR, 0, 0, 0),
+                 nd(GE_MUL, 2, 3), nd(GE_LOAD, 0, 0, 0), nd(GE_ADD, 4, 5), nd(GE_LOAD, 0, 0, 1),
+                 nd(GE_TANH, 7), nd(GE_ADD, 6, 8), nd(GE_GELU, 9), nd(GE_STORE, 10, 0, 0)}};
+}
+
 constexpr Entry kEntries[] = {
     {"store_accum_f32", types(0, 0, 0, 0, 1, GE_F32, 0), dag_store_accum()},
     {"store_accum_f16", types(0, 0, 0, 0, 1, GE_F16, 0), dag_store_accum()},
@@ -110,6 +128,9 @@ constexpr Entry kEntries[] = {
      dag_bias_relu_square()},
     {"row_bias_f16", types(1, GE_F16, 0, 1, 1, GE_F16, 0), dag_row_bias()},
     {"row_col_bias_f16", types(2, GE_F16, GE_F16, 1, 1, GE_F16, 0), dag_row_col_bias()},
+    {"linear_gelu_f16", types(1, GE_F16, 0, 1, 1, GE_F16, 0), dag_linear_gelu()},
+    {"complex_gelu_tanh_bf16", types(3, GE_BF16, GE_BF16, 1, 1, GE_BF16, 0, GE_F32),
+     dag_complex_gelu_tanh()},
 };
 
 constexpr int kCount = static_cast<int>(sizeof(kEntries) / sizeof(kEntries[0]));

@@ -38,6 +38,14 @@ enum EpiOp : uint32_t {
   OP_RDIV = 8,   // r[dst]  = src / r[dst]
   OP_MIN = 9,    // r[dst]  = min(r[dst], src)
   OP_MAX = 10,   // r[dst]  = max(r[dst], src)
+  // activations read their operand from any source: r[dst] = f(src)
+  OP_SIGMOID = 11,
+  OP_TANH = 12,
+  OP_GELU = 13,
+  OP_SILU = 14,
+  OP_HARDSWISH = 15,
+  OP_LEAKY = 16,   // r[dst]  = r[dst] > 0 ? r[dst] : src * r[dst]   (src: slope)
+  OP_RLEAKY = 17,  // r[dst]  = src > 0 ? src : r[dst] * src         (r[dst]: slope)
 };
 
 enum EpiSrc : uint32_t {

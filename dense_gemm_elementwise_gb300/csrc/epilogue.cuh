@@ -192,6 +192,43 @@ __device__ __forceinline__ float load_one(const void *base, int64_t i) {
     }                               \
   } while (0)
 
+// ------------------------------------------------------------ activations --
+// fp32 evaluations of the activation registry's functions through the CUDA
+// math library (expf, tanhf, erfcf); every other step correctly rounded.
+constexpr float kRsqrt2 = 0.70710678118654752440f;  // 1/sqrt(2)
+
+__device__ __forceinline__ float act_sigmoid(float x) { return __fdiv_rn(1.f, __fadd_rn(1.f, expf(-x))); }
+__device__ __forceinline__ float act_tanh(float x) { return tanhf(x); }
+// 1 + erf(z) = erfc(-z); erfc keeps the relative accuracy of the far
+// negative tail, where 1 + erf(z) cancels to 0
+__device__ __forceinline__ float act_gelu(float x) {
+  return __fmul_rn(__fmul_rn(0.5f, x), erfcf(__fmul_rn(-x, kRsqrt2)));
+}
+__device__ __forceinline__ float act_silu(float x) { return __fdiv_rn(x, __fadd_rn(1.f, expf(-x))); }
+__device__ __forceinline__ float act_hardswish(float x) {
+  const float c = fminf(fmaxf(__fadd_rn(x, 3.f), 0.f), 6.f);
+  return __fdiv_rn(__fmul_rn(x, c), 6.f);
+}
+
+template <uint32_t OP>
+__device__ __forceinline__ float activation(float x) {
+  if constexpr (OP == OP_SIGMOID) return act_sigmoid(x);
+  else if constexpr (OP == OP_TANH) return act_tanh(x);
+  else if constexpr (OP == OP_GELU) return act_gelu(x);
+  else if constexpr (OP == OP_SILU) return act_silu(x);
+  else return act_hardswish(x);
+}
+
+template <uint32_t OP, int C>
+__device__ __forceinline__ void activation_vec(float (&t)[C]) {
+#pragma unroll
+  for (int e = 0; e < C; ++e) t[e] = activation<OP>(t[e]);
+}
+
+__host__ __device__ constexpr bool is_activation_op(uint32_t op) {
+  return op == OP_SIGMOID || op == OP_TANH || op == OP_GELU || op == OP_SILU || op == OP_HARDSWISH;
+}
+
 // ------------------------------------------------------------ interpreter --
 template <int C, class Mem>
 __device__ __forceinline__ void run_program(const EpiProgram &P, const float (&acc)[C], const Mem &mem) {
@@ -295,6 +332,35 @@ __device__ __forceinline__ void run_program(const EpiProgram &P, const float (&a
           GE_APPLY(2, fmaxf(x, t[e])) GE_APPLY(3, fmaxf(x, t[e]))
         }
         break;
+      case OP_LEAKY:
+        switch (dst) {
+          GE_APPLY(0, x > 0.f ? x : __fmul_rn(t[e], x)) GE_APPLY(1, x > 0.f ? x : __fmul_rn(t[e], x))
+          GE_APPLY(2, x > 0.f ? x : __fmul_rn(t[e], x)) GE_APPLY(3, x > 0.f ? x : __fmul_rn(t[e], x))
+        }
+        break;
+      case OP_RLEAKY:
+        switch (dst) {
+          GE_APPLY(0, t[e] > 0.f ? t[e] : __fmul_rn(x, t[e]))
+          GE_APPLY(1, t[e] > 0.f ? t[e] : __fmul_rn(x, t[e]))
+          GE_APPLY(2, t[e] > 0.f ? t[e] : __fmul_rn(x, t[e]))
+          GE_APPLY(3, t[e] > 0.f ? t[e] : __fmul_rn(x, t[e]))
+        }
+        break;
+      case OP_SIGMOID:
+      case OP_TANH:
+      case OP_GELU:
+      case OP_SILU:
+      case OP_HARDSWISH:
+        // one copy of each activation's code, applied to the fetched operand
+        switch (op) {
+          case OP_SIGMOID: activation_vec<OP_SIGMOID>(t); break;
+          case OP_TANH: activation_vec<OP_TANH>(t); break;
+          case OP_GELU: activation_vec<OP_GELU>(t); break;
+          case OP_SILU: activation_vec<OP_SILU>(t); break;
+          default: activation_vec<OP_HARDSWISH>(t); break;
+        }
+        switch (dst) { GE_APPLY(0, t[e]) GE_APPLY(1, t[e]) GE_APPLY(2, t[e]) GE_APPLY(3, t[e]) }
+        break;
       default:  // OP_STORE
         GE_DISPATCH_DTYPE(P.out_dtype[dst], mem.template store<DT_>(dst, t));
         break;
@@ -357,6 +423,16 @@ __device__ __forceinline__ void run_static_from(float (&r)[kRegs][C], const floa
       } else if constexpr (op == OP_MAX) {
 #pragma unroll
         for (int e = 0; e < C; ++e) r[dst][e] = fmaxf(r[dst][e], t[e]);
+      } else if constexpr (op == OP_LEAKY) {
+#pragma unroll
+        for (int e = 0; e < C; ++e)
+          r[dst][e] = r[dst][e] > 0.f ? r[dst][e] : __fmul_rn(t[e], r[dst][e]);
+      } else if constexpr (op == OP_RLEAKY) {
+#pragma unroll
+        for (int e = 0; e < C; ++e) r[dst][e] = t[e] > 0.f ? t[e] : __fmul_rn(r[dst][e], t[e]);
+      } else if constexpr (is_activation_op(op)) {
+#pragma unroll
+        for (int e = 0; e < C; ++e) r[dst][e] = activation<op>(t[e]);
       } else {
         mem.template store<SP::P.out_dtype[dst]>(dst, t);
       }

@@ -78,10 +78,16 @@ int validate_impl(const ge_dtypes *dt, const ge_dag *dag) {
       case GE_DIV:
       case GE_MIN:
       case GE_MAX:
+      case GE_LEAKY_RELU:
         if (!is_value_node(dag, nd.b, i)) return GE_ERR_SSA;
         if (!is_value_node(dag, nd.a, i)) return GE_ERR_SSA;
         break;
       case GE_RELU:
+      case GE_SIGMOID:
+      case GE_TANH:
+      case GE_GELU:
+      case GE_SILU:
+      case GE_HARDSWISH:
         if (!is_value_node(dag, nd.a, i)) return GE_ERR_SSA;
         break;
       case GE_STORE:

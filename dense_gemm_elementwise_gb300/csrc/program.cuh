@@ -28,7 +28,13 @@ __host__ __device__ constexpr int src_rank(uint32_t src) {
 
 __host__ __device__ constexpr bool is_binary(int op) {
   return op == GE_MUL || op == GE_ADD || op == GE_SUB || op == GE_DIV || op == GE_MIN ||
-         op == GE_MAX;
+         op == GE_MAX || op == GE_LEAKY_RELU;
+}
+
+// activations compiled as r[dst] = f(src)
+__host__ __device__ constexpr bool is_activation(int op) {
+  return op == GE_SIGMOID || op == GE_TANH || op == GE_GELU || op == GE_SILU ||
+         op == GE_HARDSWISH;
 }
 
 struct CompileResult {
@@ -51,7 +57,7 @@ __host__ __device__ constexpr CompileResult compile_program(const ge_dtypes &dt,
     if (is_binary(nd.op)) {
       last_use[nd.a] = i;
       last_use[nd.b] = i;
-    } else if (nd.op == GE_RELU || nd.op == GE_STORE) {
+    } else if (nd.op == GE_RELU || nd.op == GE_STORE || is_activation(nd.op)) {
       last_use[nd.a] = i;
     }
   }
@@ -121,9 +127,11 @@ __host__ __device__ constexpr CompileResult compile_program(const ge_dtypes &dt,
       case GE_SUB:
       case GE_DIV:
       case GE_MIN:
-      case GE_MAX: {
-        // two-address forms; subtraction and division have a reversed form
-        // for when the second operand's register is the one reused
+      case GE_MAX:
+      case GE_LEAKY_RELU: {
+        // two-address forms; subtraction, division and leaky ReLU have a
+        // reversed form for when the second operand's register is the one
+        // reused
         const bool commutes = nd.op == GE_MUL || nd.op == GE_ADD || nd.op == GE_MIN ||
                               nd.op == GE_MAX;
         const uint32_t op = nd.op == GE_MUL   ? OP_MUL
@@ -131,8 +139,12 @@ __host__ __device__ constexpr CompileResult compile_program(const ge_dtypes &dt,
                             : nd.op == GE_SUB ? OP_SUB
                             : nd.op == GE_DIV ? OP_DIV
                             : nd.op == GE_MIN ? OP_MIN
-                                              : OP_MAX;
-        const uint32_t rop = nd.op == GE_SUB ? OP_RSUB : nd.op == GE_DIV ? OP_RDIV : op;
+                            : nd.op == GE_MAX ? OP_MAX
+                                              : OP_LEAKY;
+        const uint32_t rop = nd.op == GE_SUB          ? OP_RSUB
+                             : nd.op == GE_DIV        ? OP_RDIV
+                             : nd.op == GE_LEAKY_RELU ? OP_RLEAKY
+                                                      : op;
         const bool a_dies = loc_src[nd.a] == SRC_REG && last_use[nd.a] == i;
         const bool b_dies = loc_src[nd.b] == SRC_REG && last_use[nd.b] == i;
         int d = -1, other = -1;
@@ -197,6 +209,40 @@ __host__ __device__ constexpr CompileResult compile_program(const ge_dtypes &dt,
           P.ins[P.n_ins++] = pack_ins(OP_MOV, static_cast<uint32_t>(d), loc_src[nd.a], loc_idx[nd.a]);
         }
         P.ins[P.n_ins++] = pack_ins(OP_RELU, static_cast<uint32_t>(d), SRC_NONE, 0);
+        loc_src[i] = SRC_REG;
+        loc_idx[i] = static_cast<uint32_t>(d);
+        if (last_use[i] < 0) busy[d] = false;
+        break;
+      }
+      case GE_SIGMOID:
+      case GE_TANH:
+      case GE_GELU:
+      case GE_SILU:
+      case GE_HARDSWISH: {
+        // the operand is read from wherever it lives; its register is
+        // reused when this is its last use
+        const uint32_t op = nd.op == GE_SIGMOID ? OP_SIGMOID
+                            : nd.op == GE_TANH  ? OP_TANH
+                            : nd.op == GE_GELU  ? OP_GELU
+                            : nd.op == GE_SILU  ? OP_SILU
+                                                : OP_HARDSWISH;
+        int d = -1;
+        if (loc_src[nd.a] == SRC_REG && last_use[nd.a] == i) {
+          d = static_cast<int>(loc_idx[nd.a]);
+        } else {
+          for (int r = 0; r < kRegs; ++r)
+            if (!busy[r]) {
+              d = r;
+              break;
+            }
+          if (d < 0) {
+            R.status = GE_ERR_UNSUPPORTED;
+            return R;
+          }
+          busy[d] = true;
+          if (d + 1 > max_regs) max_regs = d + 1;
+        }
+        P.ins[P.n_ins++] = pack_ins(op, static_cast<uint32_t>(d), loc_src[nd.a], loc_idx[nd.a]);
         loc_src[i] = SRC_REG;
         loc_idx[i] = static_cast<uint32_t>(d);
         if (last_use[i] < 0) busy[d] = false;

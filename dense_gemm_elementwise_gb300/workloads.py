@@ -7,7 +7,8 @@ GEMM or epilogue arithmetic; both the CUDA path (through the C-ABI binding)
 and the CPU oracle consume what it produces.
 
 DAG tuples are ``(op, a, b, slot)`` with ``op`` one of ``accum, load, scalar,
-broadcast, col_broadcast, mul, add, sub, div, min, max, relu, store``;
+broadcast, col_broadcast, mul, add, sub, div, min, max, relu, sigmoid, tanh,
+gelu, silu, hardswish, leaky_relu, store``;
 ``a``/``b`` index earlier nodes; ``slot`` selects the aux tensor (load, row or
 column broadcast), the scalar (scalar) or the output (store).  Output slot 0
 is D.
@@ -55,6 +56,24 @@ class Dag:
 
     def maximum(self, a, b):
         return self._add("max", a, b)
+
+    def sigmoid(self, a):
+        return self._add("sigmoid", a)
+
+    def tanh(self, a):
+        return self._add("tanh", a)
+
+    def gelu(self, a):
+        return self._add("gelu", a)
+
+    def silu(self, a):
+        return self._add("silu", a)
+
+    def hardswish(self, a):
+        return self._add("hardswish", a)
+
+    def leaky_relu(self, a, slope):
+        return self._add("leaky_relu", a, slope)
 
     def scalar(self, slot):
         return self._add("scalar", slot=slot)
@@ -250,6 +269,33 @@ def dag_scale_shift():
     return g.nodes
 
 
+ACTIVATIONS = ["sigmoid", "tanh", "gelu", "silu", "hardswish", "leaky_relu"]
+
+
+def dag_activation(act):
+    """D = act(alpha*accum + C): one of the activations of the legacy
+    interface's registry (gelu, hardswish, leaky_relu, sigmoid, silu, tanh;
+    relu and identity have their own workloads).  leaky_relu takes its
+    negative slope from scalar slot 1."""
+    g = Dag()
+    t = g.add(g.mul(g.accum(), g.scalar(0)), g.load(0))
+    d = g.leaky_relu(t, g.scalar(1)) if act == "leaky_relu" else getattr(g, act)(t)
+    g.store(d, 0)
+    return g.nodes
+
+
+def dag_complex():
+    """result = (accum + bias)*scale + c + tanh(x) ; D = gelu(result)
+    ("Custom Epilogue Example", section "Complex Expressions"; bias read as a
+    row vector)."""
+    g = Dag()
+    r = g.mul(g.add(g.accum(), g.broadcast(2)), g.scalar(0))
+    r = g.add(r, g.load(0))
+    r = g.add(r, g.tanh(g.load(1)))
+    g.store(g.gelu(r), 0)
+    return g.nodes
+
+
 def dag_clamp():
     """D = min(max(alpha*accum - C, lo), hi): subtraction and binary
     maximum/minimum ("Defining an epilogue via a Python function")."""
@@ -308,7 +354,8 @@ RTOL = 1e-2
 
 
 def page_examples(L=1, M=256, N=256, K=256):
-    """Further epilogues printed on the pages, at a small size, integer inputs."""
+    """Further epilogues printed on the pages, at a small size: integer inputs
+    where the result is exact, N(0,1) inputs for the activations."""
     return [
         Workload(name="relu_aux_store", L=L, M=M, N=N, K=K, ab="f16",
                  aux=[("C", "tensor", "f16")], scalars=[("alpha", 3.0), ("two", 2.0)],
@@ -354,6 +401,19 @@ def page_examples(L=1, M=256, N=256, K=256):
                  scalars=[("alpha", 1.0), ("lo", -3.0), ("hi", 5.5)], outs=[("D", "f16")],
                  dag=dag_clamp(), dist="randint", seed=2025, exact=True,
                  cite="Defining an epilogue via a Python function: binary min and max"),
+    ] + [
+        Workload(name="act_" + act, L=L, M=M, N=N, K=K, ab="f16", aux=[("C", "tensor", "f16")],
+                 scalars=[("alpha", 0.25)] + ([("slope", 0.1)] if act == "leaky_relu" else []),
+                 outs=[("D", "f16")], dag=dag_activation(act), dist="normal", seed=2028,
+                 exact=False,
+                 cite="Python examples walkthrough: epilogue notebook, activation registry")
+        for act in ACTIVATIONS
+    ] + [
+        Workload(name="complex_gelu_tanh", L=L, M=M, N=N, K=K, ab="bf16",
+                 aux=[("c", "tensor", "bf16"), ("x", "tensor", "bf16"), ("bias", "row", "f32")],
+                 scalars=[("scale", 0.125)], outs=[("D", "bf16")], dag=dag_complex(),
+                 dist="normal", seed=2029, exact=False,
+                 cite="Custom Epilogue Example: Complex Expressions"),
     ]
 
 

@@ -71,13 +71,23 @@ typedef enum {
   GE_DIV = 9,       /* v[a] / v[b]  (fp32, correctly rounded)                */
   GE_MIN = 10,      /* min(v[a], v[b])                                       */
   GE_MAX = 11,      /* max(v[a], v[b])                                       */
-  GE_COL_BROADCAST = 12 /* aux slot `slot`, an (M,) column vector: aux[i]    */
+  GE_COL_BROADCAST = 12, /* aux slot `slot`, an (M,) column vector: aux[i]   */
+  /* Activations of the legacy interface's registry (Python examples
+   * walkthrough, epilogue notebook), evaluated in fp32 with the CUDA math
+   * library's expf / tanhf / erfcf (not bit-reproducible against another
+   * libm: compare within a tolerance).                                      */
+  GE_SIGMOID = 13,    /* 1 / (1 + exp(-v[a]))                                */
+  GE_TANH = 14,       /* tanh(v[a])                                          */
+  GE_GELU = 15,       /* v[a]/2 * (1 + erf(v[a] / sqrt(2)))  (exact GELU)     */
+  GE_SILU = 16,       /* v[a] / (1 + exp(-v[a]))                             */
+  GE_HARDSWISH = 17,  /* v[a] * min(max(v[a] + 3, 0), 6) / 6                 */
+  GE_LEAKY_RELU = 18  /* v[a] > 0 ? v[a] : v[b] * v[a]  (v[b]: the slope)    */
 } ge_op;
 
 typedef struct {
   int32_t op;   /* ge_op */
   int32_t a;    /* first operand (node index) */
-  int32_t b;    /* second operand (GE_MUL, GE_ADD) */
+  int32_t b;    /* second operand of the two-operand nodes */
   int32_t slot; /* aux / scalar / output slot */
 } ge_node;
 

@@ -6,8 +6,8 @@ CPU-baseline leg of ``bench.py`` use it; the product path never does.
 Arrays cross this boundary as numpy arrays: 16-bit element types as their raw
 ``uint16`` codes, fp32 as ``float32``.  The DAG is a list of
 ``(op, a, b, slot)`` tuples whose ``op`` is one of ``accum, load, scalar,
-broadcast, mul, add, relu, store, sub, div, min, max, col_broadcast`` (the
-node kinds of the epilogue DAG in
+broadcast, mul, add, relu, store, sub, div, min, max, col_broadcast, sigmoid,
+tanh, gelu, silu, hardswish, leaky_relu`` (the node kinds of the epilogue DAG in
 "CUTLASS Operator API: Custom epilogue fusions for GEMMs", section "How the
 epilogue fusion API works").
 """
@@ -20,7 +20,8 @@ from . import build as _build
 
 _TYPES = {"f16": 0, "bf16": 1, "f32": 2}
 _OPS = {"accum": 0, "load": 1, "scalar": 2, "broadcast": 3, "mul": 4, "add": 5,
-        "relu": 6, "store": 7, "sub": 8, "div": 9, "min": 10, "max": 11, "col_broadcast": 12}
+        "relu": 6, "store": 7, "sub": 8, "div": 9, "min": 10, "max": 11, "col_broadcast": 12,
+        "sigmoid": 13, "tanh": 14, "gelu": 15, "silu": 16, "hardswish": 17, "leaky_relu": 18}
 
 
 class _Node(ctypes.Structure):

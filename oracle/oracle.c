@@ -211,6 +211,19 @@ static void *row_worker(void *p) {
           case ORC_DIV: v[n] = v[nd->a] / v[nd->b]; break;
           case ORC_MIN: v[n] = v[nd->b] < v[nd->a] ? v[nd->b] : v[nd->a]; break;
           case ORC_MAX: v[n] = v[nd->b] > v[nd->a] ? v[nd->b] : v[nd->a]; break;
+          case ORC_SIGMOID: v[n] = 1.0 / (1.0 + exp(-v[nd->a])); break;
+          case ORC_TANH: v[n] = tanh(v[nd->a]); break;
+          /* 1 + erf(x/sqrt2) written as erfc(-x/sqrt2): the same number
+           * without the cancellation that leaves 0 for x below about -8 */
+          case ORC_GELU: v[n] = 0.5 * v[nd->a] * erfc(-v[nd->a] / sqrt(2.0)); break;
+          case ORC_SILU: v[n] = v[nd->a] / (1.0 + exp(-v[nd->a])); break;
+          case ORC_HARDSWISH: {
+            const double x = v[nd->a];
+            double c = x + 3.0;
+            c = c < 0.0 ? 0.0 : (c > 6.0 ? 6.0 : c);
+            v[n] = x * c / 6.0;
+          } break;
+          case ORC_LEAKY_RELU: v[n] = v[nd->a] > 0.0 ? v[nd->a] : v[nd->b] * v[nd->a]; break;
           case ORC_RELU: v[n] = v[nd->a] > 0.0 ? v[nd->a] : 0.0; break;
           case ORC_STORE:
             encode(jb->out_type[nd->slot], jb->outs[nd->slot], out_row * N + j, v[nd->a]);
@@ -250,9 +263,15 @@ static int validate_dag(int32_t n_nodes, const orc_node *nodes, int32_t n_aux, i
       case ORC_DIV:
       case ORC_MIN:
       case ORC_MAX:
+      case ORC_LEAKY_RELU:
         if (nd->b < 0 || nd->b >= n || nodes[nd->b].op == ORC_STORE) return ORC_BAD_DAG;
         /* fall through: operand a */
       case ORC_RELU:
+      case ORC_SIGMOID:
+      case ORC_TANH:
+      case ORC_GELU:
+      case ORC_SILU:
+      case ORC_HARDSWISH:
         if (nd->a < 0 || nd->a >= n || nodes[nd->a].op == ORC_STORE) return ORC_BAD_DAG;
         break;
       case ORC_STORE:

@@ -38,6 +38,15 @@
  *   ORC_COLBCAST s -> aux_s[i]                (column broadcast: shape (M,) or
  *                                              (M, 1), the same for every column
  *                                              j and batch l)
+ *   activations of v[a] (the legacy Python interface's activation registry:
+ *   gelu, hardswish, identity, leaky_relu, relu, sigmoid, silu, tanh; the
+ *   operator API's "Predefined elementwise activation functions"):
+ *   ORC_SIGMOID    -> 1 / (1 + exp(-x))
+ *   ORC_TANH       -> tanh(x)
+ *   ORC_GELU       -> x * Phi(x) = 0.5 * x * (1 + erf(x / sqrt(2)))
+ *   ORC_SILU       -> x * sigmoid(x) = x / (1 + exp(-x))
+ *   ORC_HARDSWISH  -> x * min(max(x + 3, 0), 6) / 6
+ *   ORC_LEAKY_RELU a b -> v[a] > 0 ? v[a] : v[b] * v[a]   (v[b]: the slope)
  *   ORC_STORE a s  -> out_s[l,i,j] = round_to_nearest_even(type_s, v[a])
  *
  * Only a store rounds; every intermediate value stays in fp64 (the pages run
@@ -77,7 +86,13 @@ enum {
   ORC_DIV = 9,
   ORC_MIN = 10,
   ORC_MAX = 11,
-  ORC_COLBCAST = 12
+  ORC_COLBCAST = 12,
+  ORC_SIGMOID = 13,
+  ORC_TANH = 14,
+  ORC_GELU = 15,
+  ORC_SILU = 16,
+  ORC_HARDSWISH = 17,
+  ORC_LEAKY_RELU = 18
 };
 
 typedef struct {

@@ -105,6 +105,38 @@ def nearest_even_f32(x):
     return np.float32(best[1])
 
 
+def _mpf(x):
+    import mpmath
+    return mpmath.mpf(x.numerator) / x.denominator
+
+
+def _frac(m):
+    """mpmath number -> exact Fraction of its binary value."""
+    import mpmath
+    sign, man, exp, _ = mpmath.mpf(m)._mpf_
+    return (-1) ** sign * Fraction(int(man)) * (Fraction(2) ** int(exp))
+
+
+def activation_exact(op, x):
+    """The activation at 60 significant digits (mpmath), as a Fraction: the
+    definitions, evaluated far beyond fp64 so the result rounds like the
+    true value."""
+    import mpmath
+    with mpmath.workdps(60):
+        m = _mpf(Fraction(x))
+        if op == "sigmoid":
+            r = 1 / (1 + mpmath.exp(-m))
+        elif op == "tanh":
+            r = mpmath.tanh(m)
+        elif op == "gelu":
+            r = m * (1 + mpmath.erf(m / mpmath.sqrt(2))) / 2
+        elif op == "silu":
+            r = m / (1 + mpmath.exp(-m))
+        else:  # hardswish
+            r = m * min(max(m + 3, 0), 6) / 6
+        return _frac(r)
+
+
 def eval_dag_exact(dag, acc, aux_vals, scalars, n_out):
     """Evaluate a DAG on exact rationals for one element.  ``aux_vals[s]`` is
     the (already selected) exact value of aux slot s at this element."""
@@ -131,6 +163,10 @@ def eval_dag_exact(dag, acc, aux_vals, scalars, n_out):
             v[n] = max(v[a], v[b])
         elif op == "relu":
             v[n] = v[a] if v[a] > 0 else Fraction(0)
+        elif op == "leaky_relu":
+            v[n] = v[a] if v[a] > 0 else v[b] * v[a]
+        elif op in ("sigmoid", "tanh", "gelu", "silu", "hardswish"):
+            v[n] = activation_exact(op, v[a])
         elif op == "store":
             outs[s] = v[a]
     return outs
@@ -324,6 +360,61 @@ def pin_new_ops_closed_form(L_):
     assert np.array_equal(np_decode(T, "bf16"), acc * 2)
 
 
+def _act_values(L_, act, xs, slope=0.25):
+    """act(x) through the oracle for fp16-representable xs: K = 1 and B = 1,
+    so accum = x exactly; D = act(accum) stored as fp32."""
+    import torch
+    g = W.Dag()
+    a = g.accum()
+    g.store(g.leaky_relu(a, g.scalar(0)) if act == "leaky_relu" else getattr(g, act)(a), 0)
+    w = W.Workload(name="act_" + act, L=1, M=len(xs), N=1, K=1, ab="f16", aux=[],
+                   scalars=[("slope", slope)], outs=[("D", "f32")], dag=g.nodes,
+                   dist="normal", seed=0, exact=False)
+    A = torch.tensor(xs, dtype=torch.float64).to(torch.float16).reshape(1, -1, 1)
+    assert np.array_equal(A.double().numpy().ravel(), np.asarray(xs, dtype=np.float64))
+    B = torch.ones(1, 1, 1, dtype=torch.float16)
+    (D,), _ = run_oracle(L_, w, A, B, [], [slope])
+    return D.ravel().astype(np.float64)
+
+
+def pin_activation_identities(L_):
+    """The activations against textbook values and identities that tie them to
+    one another: sigmoid(0) = 1/2 and sigmoid(x) + sigmoid(-x) = 1;
+    tanh(x) = 2 sigmoid(2x) - 1 and tanh odd; x Phi(x) with Phi from the
+    standard normal table (Phi(1) = 0.8413447460685429, upper tail at 8 =
+    6.220960574271785e-16) and gelu(x) - gelu(-x) = x; silu(x) = x sigmoid(x);
+    hardswish's three pieces at hand-worked points; leaky ReLU's two sides."""
+    u = 2.0 ** -23  # fp32 unit roundoff x 2: results are fp64 rounded once to fp32
+    xs = [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0, 8.0, 0.125, 0.75]
+    xn = [-x for x in xs]
+    sig_p, sig_n = _act_values(L_, "sigmoid", xs), _act_values(L_, "sigmoid", xn)
+    assert sig_p[0] == 0.5
+    assert np.all(np.abs(sig_p + sig_n - 1.0) <= 2 * u)
+    assert np.all(np.diff(_act_values(L_, "sigmoid", sorted(xn + xs[1:]))) >= 0)
+    sig_2x = _act_values(L_, "sigmoid", [2 * x for x in xs])
+    th_p, th_n = _act_values(L_, "tanh", xs), _act_values(L_, "tanh", xn)
+    assert th_p[0] == 0.0 and np.array_equal(th_p, -th_n)
+    assert np.all(np.abs(th_p - (2 * sig_2x - 1)) <= 4 * u)
+    ge_p, ge_n = _act_values(L_, "gelu", xs), _act_values(L_, "gelu", xn)
+    assert ge_p[0] == 0.0
+    assert np.all(np.abs((ge_p - ge_n) - np.array(xs)) <= 2 * u * np.maximum(1.0, np.array(xs)))
+    assert abs(ge_p[2] - 0.8413447460685429) <= u
+    assert abs(ge_n[2] + (1 - 0.8413447460685429)) <= u
+    assert ge_p[8] == 8.0
+    tail = -8.0 * 6.220960574271785e-16
+    assert abs(ge_n[8] - tail) <= 2 * u * abs(tail)
+    si_p, si_n = _act_values(L_, "silu", xs), _act_values(L_, "silu", xn)
+    assert np.all(np.abs(si_p - np.array(xs) * sig_p) <= 2 * u * np.maximum(1.0, np.array(xs)))
+    assert np.all(np.abs(si_n - np.array(xn) * sig_n) <= 2 * u)
+    hx = [-8.0, -3.0, -2.0, -1.5, 0.0, 1.0, 1.5, 3.0, 4.0, 8.0]
+    hs = _act_values(L_, "hardswish", hx)
+    want = [0.0, 0.0, -1 / 3, -0.375, 0.0, 2 / 3, 1.125, 3.0, 4.0, 8.0]
+    assert np.array_equal(hs, np.array(want, dtype=np.float32).astype(np.float64))
+    lx = [-4.0, -1.5, -0.125, 0.0, 0.125, 1.5, 4.0]
+    assert np.array_equal(_act_values(L_, "leaky_relu", lx, slope=0.25),
+                          [-1.0, -0.375, -0.03125, 0.0, 0.125, 1.5, 4.0])
+
+
 def pin_broadcast_closed_form(L_):
     """Row-broadcast bias indexed by column j, same vector for every row and
     batch: integer inputs, D = relu(0.5*A@B + C + bias), E = D*D rounded."""
@@ -442,7 +533,8 @@ def pin_rows_and_threads(L_):
 
 ALL_PINS = [pin_decode_exhaustive, pin_encode_roundtrip, pin_encode_midpoints,
             pin_encode_random_vs_table, pin_golden, pin_integer_closed_form,
-            pin_broadcast_closed_form, pin_new_ops_closed_form, pin_fraction_brute_force,
+            pin_broadcast_closed_form, pin_new_ops_closed_form, pin_activation_identities,
+            pin_fraction_brute_force,
             pin_special_cases,
             pin_relu_positive_zero, pin_rows_and_threads]
 

@@ -115,6 +115,26 @@ def test_unsupported():
     assert B.gemm_epi_validate(dt4, B.make_dag(bad)) == B.GE_ERR_UNSUPPORTED
 
 
+def test_activation_nodes():
+    """Unary activations take one earlier value; leaky ReLU two (value,
+    slope); any of them referring to itself or a later node is an SSA error."""
+    dt, _ = _base()
+    dt.n_out = 1
+    for act in W.ACTIVATIONS[:-1]:
+        ok = [("accum", 0, 0, 0), ("load", 0, 0, 0), (act, 1, 0, 0), ("add", 0, 2, 0),
+              (act, 3, 0, 0), ("store", 4, 0, 0)]
+        assert B.gemm_epi_validate(dt, B.make_dag(ok)) == B.GE_OK, act
+        bad = [("accum", 0, 0, 0), (act, 2, 0, 0), ("store", 1, 0, 0)]
+        assert B.gemm_epi_validate(dt, B.make_dag(bad)) == B.GE_ERR_SSA, act
+    ok = [("accum", 0, 0, 0), ("scalar", 0, 0, 0), ("leaky_relu", 0, 1, 0), ("store", 2, 0, 0)]
+    assert B.gemm_epi_validate(dt, B.make_dag(ok)) == B.GE_OK
+    bad = [("accum", 0, 0, 0), ("leaky_relu", 0, 2, 0), ("scalar", 0, 0, 0), ("store", 1, 0, 0)]
+    assert B.gemm_epi_validate(dt, B.make_dag(bad)) == B.GE_ERR_SSA
+    # PReLU: the slope is a row vector
+    ok = [("accum", 0, 0, 0), ("broadcast", 0, 0, 0), ("leaky_relu", 0, 1, 0), ("store", 2, 0, 0)]
+    assert B.gemm_epi_validate(dt, B.make_dag(ok)) == B.GE_OK
+
+
 def test_program_register_limit():
     """Five values live at once exceed the epilogue program's 4 registers."""
     g = W.Dag()

@@ -268,3 +268,99 @@ def test_row_col_bias_uses_catalog():
     gpu, info = _gpu.run_gpu(w, inputs)
     assert info["epi_variant"] >= 0
     _gpu.compare(w, gpu, _gpu.oracle_rows(w, inputs))
+
+
+# ------------------------------------------------------- activations --
+
+ACT_CASES = [x for x in W.page_examples(L=2, M=264, N=392, K=200)
+             if x.name.startswith("act_") or x.name.startswith("complex_")]
+
+
+def _ulp(v, dt):
+    """Spacing of the output type at magnitude v."""
+    p, emin = {"f16": (11, -14), "bf16": (8, -126), "f32": (24, -126)}[dt]
+    e = np.floor(np.log2(np.maximum(np.abs(v), 2.0 ** emin)))
+    return 2.0 ** (e - (p - 1))
+
+
+@pytest.mark.parametrize("w", ACT_CASES, ids=lambda w: w.name)
+@pytest.mark.parametrize("variant", [(1, 128, 1), (2, 256, 1)], ids=vid)
+def test_activations_within_one_ulp(w, variant):
+    """The fp32 activations (CUDA math library) against the fp64 oracle.
+    The activation's argument differs between the two sides by at most the
+    fp32 summation bound K * 2^-24 * sum_k |a_ik b_kj| (times the scalar
+    applied to accum) plus a few fp32 roundings of its own size, and the
+    math library adds a few fp32 ulps; with every activation's slope at most
+    1.5, each output then lies within one unit in the last place of its type,
+    plus 1.5 times that bound, plus 32 fp32 ulps of the oracle's, and nearly
+    all are identical."""
+    inputs = W.make_inputs(w)
+    gpu, info = _gpu.run_gpu(w, inputs, options=opts(variant))
+    ref = _gpu.oracle_rows(w, inputs)
+    A, Bm = inputs[0].double().numpy(), inputs[1].double().numpy()
+    S = np.einsum("lik,lkj->lij", np.abs(A), np.abs(Bm)).reshape(w.L * w.M, w.N)
+    u = 2.0 ** -24
+    arg_err = abs(w.scalars[0][1]) * w.K * u * S
+    for (name, dt), g, r in zip(w.outs, gpu, ref):
+        gv = _gpu.decode(W.to_codes(g).reshape(w.L * w.M, w.N), dt)
+        rv = _gpu.decode(r, dt)
+        assert not np.isnan(gv).any()
+        lim = (_ulp(np.maximum(np.abs(gv), np.abs(rv)), dt) + 1.5 * arg_err +
+               32 * u * (1 + np.abs(rv)))
+        err = np.abs(gv - rv)
+        assert (err <= lim).all(), (name, float((err - lim).max()), gv[err > lim][:4],
+                                    rv[err > lim][:4])
+        assert (gv == rv).mean() > 0.97, (name, float((gv == rv).mean()))
+
+
+def test_activation_special_inputs():
+    """Large-magnitude and zero arguments: sigmoid saturates to 0 and 1,
+    tanh to -1 and 1, gelu and silu to 0 and x, hardswish to 0 and x,
+    without NaN (K = 8, accum = 64 * a row of A)."""
+    import torch
+    for act in W.ACTIVATIONS:
+        w = [x for x in W.page_examples(L=1, M=128, N=64, K=8) if x.name == "act_" + act][0]
+        w = dataclasses.replace(w, outs=[("D", "f32")])
+        A = torch.zeros(1, 128, 8, dtype=torch.float16)
+        A[0, :, 0] = torch.linspace(-60, 60, 128).to(torch.float16)
+        Bm = torch.zeros(1, 8, 64, dtype=torch.float16)
+        Bm[0, 0, :] = 64.0
+        C = torch.zeros(1, 128, 64, dtype=torch.float16)
+        inputs = (A, Bm, [C], [0.25] + ([0.1] if act == "leaky_relu" else []))
+        gpu, _ = _gpu.run_gpu(w, inputs)
+        ref = _gpu.oracle_rows(w, inputs)
+        gv = _gpu.decode(W.to_codes(gpu[0]).reshape(128, 64), "f32")
+        rv = _gpu.decode(ref[0], "f32")
+        assert not np.isnan(gv).any(), act
+        assert np.allclose(gv, rv, rtol=4e-6, atol=1e-30), (act, np.abs(gv - rv).max())
+
+
+def _leaky_workloads():
+    """Leaky ReLU with the slope in a register that dies while the value
+    lives on (the reversed form), and PReLU with a per-column slope vector;
+    integer inputs and half-integer slopes keep both bit-exact."""
+    g = W.Dag()
+    t = g.mul(g.accum(), g.scalar(0))
+    s = g.mul(g.load(0), g.scalar(1))
+    g.store(g.leaky_relu(t, s), 0)
+    g.store(t, 1)
+    rev = W.Workload(name="leaky_reversed", L=2, M=264, N=392, K=200, ab="f16",
+                     aux=[("C", "tensor", "f16")], scalars=[("alpha", 1.0), ("half", 0.5)],
+                     outs=[("D", "f16"), ("T", "f16")], dag=g.nodes, dist="randint", seed=32,
+                     exact=True)
+    g = W.Dag()
+    g.store(g.leaky_relu(g.accum(), g.broadcast(0)), 0)
+    prelu = W.Workload(name="prelu_row_slope", L=2, M=200, N=264, K=136, ab="bf16",
+                       aux=[("slope", "row", "f32")], scalars=[], outs=[("D", "bf16")],
+                       dag=g.nodes, dist="randint", seed=33, exact=True)
+    return [rev, prelu]
+
+
+@pytest.mark.parametrize("w", _leaky_workloads(), ids=lambda w: w.name)
+@pytest.mark.parametrize("variant", [(1, 128, 1), (2, 256, 1)], ids=vid)
+def test_leaky_relu_forms(w, variant):
+    inputs = W.make_inputs(w)
+    gpu, info = _gpu.run_gpu(w, inputs, options=opts(variant))
+    _gpu.compare(w, gpu, _gpu.oracle_rows(w, inputs))
+    unf, _ = _gpu.run_gpu(w, inputs, unfused=True, options=opts(variant))
+    _gpu.bitwise_equal(gpu, unf)

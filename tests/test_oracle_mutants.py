@@ -54,6 +54,19 @@ MUTANTS = [
     ("col_broadcast_by_column",
      "case ORC_COLBCAST: v[n] = decode(jb->aux_type[nd->slot], jb->aux[nd->slot], i);",
      "case ORC_COLBCAST: v[n] = decode(jb->aux_type[nd->slot], jb->aux[nd->slot], j % M);"),
+    ("sigmoid_sign", "case ORC_SIGMOID: v[n] = 1.0 / (1.0 + exp(-v[nd->a]));",
+     "case ORC_SIGMOID: v[n] = 1.0 / (1.0 + exp(v[nd->a]));"),
+    ("tanh_half_argument", "case ORC_TANH: v[n] = tanh(v[nd->a]);",
+     "case ORC_TANH: v[n] = 2.0 / (1.0 + exp(-v[nd->a])) - 1.0;"),
+    ("gelu_without_sqrt", "erfc(-v[nd->a] / sqrt(2.0))", "erfc(-v[nd->a] / 2.0)"),
+    ("gelu_cancels_tail", "0.5 * v[nd->a] * erfc(-v[nd->a] / sqrt(2.0));",
+     "0.5 * v[nd->a] * (1.0 + erf(v[nd->a] / sqrt(2.0)));"),
+    ("silu_sign", "case ORC_SILU: v[n] = v[nd->a] / (1.0 + exp(-v[nd->a]));",
+     "case ORC_SILU: v[n] = v[nd->a] / (1.0 + exp(v[nd->a]));"),
+    ("hardswish_clamp_3", "c = c < 0.0 ? 0.0 : (c > 6.0 ? 6.0 : c);",
+     "c = c < 0.0 ? 0.0 : (c > 3.0 ? 3.0 : c);"),
+    ("leaky_side", "case ORC_LEAKY_RELU: v[n] = v[nd->a] > 0.0 ? v[nd->a] : v[nd->b] * v[nd->a];",
+     "case ORC_LEAKY_RELU: v[n] = v[nd->a] < 0.0 ? v[nd->a] : v[nd->b] * v[nd->a];"),
 ]
 
 
