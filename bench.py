@@ -417,9 +417,229 @@ def run_ours(args, w):
     print(json.dumps(line), flush=True)
 
 
+# ------------------------------------------------------- grouped GEMM ---
+
+GROUPED_METRIC = "grouped GEMM+epilogue TFLOP/s, all problems in one launch (1 GPU)"
+
+
+def grouped_oracle_time(w, inputs):
+    import oracle
+    from dense_gemm_elementwise_gb300 import workloads as W
+    As, Bs, auxs, scalars = inputs
+    t0 = time.perf_counter()
+    oracle.grouped_gemm_epilogue(
+        w.problems, w.ab, [W.to_codes(a) for a in As], [W.to_codes(b) for b in Bs],
+        [[W.to_codes(x) for x in per] for per in auxs], [s[2] for s in w.aux], scalars, w.dag,
+        [dt for _, dt in w.outs], threads=oracle.threads_default())
+    return time.perf_counter() - t0
+
+
+def run_grouped_reference(args, w):
+    """The oracle, as it stands, on the whole grouped workload per step."""
+    import oracle
+    from dense_gemm_elementwise_gb300 import workloads as W
+    rank, world, _ = dist_setup(args.gpus)
+    if rank != 0:
+        return
+    inputs = W.make_grouped_inputs(w)
+    for _ in range(args.warmup):
+        grouped_oracle_time(w, inputs)
+    total = sum(grouped_oracle_time(w, inputs) for _ in range(args.steps))
+    ms = total / args.steps * 1e3
+    value = w.flops() / (ms * 1e-3) / 1e12
+    threads = oracle.threads_default()
+    sample = "all %d problems per step, fp64" % len(w.problems)
+    print(json.dumps({
+        "impl": "reference", "metric": GROUPED_METRIC, "value": value, "unit": "TFLOP/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": {"workload": w.name, "problems": len(w.problems)},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0}}), flush=True)
+
+
+def run_grouped(args, w):
+    """One grouped launch per step over every problem of the workload, against
+    one gemm_epi_run launch per problem on the same data."""
+    import torch
+
+    from dense_gemm_elementwise_gb300 import binding as B
+    from dense_gemm_elementwise_gb300 import workloads as W
+
+    rank, world, local = dist_setup(args.gpus)
+    torch.cuda.set_device(local)
+    dev_ = torch.device("cuda", local)
+    stream = torch.cuda.Stream(device=dev_)
+    inputs = W.make_grouped_inputs(w)
+    As, Bs, auxs, scalars = inputs
+    Ad = [a.to(dev_) for a in As]
+    Bd = [b.to(dev_) for b in Bs]
+    auxd = [[x.to(dev_) for x in per] for per in auxs]
+    outs = [[torch.empty(m, n, dtype=W.TORCH_DTYPE[dt], device=dev_) for _, dt in w.outs]
+            for m, n, k in w.problems]
+    dtypes = B.make_dtypes(w.ab, [s[2] for s in w.aux], len(w.scalars), [dt for _, dt in w.outs])
+    dag = B.make_dag(w.dag)
+    opts = None
+    if args.opt:
+        opts = B.ge_options(**{k: int(v) for k, v in (kv.split("=") for kv in args.opt.split(","))})
+    plan = B.gemm_epi_grouped_plan_create(w.problems, dtypes, dag, opts)
+    info = B.gemm_epi_plan_info(plan)
+    flops = w.flops()
+    # the inputs fit in L2: flush it before every timed step by writing 512 MiB
+    # and then reading 256 MiB, so that the write-back of the dirty lines the
+    # write leaves behind is paid before the step, not inside it
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev_)
+    clean = torch.ones(64 << 20, dtype=torch.float32, device=dev_)
+
+    def flush_l2():
+        flush.zero_()
+        clean.sum()
+
+    def timed(fn, steps):
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(steps)]
+        torch.cuda.synchronize()
+        barrier(world)
+        torch.cuda.synchronize()
+        with torch.cuda.stream(stream):
+            for s, e in evs:
+                flush_l2()
+                s.record(stream)
+                fn()
+                e.record(stream)
+        torch.cuda.synchronize()
+        barrier(world)
+        torch.cuda.synchronize()
+        return sum(s.elapsed_time(e) for s, e in evs) / steps
+
+    # arguments marshalled once: a step's host work is one C call, far shorter
+    # than the L2 flush queued before it, so the GPU never waits on the host
+    grouped_call = B.prepare_grouped_run(plan, Ad, Bd, auxd, scalars, outs, stream=stream)
+
+    def grouped():
+        st = grouped_call()
+        if st != B.GE_OK:
+            raise B.GemmEpiError(st, "gemm_epi_grouped_run")
+
+    for _ in range(args.warmup):
+        grouped()
+    torch.cuda.synchronize()
+    if B.gemm_epi_last_error(plan) != B.GE_OK:
+        raise RuntimeError("device-side timeout during warm-up")
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.2)
+    ms = timed(grouped, args.steps)
+    clk = clocks.stop()
+    ms_max = max_over_ranks(ms, world)
+    if B.gemm_epi_last_error(plan) != B.GE_OK:
+        raise RuntimeError("device-side timeout during the timed region")
+    value = world * flops / (ms_max * 1e-3) / 1e12
+
+    # one launch per problem (a plan each), same buffers: issued eagerly (the
+    # host's launch rate included) and replayed from a CUDA graph (device time)
+    plans = [B.gemm_epi_plan_create(1, m, n, k, dtypes, dag, opts) for m, n, k in w.problems]
+    calls = [B.prepare_run(pl, Ad[g], Bd[g], auxd[g], scalars, outs[g], stream=stream)
+             for g, pl in enumerate(plans)]
+
+    def per_problem():
+        for c in calls:
+            st = c()
+            if st != B.GE_OK:
+                raise B.GemmEpiError(st, "gemm_epi_run")
+
+    for _ in range(max(3, args.warmup // 4)):
+        per_problem()
+    pms = timed(per_problem, max(3, args.steps // 4))
+    graph = torch.cuda.CUDAGraph()
+    torch.cuda.synchronize()
+    with torch.cuda.graph(graph, stream=stream):
+        per_problem()
+    graph.replay()
+    torch.cuda.synchronize()
+    gms = timed(graph.replay, max(3, args.steps // 4))
+    del graph
+    torch.cuda.synchronize()
+    if B.gemm_epi_last_error(None) != B.GE_OK:
+        raise RuntimeError("device-side timeout in the per-problem launches")
+    for pl in plans:
+        B.gemm_epi_plan_destroy(pl)
+    separate = {"ms_per_step": pms, "value": flops / (pms * 1e-3) / 1e12,
+                "grouped_speedup": pms / ms, "launches_per_step": len(w.problems),
+                "graph_ms_per_step": gms, "graph_value": flops / (gms * 1e-3) / 1e12,
+                "grouped_speedup_vs_graph": gms / ms}
+
+    e2e = None
+    if not args.no_e2e:
+        hA = [a.pin_memory() for a in As]
+        hB = [b.pin_memory() for b in Bs]
+        haux = [[x.pin_memory() for x in per] for per in auxs]
+        houts = [[torch.empty(o.shape, dtype=o.dtype).pin_memory() for o in per] for per in outs]
+        h2d = sum(t.numel() * t.element_size() for t in hA + hB + [x for p in haux for x in p])
+        d2h = sum(t.numel() * t.element_size() for p in houts for t in p)
+
+        def e2e_step():
+            for d, h in zip(Ad + Bd + [x for p in auxd for x in p],
+                            hA + hB + [x for p in haux for x in p]):
+                d.copy_(h, non_blocking=True)
+            grouped()
+            for pd, ph in zip(outs, houts):
+                for d, h in zip(pd, ph):
+                    h.copy_(d, non_blocking=True)
+
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                e2e_step()
+        ems = max_over_ranks(timed(e2e_step, max(3, args.steps // 10)), world)
+        e2e = {"value": world * flops / (ems * 1e-3) / 1e12, "unit": "TFLOP/s",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": ems}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        import oracle
+        t = grouped_oracle_time(w, inputs)
+        cpu = {"value": flops / t / 1e12, "unit": "TFLOP/s", "cores": oracle.threads_default(),
+               "kind": "oracle", "sample": "all %d problems, fp64, %.2f s wall"
+                                           % (len(w.problems), t)}
+
+    B.gemm_epi_plan_destroy(plan)
+    if rank != 0:
+        return
+    pk, pk_src = peaks()
+    peak = float(pk.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    achieved = flops / (ms * 1e-3) / 1e12
+    print(json.dumps({
+        "metric": GROUPED_METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_max,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": w.ab, "data": "synthetic",
+        "config": {"workload": w.name, "problems": len(w.problems),
+                   "flops_per_step": flops, "alg_bytes_per_step": w.alg_bytes(),
+                   "l2": "flushed before every timed step: 512 MiB write, then 256 MiB read",
+                   "plan": info,
+                   "options": args.opt or "auto",
+                   "parallelism": "replicas" if world > 1 else "single"},
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                     "frac": achieved / peak, "traffic": None,
+                     "peak_source": "%s bf16 dense burst" % pk_src},
+        "gpu_launches": args.steps, "clocks": clk, "one_launch_per_problem": separate,
+        "e2e": e2e, "cpu_baseline": cpu}), flush=True)
+
+
 def main():
     args = parse()
     from dense_gemm_elementwise_gb300 import workloads as W
+    if args.workload in W.GROUPED_BY_NAME:
+        w = W.GROUPED_BY_NAME[args.workload]
+        if args.impl == "reference":
+            run_grouped_reference(args, w)
+        else:
+            from dense_gemm_elementwise_gb300 import build as gbuild
+            gbuild.build()
+            run_grouped(args, w)
+        return
     table = dict(W.BY_NAME)
     table.update({x.name: x for x in W.page_examples()})
     w = table[args.workload]

@@ -36,8 +36,9 @@ OP = {"accum": GE_ACCFETCH, "load": GE_LOAD, "scalar": GE_SCALAR, "broadcast": G
 EXPORTS = ["gemm_epi_plan_create", "gemm_epi_plan_create_ex", "gemm_epi_validate", "gemm_epi_run",
            "gemm_epi_unfused_workspace_bytes", "gemm_epi_run_unfused", "gemm_epi_plan_destroy",
            "gemm_epi_plan_info", "gemm_epi_status_string", "gemm_epi_last_error",
-           "gemm_epi_run_unfused_noalloc"]
+           "gemm_epi_run_unfused_noalloc", "gemm_epi_grouped_plan_create", "gemm_epi_grouped_run"]
 GE_NOALLOC_SCRATCH_BYTES = 16 * 1024 * 1024
+GE_MAX_GROUPS = 4096
 
 
 class ge_node(ctypes.Structure):
@@ -60,6 +61,10 @@ class ge_options(ctypes.Structure):
                 ("stages", ctypes.c_int32), ("max_ctas", ctypes.c_int32),
                 ("raster_group", ctypes.c_int32), ("timeout_ms", ctypes.c_int32),
                 ("debug_flags", ctypes.c_uint32), ("cluster_n", ctypes.c_int32)]
+
+
+class ge_problem(ctypes.Structure):
+    _fields_ = [("M", ctypes.c_int64), ("N", ctypes.c_int64), ("K", ctypes.c_int64)]
 
 
 class ge_plan_info(ctypes.Structure):
@@ -105,6 +110,12 @@ def _load():
                                        ctypes.c_size_t, P]
     L.gemm_epi_run_unfused_noalloc.restype = ctypes.c_int
     L.gemm_epi_run_unfused_noalloc.argtypes = [P, P, P, pp, ctypes.POINTER(ctypes.c_float), pp, P]
+    L.gemm_epi_grouped_plan_create.restype = ctypes.c_int
+    L.gemm_epi_grouped_plan_create.argtypes = [pp, i32, ctypes.POINTER(ge_problem),
+                                               ctypes.POINTER(ge_dtypes), ctypes.POINTER(ge_dag),
+                                               ctypes.POINTER(ge_options)]
+    L.gemm_epi_grouped_run.restype = ctypes.c_int
+    L.gemm_epi_grouped_run.argtypes = [P, pp, pp, pp, ctypes.POINTER(ctypes.c_float), pp, P]
     L.gemm_epi_plan_destroy.restype = None
     L.gemm_epi_plan_destroy.argtypes = [P]
     L.gemm_epi_plan_info.restype = ctypes.c_int
@@ -238,6 +249,53 @@ def gemm_epi_run_unfused_noalloc(plan, A, B, aux, scalars, outs, stream=None, ch
     if check and st != GE_OK:
         raise GemmEpiError(st, "gemm_epi_run_unfused_noalloc")
     return st
+
+
+def gemm_epi_grouped_plan_create(problems, dtypes, dag, options=None):
+    """``problems``: (M, N, K) triples.  Returns the plan handle; raises
+    GemmEpiError with the status code."""
+    n = len(problems)
+    arr = (ge_problem * max(n, 1))(*[ge_problem(int(m), int(nn), int(k)) for m, nn, k in problems])
+    h = ctypes.c_void_p()
+    st = lib.gemm_epi_grouped_plan_create(ctypes.byref(h), n, arr, ctypes.byref(dtypes),
+                                          ctypes.byref(dag),
+                                          ctypes.byref(options) if options is not None else None)
+    if st != GE_OK:
+        raise GemmEpiError(st, "gemm_epi_grouped_plan_create")
+    return h
+
+
+def gemm_epi_grouped_run(plan, As, Bs, aux, scalars, outs, stream=None, check=True):
+    """``As``, ``Bs``: one tensor per problem; ``aux``, ``outs``: one list per
+    problem (its aux slots / output slots), flattened problem-major."""
+    flat_aux = [x for per in aux for x in per]
+    flat_out = [x for per in outs for x in per]
+    st = lib.gemm_epi_grouped_run(plan, _ptr_array(As), _ptr_array(Bs),
+                                  _ptr_array(flat_aux) if flat_aux else None, _scalars(scalars),
+                                  _ptr_array(flat_out), _stream(stream))
+    if check and st != GE_OK:
+        raise GemmEpiError(st, "gemm_epi_grouped_run")
+    return st
+
+
+def prepare_grouped_run(plan, As, Bs, aux, scalars, outs, stream=None):
+    """Marshal the arguments of gemm_epi_grouped_run once; the returned
+    callable issues the run with no per-call Python marshalling and returns
+    its status."""
+    flat_aux = [x for per in aux for x in per]
+    flat_out = [x for per in outs for x in per]
+    args = (plan, _ptr_array(As), _ptr_array(Bs), _ptr_array(flat_aux) if flat_aux else None,
+            _scalars(scalars), _ptr_array(flat_out), _stream(stream))
+    fn = lib.gemm_epi_grouped_run
+    return lambda: fn(*args)
+
+
+def prepare_run(plan, A, B, aux, scalars, outs, stream=None):
+    """As prepare_grouped_run, for gemm_epi_run."""
+    args = (plan, _addr(A), _addr(B), _ptr_array(aux), _scalars(scalars), _ptr_array(outs),
+            _stream(stream))
+    fn = lib.gemm_epi_run
+    return lambda: fn(*args)
 
 
 def gemm_epi_status_string(status):

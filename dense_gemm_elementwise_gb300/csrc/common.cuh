@@ -90,7 +90,22 @@ constexpr int UMMA_K = 16;   // K of one tcgen05.mma.kind::f16
 constexpr int kEpiWarps = 4;
 constexpr int kThreads = 64 + 32 * kEpiWarps;  // producer warp, MMA warp, epilogue warps
 constexpr int kMaxStages = 8;
-constexpr int kMaxAuxStages = 4;
+constexpr int kMaxAuxStages = 8;
+
+// One problem of a grouped GEMM, in device memory (a table uploaded per run).
+// Its tiles are [tile_begin, tile_end) of the launch's tile sequence; within
+// the problem they are ordered like the tiles of one batch of a batched GEMM.
+// The tile -> (problem, m block, n block, k blocks) map itself is a separate
+// table (KParams::tile_info), fixed when the plan is made.
+struct alignas(128) GroupDesc {
+  CUtensorMap tmA;                    // (K, M, 1)
+  CUtensorMap tmB;                    // (N, K, 1)
+  CUtensorMap tmAux[GE_MAX_TMA_AUX];  // (N, M, 1)
+  CUtensorMap tmOut[GE_MAX_OUT];      // (N, M, 1)
+  const void *bcast_ptr[GE_MAX_AUX];
+  const void *cbcast_ptr[GE_MAX_AUX];
+  int32_t M, N, num_m_blk, num_n_blk, num_kb, tile_begin, tile_end, problem;
+};
 
 struct KParams {
   CUtensorMap tmA;                    // (K, M, L) box (64, 128, 1), 128B swizzle
@@ -114,6 +129,9 @@ struct KParams {
   uint32_t b_lbo, b_sbo;  // B smem descriptor strides (bytes)
   uint64_t timeout_ns;
   uint32_t debug_flags;
+  const GroupDesc *groups;  // grouped GEMM: the problem table (else nullptr)
+  const int4 *tile_info;    // grouped GEMM: per tile {problem entry, m block, n block, k blocks}
+  int32_t num_groups;
 };
 
 // Unfused elementwise kernel parameters.

@@ -16,6 +16,11 @@
 // tile i+1.  Ragged M/N/K edges are handled by TMA: out-of-range loads read
 // zeros, out-of-range stores are dropped.
 //
+// A grouped launch (KParams::groups set) runs many problems of different
+// sizes: tile t is looked up in a per-tile table (problem, m/n block, k
+// blocks), and each problem brings its own tensor maps and vector pointers
+// from a problem table in global memory.
+//
 // MC = 2: two CTA pairs of a 4-CTA cluster compute adjacent N tiles with the
 // same A rows; each CTA fetches half of its A rows and multicasts them to its
 // counterpart in the other pair (25% less L2->SM traffic).  A stage is free
@@ -61,25 +66,71 @@ constexpr uint32_t kBarEmpty = 64;                     // kMaxStages x 8
 constexpr uint32_t kBarTmemFull = 128;                 // 2 x 8
 constexpr uint32_t kBarTmemEmpty = 144;                // 2 x 8
 constexpr uint32_t kBarAux = 160;                      // kEpiWarps x kMaxAuxStages x 8
-constexpr uint32_t kBarDrain = kBarAux + 8 * kEpiWarps * kMaxAuxStages;  // 288
-constexpr uint32_t kTmemSlot = kBarDrain + 8;          // 296
-constexpr uint32_t kAbortFlag = kTmemSlot + 4;         // 300
+constexpr uint32_t kBarDrain = kBarAux + 8 * kEpiWarps * kMaxAuxStages;  // 416
+constexpr uint32_t kTmemSlot = kBarDrain + 8;          // 424
+constexpr uint32_t kAbortFlag = kTmemSlot + 4;         // 428
 constexpr uint32_t kBarBlockBytes = 512;
+static_assert(kAbortFlag + 4 <= kBarBlockBytes, "barrier block overflow");
 
-__device__ __forceinline__ void tile_coords(const KParams &p, int t, int &l, int &mb, int &nb) {
-  const int per_batch = p.num_m_blk * p.num_n_blk;
+__device__ __forceinline__ void tile_coords(int num_m_blk, int num_n_blk, int G, int t, int &l,
+                                            int &mb, int &nb) {
+  const int per_batch = num_m_blk * num_n_blk;
   l = t / per_batch;
   const int r = t - l * per_batch;
   // raster: groups of G m-blocks; within a group m varies fastest, so tiles
   // processed at the same time share their B columns (and A rows across groups)
-  const int G = p.raster_group;
-  const int group = r / (G * p.num_n_blk);
+  const int group = r / (G * num_n_blk);
   const int first_m = group * G;
-  const int gsize = min(p.num_m_blk - first_m, G);
-  const int rr = r - group * G * p.num_n_blk;
+  const int gsize = min(num_m_blk - first_m, G);
+  const int rr = r - group * G * num_n_blk;
   mb = first_m + rr % gsize;
   nb = rr / gsize;
 }
+
+// A tile of the launch: its batch and block coordinates, its k-block count and,
+// for a grouped GEMM, the problem it belongs to.
+struct TileRef {
+  int l, mb, nb, num_kb;
+  const GroupDesc *gd;  // nullptr: the batched problem described by KParams
+};
+
+// Tile t of the launch: computed for a batched GEMM, one 16-byte table load
+// for a grouped one.
+__device__ __forceinline__ TileRef locate(const KParams &p, int t) {
+  TileRef r;
+  if (p.groups == nullptr) {
+    tile_coords(p.num_m_blk, p.num_n_blk, p.raster_group, t, r.l, r.mb, r.nb);
+    r.num_kb = p.num_kb;
+    r.gd = nullptr;
+  } else {
+    const int4 ti = __ldg(p.tile_info + t);
+    r.l = 0;
+    r.mb = ti.y;
+    r.nb = ti.z;
+    r.num_kb = ti.w;
+    r.gd = p.groups + ti.x;
+  }
+  return r;
+}
+
+// This CTA's tiles in order, each looked up one tile ahead so that a table
+// load overlaps the work on the tile before it.
+struct TileCursor {
+  const KParams &p;
+  int unit, n_units, count, i;
+  TileRef nxt;
+  __device__ __forceinline__ TileCursor(const KParams &p_, int unit_, int n_units_, int count_)
+      : p(p_), unit(unit_), n_units(n_units_), count(count_), i(0) {
+    if (count > 0) nxt = locate(p, unit);
+  }
+  __device__ __forceinline__ TileRef next() {
+    const TileRef r = nxt;
+    if (++i < count) nxt = locate(p, unit + i * n_units);
+    return r;
+  }
+  // the tile after the one next() returned last (valid while i < count)
+  __device__ __forceinline__ bool has_more() const { return i < count; }
+};
 
 struct Waiter {
   volatile uint32_t *abort_flag;  // shared: this CTA gave up
@@ -131,6 +182,9 @@ struct Waiter {
 // global memory (the same addresses for every lane).
 struct FusedMem {
   const KParams *p;
+  const void *const *bptr;  // row-broadcast vectors of this tile's problem
+  const void *const *cptr;  // column-broadcast vectors
+  int M, N;                 // this tile's problem
   const uint8_t *aux_stage;
   uint8_t *out_stage;
   int row, half, col0;
@@ -141,11 +195,11 @@ struct FusedMem {
   }
   template <int DT>
   __device__ __forceinline__ void bcast(uint32_t i, float (&t)[CH]) const {
-    row_load<DT, CH>(p->bcast_ptr[i], col0, p->N, t);
+    row_load<DT, CH>(bptr[i], col0, N, t);
   }
   template <int DT>
   __device__ __forceinline__ void cbcast(uint32_t i, float (&t)[CH]) const {
-    const float v = grow < p->M ? load_one<DT>(p->cbcast_ptr[i], grow) : 0.f;
+    const float v = grow < M ? load_one<DT>(cptr[i], grow) : 0.f;
 #pragma unroll
     for (int e = 0; e < CH; ++e) t[e] = v;
   }
@@ -193,7 +247,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_epi_kernel(const __grid_cons
     *abort_flag = 0u;
     fence_mbarrier_init();
   }
-  if (warp == 0 && lane == 0) {
+  if (warp == 0 && lane == 0 && p.groups == nullptr) {
     prefetch_tensormap(&p.tmA);
     prefetch_tensormap(&p.tmB);
   }
@@ -217,13 +271,21 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_epi_kernel(const __grid_cons
       int fills = 0, skipped = -1;
       bool skip = (p.debug_flags & GE_DEBUG_SKIP_FIRST_LOAD) != 0u;
       bool ok = true;
+      TileCursor tc(p, unit, n_units, my_tiles);
+      const GroupDesc *ready_gd = nullptr;  // problem whose A/B maps are fenced and prefetched
       for (int i = 0; ok && i < my_tiles; ++i) {
-        int l, mb, nb;
-        tile_coords(p, unit + i * n_units, l, mb, nb);
-        nb = nb * MC + pair;
+        const TileRef tr = tc.next();
+        const int l = tr.l, mb = tr.mb, nb = tr.nb * MC + pair;
+        const CUtensorMap *mA = tr.gd ? &tr.gd->tmA : &p.tmA;
+        const CUtensorMap *mB = tr.gd ? &tr.gd->tmB : &p.tmB;
+        if (tr.gd && tr.gd != ready_gd) {
+          fence_tensormap_acquire(mA);
+          fence_tensormap_acquire(mB);
+          ready_gd = tr.gd;
+        }
         const int m0 = mb * T::kMmaM + static_cast<int>(rank) * BM;
         const int n0 = nb * BN + static_cast<int>(rank) * T::kBnLocal;
-        for (int kb = 0; kb < p.num_kb; ++kb) {
+        for (int kb = 0; kb < tr.num_kb; ++kb) {
           if (!wt.wait(bar + kBarEmpty + 8 * stage, phase ^ 1u, SITE_PRODUCER_EMPTY)) {
             ok = false;
             break;
@@ -239,25 +301,25 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_epi_kernel(const __grid_cons
               const uint32_t fb = mapa_shared(fb_local, leader);
               if (rank == 0) mbar_arrive_expect_tx(fb_local, p.tx_bytes);
               if constexpr (MC == 1) {
-                tma_load_3d_pair(sa, &p.tmA, fb, kb * BK, m0, l);
+                tma_load_3d_pair(sa, mA, fb, kb * BK, m0, l);
               } else {
                 // this pair fetches its share of the A rows and multicasts it to
                 // the CTA with the same rank in every pair of the cluster
                 uint16_t mask = 0;
 #pragma unroll
                 for (int pp = 0; pp < MC; ++pp) mask |= static_cast<uint16_t>(1u << (pp * CG + rank));
-                tma_load_3d_pair_mc(sa + pair * T::kALoadRows * 128, &p.tmA, fb, kb * BK,
+                tma_load_3d_pair_mc(sa + pair * T::kALoadRows * 128, mA, fb, kb * BK,
                                     m0 + pair * T::kALoadRows, l, mask);
               }
 #pragma unroll
               for (int j = 0; j < T::kBAtoms; ++j)
-                tma_load_3d_pair(sbb + j * 8192, &p.tmB, fb, n0 + 64 * j, kb * BK, l);
+                tma_load_3d_pair(sbb + j * 8192, mB, fb, n0 + 64 * j, kb * BK, l);
             } else {
               mbar_arrive_expect_tx(fb_local, p.tx_bytes);
-              tma_load_3d(sa, &p.tmA, fb_local, kb * BK, m0, l);
+              tma_load_3d(sa, mA, fb_local, kb * BK, m0, l);
 #pragma unroll
               for (int j = 0; j < T::kBAtoms; ++j)
-                tma_load_3d(sbb + j * 8192, &p.tmB, fb_local, n0 + 64 * j, kb * BK, l);
+                tma_load_3d(sbb + j * 8192, mB, fb_local, n0 + 64 * j, kb * BK, l);
             }
           }
           ++fills;
@@ -265,6 +327,14 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_epi_kernel(const __grid_cons
             stage = 0;
             phase ^= 1u;
           }
+        }
+        // while the MMA drains this tile, make the next problem's maps ready
+        if (tc.has_more() && tc.nxt.gd && tc.nxt.gd != ready_gd) {
+          ready_gd = tc.nxt.gd;
+          fence_tensormap_acquire(&ready_gd->tmA);
+          fence_tensormap_acquire(&ready_gd->tmB);
+          prefetch_tensormap(&ready_gd->tmA);
+          prefetch_tensormap(&ready_gd->tmB);
         }
       }
       if (ok) {
@@ -297,14 +367,16 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_epi_kernel(const __grid_cons
       int abuf = 0;
       uint32_t aphase = 0;
       bool ok = true;
+      TileCursor tc(p, unit, n_units, my_tiles);
       for (int i = 0; ok && i < my_tiles; ++i) {
+        const int num_kb = tc.next().num_kb;
         if (!wt.wait<CG == 2>(bar + kBarTmemEmpty + 8 * abuf, aphase ^ 1u, SITE_MMA_TMEM_EMPTY)) {
           ok = false;
           break;
         }
         tc_fence_after();
         const uint32_t d = tmem_base + static_cast<uint32_t>(abuf * BN);
-        for (int kb = 0; kb < p.num_kb; ++kb) {
+        for (int kb = 0; kb < num_kb; ++kb) {
           if (!wt.wait(bar + kBarFull + 8 * stage, phase, SITE_MMA_FULL)) {
             ok = false;
             break;
@@ -358,17 +430,26 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_epi_kernel(const __grid_cons
     uint32_t aphase = 0;
     bool ok = true;
     int pf_tile = -1, pf_x0 = 0, pf_y = 0, pf_l = 0;  // prefetch: coordinates of tile pf_tile
+    TileCursor pf_tc(p, unit, n_units, my_tiles);        // tiles of the aux prefetch
+    TileCursor tc(p, unit, n_units, my_tiles);           // tiles of the epilogue proper
+    const CUtensorMap *pf_maps = p.tmAux;               // aux maps of tile pf_tile
+    const GroupDesc *out_gd = nullptr;                  // problem whose output maps are fenced
 
     // TMA loads of every Load tensor for this warp's 32 rows of step gi
     auto issue_aux = [&](int gi) {
       const int ii = gi / T::kSteps;
       if (ii != pf_tile) {
-        int mb2, nb2;
-        tile_coords(p, unit + ii * n_units, pf_l, mb2, nb2);
-        nb2 = nb2 * MC + pair;
+        const TileRef tr = pf_tc.next();  // tiles are entered in order, one at a time
+        pf_l = tr.l;
         pf_tile = ii;
-        pf_x0 = nb2 * BN;
-        pf_y = mb2 * T::kMmaM + static_cast<int>(rank) * BM + q * 32;
+        pf_x0 = (tr.nb * MC + pair) * BN;
+        pf_y = tr.mb * T::kMmaM + static_cast<int>(rank) * BM + q * 32;
+        if (tr.gd && pf_maps != tr.gd->tmAux)
+          for (int a = 0; a < p.prog.n_tma_aux; ++a) {
+            fence_tensormap_acquire(&tr.gd->tmAux[a]);
+            prefetch_tensormap(&tr.gd->tmAux[a]);
+          }
+        pf_maps = tr.gd ? tr.gd->tmAux : p.tmAux;
       }
       const int as = gi % SA;
       const uint32_t ab = auxbar_w + 8u * as;
@@ -377,15 +458,24 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_epi_kernel(const __grid_cons
       mbar_arrive_expect_tx(ab, p.aux_tx_bytes);
       const int x = pf_x0 + (gi - ii * T::kSteps) * EW;
       for (int a = 0; a < p.prog.n_tma_aux; ++a)
-        tma_load_3d(smem_u32(dst + p.aux_off[a]), &p.tmAux[a], ab, x, pf_y, pf_l);
+        tma_load_3d(smem_u32(dst + p.aux_off[a]), &pf_maps[a], ab, x, pf_y, pf_l);
     };
 
     for (int i = 0; ok && i < my_tiles; ++i) {
-      int l, mb, nb;
-      tile_coords(p, unit + i * n_units, l, mb, nb);
-      nb = nb * MC + pair;
+      const TileRef tr = tc.next();
+      const int l = tr.l, mb = tr.mb, nb = tr.nb * MC + pair;
       const int m0 = mb * T::kMmaM + static_cast<int>(rank) * BM + q * 32;
       const int n0 = nb * BN;
+      const CUtensorMap *out_maps = tr.gd ? tr.gd->tmOut : p.tmOut;
+      const void *const *bptr = tr.gd ? tr.gd->bcast_ptr : p.bcast_ptr;
+      const void *const *cptr = tr.gd ? tr.gd->cbcast_ptr : p.cbcast_ptr;
+      const int pM = tr.gd ? __ldg(&tr.gd->M) : p.M;
+      const int pN = tr.gd ? __ldg(&tr.gd->N) : p.N;
+      // output maps of this problem, unless made ready during the last tile
+      if (lane == 0 && tr.gd && tr.gd != out_gd) {
+        for (int o = 0; o < p.prog.n_out; ++o) fence_tensormap_acquire(&out_maps[o]);
+        out_gd = tr.gd;
+      }
       // start this tile's aux loads before its accumulator is ready
       if (has_aux && lane == 0) {
         while (issued < total && issued < g + SA) issue_aux(issued++);
@@ -395,6 +485,15 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_epi_kernel(const __grid_cons
       if (!__all_sync(0xffffffffu, got)) {
         ok = false;
         break;
+      }
+      // the next tile's problem: make its output maps ready while this tile's
+      // epilogue runs (its table entry was loaded with this tile's)
+      if (lane == 0 && tc.has_more() && tc.nxt.gd && tc.nxt.gd != out_gd) {
+        out_gd = tc.nxt.gd;
+        for (int o = 0; o < p.prog.n_out; ++o) {
+          fence_tensormap_acquire(&out_gd->tmOut[o]);
+          prefetch_tensormap(&out_gd->tmOut[o]);
+        }
       }
       tc_fence_after();
       for (int s = 0; s < T::kSteps; ++s, ++g) {
@@ -431,14 +530,15 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_epi_kernel(const __grid_cons
         uint8_t *ostage = out_w + obuf * p.out_stage_bytes;
         const uint8_t *astage = aux_w + (g % SA) * p.aux_stage_bytes;
         const int c0 = n0 + s * EW;
-        Epi::template run<CH>(p.prog, acc0, FusedMem{&p, astage, ostage, lane, 0, c0, m0 + lane});
-        Epi::template run<CH>(p.prog, acc1,
-                              FusedMem{&p, astage, ostage, lane, 1, c0 + CH, m0 + lane});
+        Epi::template run<CH>(p.prog, acc0, FusedMem{&p, bptr, cptr, pM, pN, astage, ostage, lane,
+                                                     0, c0, m0 + lane});
+        Epi::template run<CH>(p.prog, acc1, FusedMem{&p, bptr, cptr, pM, pN, astage, ostage, lane,
+                                                     1, c0 + CH, m0 + lane});
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) {
           for (int o = 0; o < p.prog.n_out; ++o)
-            tma_store_3d(&p.tmOut[o], smem_u32(ostage + p.out_off[o]), c0, m0, l);
+            tma_store_3d(&out_maps[o], smem_u32(ostage + p.out_off[o]), c0, m0, l);
           bulk_commit_group();
         }
         obuf ^= 1;

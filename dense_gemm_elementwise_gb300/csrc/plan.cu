@@ -13,6 +13,7 @@
 #include <cstring>
 #include <mutex>
 #include <new>
+#include <vector>
 
 #include "catalog.cuh"
 #include "common.cuh"
@@ -182,8 +183,11 @@ constexpr int kBarBlock = 512;
 constexpr int kAlignSlack = 1024;
 
 // Shared-memory layout for (cg, bn) and a program; stages = 0 picks the most
-// that fit.  Returns GE_ERR_SMEM if fewer than 2 (or the requested count) fit.
-int make_layout(Layout *Lo, int cg, int bn, int want_stages, const EpiProgram &P, int max_smem) {
+// that fit.  The aux prefetch gets the deepest ring (up to max_aux) that still
+// leaves min_main mainloop stages.  Returns GE_ERR_SMEM if fewer than 2 (or the
+// requested count) fit.
+int make_layout(Layout *Lo, int cg, int bn, int want_stages, const EpiProgram &P, int max_smem,
+                int max_aux = 4, int min_main = 5) {
   const uint32_t a_bytes = BM * BK * 2;
   const uint32_t b_bytes = static_cast<uint32_t>(bn / cg) * BK * 2;
   uint32_t aux_stage = 0, out_stage = 0;
@@ -201,13 +205,12 @@ int make_layout(Layout *Lo, int cg, int bn, int want_stages, const EpiProgram &P
     const int s = room > 0 ? static_cast<int>(room / (a_bytes + b_bytes)) : 0;
     return std::min(s, kMaxStages);
   };
-  // deepest aux prefetch that still leaves at least 5 mainloop stages
   int sa = 1, stages = stages_with(1);
   if (P.n_tma_aux > 0) {
     sa = 2;
     stages = stages_with(2);
-    for (int cand = kMaxAuxStages; cand > 2; --cand)
-      if (stages_with(cand) >= 5) {
+    for (int cand = std::min(max_aux, kMaxAuxStages); cand > 2; --cand)
+      if (stages_with(cand) >= min_main) {
         sa = cand;
         stages = stages_with(cand);
         break;
@@ -242,6 +245,8 @@ int make_layout(Layout *Lo, int cg, int bn, int want_stages, const EpiProgram &P
 }  // namespace
 
 // ------------------------------------------------------------------- plan --
+constexpr int kGroupSlots = 4;  // problem tables of a grouped plan, used in turn
+
 struct gemm_epi_plan {
   int64_t L = 0, M = 0, N = 0, K = 0;
   ge_dtypes dt{};
@@ -261,6 +266,30 @@ struct gemm_epi_plan {
   const void *aA = nullptr, *aB = nullptr;
   void *aWs = nullptr;
   bool acc_maps_ok = false;
+  // grouped GEMM (n_groups > 0)
+  int n_groups = 0;
+  std::vector<ge_problem> problems;
+  std::vector<int> order;           // problem of each table entry (most k-blocks first)
+  GroupDesc *d_desc = nullptr;      // kGroupSlots tables of n_groups entries, device
+  GroupDesc *h_desc = nullptr;      // their pinned host staging
+  int4 *d_tiles = nullptr;          // per tile {table entry, m block, n block, k blocks}
+  cudaEvent_t ev[kGroupSlots] = {};  // recorded after the latest run that read each table
+  bool ev_used[kGroupSlots] = {};
+  cudaStream_t ev_stream[kGroupSlots] = {};  // the stream of that run
+  int slot = -1;                    // table of the latest run
+  std::vector<const void *> slot_ptrs[kGroupSlots];  // pointers each table was built for
+
+  ~gemm_epi_plan() {
+    for (int s = 0; s < kGroupSlots; ++s)
+      if (ev[s]) {
+        if (ev_used[s]) cudaEventSynchronize(ev[s]);
+        cudaEventDestroy(ev[s]);
+      }
+    if (d_desc) cudaFree(d_desc);
+    if (d_tiles) cudaFree(d_tiles);
+    if (h_desc) cudaFreeHost(h_desc);
+    cudaGetLastError();
+  }
 };
 
 namespace {
@@ -593,7 +622,7 @@ int gemm_epi_plan_info(const gemm_epi_plan *pl, ge_plan_info *info) {
 
 int gemm_epi_run(gemm_epi_plan *pl, const void *A, const void *B, const void *const *aux,
                  const float *scalars, void *const *outs, void *stream) {
-  if (!pl) return GE_ERR_INVALID;
+  if (!pl || pl->n_groups) return GE_ERR_INVALID;
   int st = check_run_args(pl, A, B, aux, scalars, outs);
   if (st != GE_OK) return st;
   KParams &kp = pl->kp;
@@ -624,14 +653,14 @@ int gemm_epi_run(gemm_epi_plan *pl, const void *A, const void *B, const void *co
 }
 
 size_t gemm_epi_unfused_workspace_bytes(const gemm_epi_plan *pl) {
-  if (!pl) return 0;
+  if (!pl || pl->n_groups) return 0;
   return static_cast<size_t>(pl->L) * static_cast<size_t>(pl->M) * static_cast<size_t>(pl->N) * 4u;
 }
 
 int gemm_epi_run_unfused(gemm_epi_plan *pl, const void *A, const void *B, const void *const *aux,
                          const float *scalars, void *const *outs, void *workspace,
                          size_t workspace_bytes, void *stream) {
-  if (!pl) return GE_ERR_INVALID;
+  if (!pl || pl->n_groups) return GE_ERR_INVALID;
   int st = check_run_args(pl, A, B, aux, scalars, outs);
   if (st != GE_OK) return st;
   if (!workspace || !aligned16(workspace) || workspace_bytes < gemm_epi_unfused_workspace_bytes(pl))
@@ -675,6 +704,342 @@ int gemm_epi_run_unfused(gemm_epi_plan *pl, const void *A, const void *B, const 
   void *args[] = {&ep};
   e = cudaLaunchKernelExC(&cfg, ew_kernel(pl->epi), args);
   return e == cudaSuccess ? GE_OK : GE_ERR_CUDA;
+}
+
+}  // extern "C"
+
+// ------------------------------------------------------------ grouped GEMM --
+namespace {
+
+// Cost of one tile of a grouped problem in SM clocks: the mainloop (the
+// model of est_cycles) or the epilogue, whichever is slower, since the two
+// overlap across consecutive tiles, plus a fixed cost per tile.  The epilogue
+// and fixed terms are fitted to measured launches of many short problems,
+// whose tiles are short: 900 clocks per 16-column chunk, 4000 per tile.
+double grouped_tile_cycles(int64_t K, int cg, int bn) {
+  const int64_t kb = (K + BK - 1) / BK;
+  const double fill = double((BM + bn / cg) * BK * 2) / 48.0;
+  const double main = kb * std::max(2.0 * bn, fill);
+  return std::max(main, (bn / CH) * 900.0) + 4000.0;
+}
+
+// The launch deals the tiles (problems with the most k-blocks first) round
+// robin to the units; it lasts about as long as the busiest unit.
+double est_cycles_grouped(const gemm_epi_plan *pl, const std::vector<int> &order, int cg, int bn,
+                          int units) {
+  std::vector<double> busy(static_cast<size_t>(units), 0.0);
+  int64_t t = 0;
+  for (int g : order) {
+    const ge_problem &pr = pl->problems[g];
+    const int64_t tiles = ((pr.M + BM * cg - 1) / (BM * cg)) * ((pr.N + bn - 1) / bn);
+    const double c = grouped_tile_cycles(pr.K, cg, bn);
+    // whole rounds of the deal add c to every unit; the rest to the next ones
+    const int64_t rounds = tiles / units, rest = tiles % units;
+    for (int u = 0; u < units; ++u) busy[u] += rounds * c;
+    for (int64_t r = 0; r < rest; ++r) busy[(t + r) % units] += c;
+    t = (t + tiles) % units;
+  }
+  return *std::max_element(busy.begin(), busy.end());
+}
+
+int configure_grouped(gemm_epi_plan *pl) {
+  const ge_options &o = pl->opt;
+  if (o.cta_group != 0 && o.cta_group != 1 && o.cta_group != 2) return GE_ERR_INVALID;
+  if (o.tile_n != 0 && o.tile_n != 64 && o.tile_n != 128 && o.tile_n != 256) return GE_ERR_INVALID;
+  if (o.stages < 0 || o.stages > kMaxStages || o.max_ctas < 0 || o.raster_group < 0 ||
+      o.timeout_ms < 0 || (o.cluster_n != 0 && o.cluster_n != 1 && o.cluster_n != 2))
+    return GE_ERR_INVALID;
+  if (o.cluster_n == 2) return GE_ERR_UNSUPPORTED;
+  const int cand[5][2] = {{2, 256}, {2, 128}, {1, 256}, {1, 128}, {1, 64}};
+  int sms = pl->num_sms;
+  if (o.max_ctas) sms = std::min(sms, o.max_ctas);
+  // table order: problems with the most k-blocks first, so the round-robin
+  // deal hands every unit its long tiles early and the short ones last
+  const int n = pl->n_groups;
+  pl->order.resize(n);
+  for (int g = 0; g < n; ++g) pl->order[g] = g;
+  std::stable_sort(pl->order.begin(), pl->order.end(), [&](int a, int b) {
+    return pl->problems[a].K > pl->problems[b].K;
+  });
+  int best = -1;
+  double best_c = 0;
+  for (int c = 0; c < 5; ++c) {
+    const int cg = cand[c][0], bn = cand[c][1];
+    if (o.cta_group && o.cta_group != cg) continue;
+    if (o.tile_n && o.tile_n != bn) continue;
+    if (sms < cg) continue;
+    const double cost = est_cycles_grouped(pl, pl->order, cg, bn, sms / cg);
+    if (best < 0 || cost < best_c * 0.98) {
+      best = c;
+      best_c = cost;
+    }
+  }
+  if (best < 0) return GE_ERR_INVALID;
+  const int cg = cand[best][0], bn = cand[best][1];
+  // short problems make short tiles, whose epilogue would wait on aux loads
+  // issued only a few steps ahead: prefetch up to two tiles' steps of aux
+  // data, keeping 4 mainloop stages
+  int st = make_layout(&pl->lay, cg, bn, o.stages, pl->prog, pl->max_smem,
+                       std::min(kMaxAuxStages, 2 * bn / EW), 4);
+  if (st != GE_OK) return st;
+  Layout &Lo = pl->lay;
+  Lo.mc = 1;
+  Lo.raster_group = o.raster_group ? o.raster_group : 8;
+  int64_t tiles = 0;
+  for (int j = 0; j < n; ++j) {
+    const ge_problem &pr = pl->problems[pl->order[j]];
+    tiles += ((pr.M + BM * cg - 1) / (BM * cg)) * ((pr.N + bn - 1) / bn);
+  }
+  if (tiles > (int64_t(1) << 24)) return GE_ERR_SHAPE;  // the tile table: 16 bytes a tile
+  Lo.num_tiles = static_cast<int>(tiles);
+  const void *fn = gemm_kernel(cg, bn, 1, pl->epi);
+  if (!fn) return GE_ERR_INVALID;
+  if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, Lo.smem) != cudaSuccess)
+    return GE_ERR_CUDA;
+  int units = std::max(1, sms / cg);
+  if (cg > 1) {
+    int clusters = 0;
+    cudaLaunchAttribute attr[1];
+    cudaLaunchConfig_t cfg = launch_config(Lo, nullptr, attr);
+    cfg.gridDim = dim3(static_cast<unsigned>(cg));
+    if (cudaOccupancyMaxActiveClusters(&clusters, fn, &cfg) == cudaSuccess && clusters > 0)
+      units = std::min(units, clusters);
+    cudaGetLastError();
+  }
+  units = static_cast<int>(std::min<int64_t>(units, tiles));
+  Lo.grid = units * cg;
+  return GE_OK;
+}
+
+// Host copy of tile_coords: the order of one problem's tiles.
+void raster_coords(int num_m_blk, int num_n_blk, int G, int r, int *mb, int *nb) {
+  const int group = r / (G * num_n_blk);
+  const int first_m = group * G;
+  const int gsize = std::min(num_m_blk - first_m, G);
+  const int rr = r - group * G * num_n_blk;
+  *mb = first_m + rr % gsize;
+  *nb = rr / gsize;
+}
+
+// The launch's tile sequence: every table entry's tiles in turn.
+std::vector<int4> grouped_tile_table(const gemm_epi_plan *pl) {
+  std::vector<int4> t;
+  t.reserve(static_cast<size_t>(pl->lay.num_tiles));
+  const GroupDesc *d = pl->h_desc;  // table 0 (the shapes are the same in all)
+  for (int j = 0; j < pl->n_groups; ++j)
+    for (int r = 0; r < d[j].tile_end - d[j].tile_begin; ++r) {
+      int mb = 0, nb = 0;
+      raster_coords(d[j].num_m_blk, d[j].num_n_blk, pl->lay.raster_group, r, &mb, &nb);
+      t.push_back(make_int4(j, mb, nb, d[j].num_kb));
+    }
+  return t;
+}
+
+// The sizes and tile ranges of every table entry (the same in all tables).
+void fill_group_shapes(gemm_epi_plan *pl) {
+  const int n = pl->n_groups, cg = pl->lay.cg, bn = pl->lay.bn;
+  for (int s = 0; s < kGroupSlots; ++s) {
+    int begin = 0;
+    for (int j = 0; j < n; ++j) {
+      const ge_problem &pr = pl->problems[pl->order[j]];
+      GroupDesc &d = pl->h_desc[s * n + j];
+      std::memset(static_cast<void *>(&d), 0, sizeof(d));
+      d.M = static_cast<int32_t>(pr.M);
+      d.N = static_cast<int32_t>(pr.N);
+      d.num_m_blk = static_cast<int32_t>((pr.M + BM * cg - 1) / (BM * cg));
+      d.num_n_blk = static_cast<int32_t>((pr.N + bn - 1) / bn);
+      d.num_kb = static_cast<int32_t>((pr.K + BK - 1) / BK);
+      d.tile_begin = begin;
+      begin += d.num_m_blk * d.num_n_blk;
+      d.tile_end = begin;
+      d.problem = pl->order[j];
+    }
+  }
+}
+
+// Encode the tensor maps and vector pointers of table `s` for one run.
+bool build_group_table(gemm_epi_plan *pl, int s, const void *const *A, const void *const *B,
+                       const void *const *aux, void *const *outs) {
+  const EpiProgram &P = pl->prog;
+  const int n = pl->n_groups, na = pl->dt.n_aux, no = pl->dt.n_out, ab = pl->dt.ab;
+  for (int j = 0; j < n; ++j) {
+    const int g = pl->order[j];
+    const ge_problem &pr = pl->problems[g];
+    GroupDesc &d = pl->h_desc[s * n + j];
+    const uint64_t M = pr.M, N = pr.N, K = pr.K;
+    if (!encode3d(&d.tmA, ab, A[g], K, M, 1, BK, BM, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B) ||
+        !encode3d(&d.tmB, ab, B[g], N, K, 1, 64, BK, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B))
+      return false;
+    for (int t = 0; t < P.n_tma_aux; ++t)
+      if (!encode3d(&d.tmAux[t], P.tma_aux_dtype[t], aux[g * na + P.tma_aux_slot[t]], N, M, 1, EW,
+                    32, epi_swizzle(P.tma_aux_dtype[t]), CU_TENSOR_MAP_L2_PROMOTION_L2_128B))
+        return false;
+    for (int o = 0; o < no; ++o)
+      if (!encode3d(&d.tmOut[o], P.out_dtype[o], outs[g * no + o], N, M, 1, EW, 32,
+                    epi_swizzle(P.out_dtype[o]), CU_TENSOR_MAP_L2_PROMOTION_L2_128B))
+        return false;
+    for (int b = 0; b < P.n_bcast; ++b) d.bcast_ptr[b] = aux[g * na + P.bcast_slot[b]];
+    for (int b = 0; b < P.n_cbcast; ++b) d.cbcast_ptr[b] = aux[g * na + P.cbcast_slot[b]];
+  }
+  return true;
+}
+
+int check_grouped_args(const gemm_epi_plan *pl, const void *const *A, const void *const *B,
+                       const void *const *aux, const float *scalars, void *const *outs) {
+  if (!A || !B || !outs) return GE_ERR_MISSING_ARG;
+  if (pl->dt.n_scalar > 0 && !scalars) return GE_ERR_MISSING_ARG;
+  const EpiProgram &P = pl->prog;
+  const int na = pl->dt.n_aux, no = pl->dt.n_out;
+  if ((P.n_tma_aux + P.n_bcast + P.n_cbcast) > 0 && !aux) return GE_ERR_MISSING_ARG;
+  auto check = [](const void *p) {
+    return !p ? GE_ERR_MISSING_ARG : (aligned16(p) ? GE_OK : GE_ERR_MISALIGNED);
+  };
+  for (int g = 0; g < pl->n_groups; ++g) {
+    int st = GE_OK;
+    if ((st = check(A[g])) != GE_OK || (st = check(B[g])) != GE_OK) return st;
+    for (int t = 0; t < P.n_tma_aux; ++t)
+      if ((st = check(aux[g * na + P.tma_aux_slot[t]])) != GE_OK) return st;
+    for (int b = 0; b < P.n_bcast; ++b)
+      if ((st = check(aux[g * na + P.bcast_slot[b]])) != GE_OK) return st;
+    for (int b = 0; b < P.n_cbcast; ++b)
+      if ((st = check(aux[g * na + P.cbcast_slot[b]])) != GE_OK) return st;
+    for (int o = 0; o < no; ++o)
+      if ((st = check(outs[g * no + o])) != GE_OK) return st;
+  }
+  return GE_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int gemm_epi_grouped_plan_create(gemm_epi_plan **plan, int32_t n_problems,
+                                 const ge_problem *problems, const ge_dtypes *dtypes,
+                                 const ge_dag *dag, const ge_options *opts) {
+  if (!plan) return GE_ERR_INVALID;
+  *plan = nullptr;
+  int st = validate_impl(dtypes, dag);
+  if (st != GE_OK) return st;
+  if (!problems) return GE_ERR_INVALID;
+  if (n_problems < 1 || n_problems > GE_MAX_GROUPS) return GE_ERR_SHAPE;
+  for (int g = 0; g < n_problems; ++g) {
+    const ge_problem &pr = problems[g];
+    if (pr.M <= 0 || pr.N <= 0 || pr.K <= 0) return GE_ERR_SHAPE;
+    if (pr.M > (int64_t(1) << 31) - 1 || pr.N > (int64_t(1) << 31) - 1 ||
+        pr.K > (int64_t(1) << 31) - 1)
+      return GE_ERR_SHAPE;
+    if ((pr.K * esize(dtypes->ab)) % 16 != 0 || (pr.N * esize(dtypes->ab)) % 16 != 0)
+      return GE_ERR_MISALIGNED;
+    for (int o = 0; o < dtypes->n_out; ++o)
+      if ((pr.N * esize(dtypes->out[o])) % 16 != 0) return GE_ERR_MISALIGNED;
+    for (int s = 0; s < dtypes->n_aux; ++s)
+      if ((pr.N * esize(dtypes->aux[s])) % 16 != 0) return GE_ERR_MISALIGNED;
+  }
+  gemm_epi_plan *pl = new (std::nothrow) gemm_epi_plan();
+  if (!pl) return GE_ERR_INVALID;
+  pl->n_groups = n_problems;
+  pl->problems.assign(problems, problems + n_problems);
+  pl->L = 1;
+  pl->dt = *dtypes;
+  pl->dag = *dag;
+  if (opts) pl->opt = *opts;
+  {
+    const CompileResult cr = compile_program(*dtypes, *dag);
+    st = cr.status;
+    pl->prog = cr.prog;
+  }
+  if (st == GE_OK) {
+    const bool interp = (pl->opt.debug_flags & GE_DEBUG_FORCE_INTERPRETER) != 0u;
+    pl->epi = interp ? -1 : match_catalog(pl->prog);
+    st = check_device(&pl->device, &pl->num_sms, &pl->max_smem);
+  }
+  if (st == GE_OK) {
+    void *sym = nullptr;
+    if (cudaGetSymbolAddress(&sym, g_ge_status) != cudaSuccess) st = GE_ERR_CUDA;
+    pl->status = static_cast<uint32_t *>(sym);
+  }
+  if (st == GE_OK) st = configure_grouped(pl);
+  if (st == GE_OK && !encode_fn()) st = GE_ERR_CUDA;
+  if (st == GE_OK) {
+    const size_t bytes = sizeof(GroupDesc) * size_t(kGroupSlots) * size_t(n_problems);
+    if (cudaMalloc(&pl->d_desc, bytes) != cudaSuccess ||
+        cudaMallocHost(&pl->h_desc, bytes) != cudaSuccess)
+      st = GE_ERR_CUDA;
+    for (int s = 0; st == GE_OK && s < kGroupSlots; ++s)
+      if (cudaEventCreateWithFlags(&pl->ev[s], cudaEventDisableTiming) != cudaSuccess)
+        st = GE_ERR_CUDA;
+  }
+  if (st != GE_OK) {
+    cudaGetLastError();
+    delete pl;
+    return st;
+  }
+  fill_group_shapes(pl);
+  {
+    const std::vector<int4> tiles = grouped_tile_table(pl);
+    const size_t bytes = sizeof(int4) * tiles.size();
+    if (cudaMalloc(&pl->d_tiles, bytes) != cudaSuccess ||
+        cudaMemcpy(pl->d_tiles, tiles.data(), bytes, cudaMemcpyHostToDevice) != cudaSuccess) {
+      cudaGetLastError();
+      delete pl;
+      return GE_ERR_CUDA;
+    }
+  }
+  fill_params(pl, pl->lay, pl->prog, &pl->kp);
+  pl->kp.num_tiles = pl->lay.num_tiles;
+  pl->kp.num_groups = n_problems;
+  pl->kp.tile_info = pl->d_tiles;
+  if (log_enabled()) log_plan(pl);
+  *plan = pl;
+  return GE_OK;
+}
+
+int gemm_epi_grouped_run(gemm_epi_plan *pl, const void *const *A, const void *const *B,
+                         const void *const *aux, const float *scalars, void *const *outs,
+                         void *stream) {
+  if (!pl || !pl->n_groups) return GE_ERR_INVALID;
+  int st = check_grouped_args(pl, A, B, aux, scalars, outs);
+  if (st != GE_OK) return st;
+  const int n = pl->n_groups, na = pl->dt.n_aux, no = pl->dt.n_out;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  // the pointers this run's table must hold
+  std::vector<const void *> ptrs;
+  ptrs.reserve(size_t(n) * (2 + na + no));
+  for (int g = 0; g < n; ++g) {
+    ptrs.push_back(A[g]);
+    ptrs.push_back(B[g]);
+    for (int a = 0; a < na; ++a) ptrs.push_back(aux ? aux[g * na + a] : nullptr);
+    for (int o = 0; o < no; ++o) ptrs.push_back(outs[g * no + o]);
+  }
+  if (pl->slot < 0 || pl->slot_ptrs[pl->slot] != ptrs) {
+    const int next = (pl->slot + 1) % kGroupSlots;
+    // the staging and device table of `next` are free once the run that used
+    // them last has finished
+    if (pl->ev_used[next] && cudaEventSynchronize(pl->ev[next]) != cudaSuccess) return GE_ERR_CUDA;
+    pl->slot_ptrs[next].clear();
+    if (!build_group_table(pl, next, A, B, aux, outs)) return GE_ERR_CUDA;
+    const size_t bytes = sizeof(GroupDesc) * size_t(n);
+    if (cudaMemcpyAsync(pl->d_desc + size_t(next) * n, pl->h_desc + size_t(next) * n, bytes,
+                        cudaMemcpyHostToDevice, s) != cudaSuccess)
+      return GE_ERR_CUDA;
+    pl->slot = next;
+    pl->slot_ptrs[next] = std::move(ptrs);
+  } else if (pl->ev_used[pl->slot] && pl->ev_stream[pl->slot] != s) {
+    // a table reused from another stream: order this run after the last run
+    // that read it (which follows the table's copy), so every earlier reader
+    // of the table is finished when its event next completes
+    if (cudaStreamWaitEvent(s, pl->ev[pl->slot], 0) != cudaSuccess) return GE_ERR_CUDA;
+  }
+  KParams &kp = pl->kp;
+  kp.groups = pl->d_desc + size_t(pl->slot) * n;
+  for (int i = 0; i < pl->dt.n_scalar; ++i) kp.prog.scalars[i] = scalars[i];
+  if (launch_gemm(pl->lay, pl->epi, kp, s) != cudaSuccess) return GE_ERR_CUDA;
+  if (cudaEventRecord(pl->ev[pl->slot], s) != cudaSuccess) return GE_ERR_CUDA;
+  pl->ev_used[pl->slot] = true;
+  pl->ev_stream[pl->slot] = s;
+  return GE_OK;
 }
 
 const char *gemm_epi_status_string(int status) {
@@ -735,7 +1100,7 @@ void *g_noalloc_ptr[kMaxDevices] = {};
 extern "C" int gemm_epi_run_unfused_noalloc(gemm_epi_plan *pl, const void *A, const void *B,
                                             const void *const *aux, const float *scalars,
                                             void *const *outs, void *stream) {
-  if (!pl) return GE_ERR_INVALID;
+  if (!pl || pl->n_groups) return GE_ERR_INVALID;
   if (gemm_epi_unfused_workspace_bytes(pl) > GE_NOALLOC_SCRATCH_BYTES) return GE_ERR_WORKSPACE;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {

@@ -102,6 +102,15 @@ __device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t par
 }
 
 // --------------------------------------------------------------------- TMA --
+// Order this thread's later uses of a tensor map in global memory after the
+// writes that produced it (the table a grouped launch reads is copied in just
+// before the launch).
+__device__ __forceinline__ void fence_tensormap_acquire(const CUtensorMap *m) {
+  asm volatile("fence.proxy.tensormap::generic.acquire.gpu [%0], 128;" ::"l"(
+                   reinterpret_cast<uint64_t>(m))
+               : "memory");
+}
+
 __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap *m) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(m)) : "memory");
 }

@@ -494,3 +494,114 @@ def to_codes(t: torch.Tensor) -> np.ndarray:
     if t.dtype == torch.float32:
         return t.numpy()
     raise TypeError(t.dtype)
+
+
+# ---------------------------------------------------------- grouped GEMM ---
+
+@dataclass
+class GroupedWorkload:
+    """Independent problems of different sizes sharing one epilogue, its types
+    and its scalars.  Per problem: A (M,K), B (K,N), Load tensors and
+    outputs (M,N), row vectors (N,), column vectors (M,)."""
+    name: str
+    problems: List[Tuple[int, int, int]]      # (M, N, K)
+    ab: str
+    aux: List[tuple]                          # as Workload.aux
+    scalars: List[Tuple[str, float]]
+    outs: List[Tuple[str, str]]
+    dag: List[Tuple[str, int, int, int]]
+    dist: str                                 # "randint3" or "randint" or "normal"
+    seed: int
+    exact: bool
+    cite: str = ""
+
+    def flops(self) -> float:
+        return float(sum(2 * m * n * k for m, n, k in self.problems))
+
+    def alg_bytes(self) -> int:
+        b = 0
+        for m, n, k in self.problems:
+            b += (m * k + k * n) * ESIZE[self.ab]
+            for spec in self.aux:
+                b += {"tensor": m * n, "row": n, "col": m}[spec[1]] * ESIZE[spec[2]]
+            for _, dt in self.outs:
+                b += m * n * ESIZE[dt]
+        return b
+
+    def problem(self, g: int) -> Workload:
+        """Problem g as a one-batch Workload (same epilogue and types)."""
+        m, n, k = self.problems[g]
+        return Workload(name="%s[%d]" % (self.name, g), L=1, M=m, N=n, K=k, ab=self.ab,
+                        aux=self.aux, scalars=self.scalars, outs=self.outs, dag=self.dag,
+                        dist=self.dist, seed=self.seed, exact=self.exact, cite=self.cite)
+
+
+def generate_problem_sizes(count, seed=2023, sizes=(128, 256, 512, 1024)):
+    """M, N, K of each problem drawn in that order from ``sizes`` with Python's
+    ``random`` seeded once (the grouped-GEMM notebook's generate_problems)."""
+    import random
+    rng = random.Random(seed)
+    return [tuple(rng.choice(sizes) for _ in range(3)) for _ in range(count)]
+
+
+def grouped_workloads():
+    """The grouped-GEMM notebook's batch (50 problems, fp16, values from
+    {-3,...,2}, D = A @ B written as alpha*accum + beta*C with alpha 1 and
+    beta 0, the interface's defaults) and a custom epilogue over ragged
+    problems ("Combine custom epilogues with grouped operations")."""
+    g = Dag()
+    t = g.add(g.mul(g.accum(), g.scalar(0)), g.mul(g.load(0), g.scalar(1)))
+    g.store(t, 0)
+    linear = g.nodes
+    g = Dag()
+    t = g.add(g.add(g.mul(g.accum(), g.scalar(0)), g.load(0)), g.broadcast(1))
+    g.store(g.relu(t), 0)
+    g.store(t, 1)
+    bias_relu = g.nodes
+    ragged = [(72, 136, 200), (264, 520, 64), (200, 8, 1000), (1, 256, 128), (520, 392, 136),
+              (129, 264, 72), (384, 1032, 520), (8, 8, 8), (300, 24, 64), (1024, 128, 1024),
+              (513, 392, 8), (136, 136, 136)]
+    return [
+        GroupedWorkload(name="grouped_gemm_50", problems=generate_problem_sizes(50), ab="f16",
+                        aux=[("C", "tensor", "f16")], scalars=[("alpha", 1.0), ("beta", 0.0)],
+                        outs=[("D", "f16")], dag=linear, dist="randint3", seed=2023, exact=True,
+                        cite="Python interface walkthrough, example three: Grouped GEMM"),
+        GroupedWorkload(name="grouped_bias_relu_ragged", problems=ragged, ab="bf16",
+                        aux=[("C", "tensor", "bf16"), ("bias", "row", "f32")],
+                        scalars=[("alpha", 0.5)], outs=[("D", "bf16"), ("T", "f32")],
+                        dag=bias_relu, dist="randint", seed=2030, exact=True,
+                        cite="Custom Epilogue Example, Next Steps: grouped operations"),
+    ]
+
+
+GROUPED_BY_NAME = {w.name: w for w in grouped_workloads()}
+
+
+def make_grouped_inputs(w: GroupedWorkload):
+    """Seeded host tensors ``(As, Bs, auxs, scalars)``: per problem, in problem
+    order, A, B, then its aux slots, all from one torch CPU generator.
+
+    * ``randint3``: integers from {-3,...,2} (torch.randint(-3, 3, ...) as in
+      the grouped-GEMM notebook's initialize);
+    * ``randint``: integers from {-2,...,2};
+    * ``normal``: N(0, 1) rounded to the type.
+    """
+    g = torch.Generator().manual_seed(w.seed)
+
+    def draw(shp, dt):
+        if w.dist == "randint3":
+            return torch.randint(-3, 3, shp, generator=g, dtype=torch.float32).to(TORCH_DTYPE[dt])
+        if w.dist == "randint":
+            return torch.randint(-2, 3, shp, generator=g, dtype=torch.float32).to(TORCH_DTYPE[dt])
+        if w.dist == "normal":
+            return _normal(g, shp, dt)
+        raise ValueError(w.dist)
+
+    As, Bs, auxs = [], [], []
+    for m, n, k in w.problems:
+        As.append(draw((m, k), w.ab).contiguous())
+        Bs.append(draw((k, n), w.ab).contiguous())
+        auxs.append([draw({"tensor": (m, n), "row": (n,), "col": (m,)}[spec[1]], spec[2])
+                     .contiguous() for spec in w.aux])
+    scalars = [float(v) for _, v in w.scalars]
+    return As, Bs, auxs, scalars

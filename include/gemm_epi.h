@@ -195,8 +195,10 @@ int gemm_epi_validate(const ge_dtypes *dtypes, const ge_dag *dag);
  *   aux       n_aux device pointers; entries for slots the DAG never reads may be NULL
  *   scalars   n_scalar host floats (read during the call; may be NULL if n_scalar == 0)
  *   outs      n_out device pointers, each (L,M,N) of its output type
- * Errors: GE_ERR_INVALID, _MISSING_ARG, _MISALIGNED, _CUDA (launch failed).
- * A device-side timeout is reported later by gemm_epi_last_error.
+ * Errors: GE_ERR_INVALID (also for a grouped plan), _MISSING_ARG,
+ * _MISALIGNED, _CUDA (launch failed).  A device-side timeout is reported
+ * later by gemm_epi_last_error.  The unfused entry points below reject
+ * grouped plans the same way.
  */
 int gemm_epi_run(gemm_epi_plan *plan, const void *A, const void *B, const void *const *aux,
                  const float *scalars, void *const *outs, void *stream);
@@ -251,7 +253,58 @@ int gemm_epi_run_unfused_noalloc(gemm_epi_plan *plan, const void *A, const void 
                                  const void *const *aux, const float *scalars, void *const *outs,
                                  void *stream);
 
-/* Free a plan (NULL is ignored).  Does not synchronise. */
+/*
+ * Grouped GEMM with a fused epilogue ("Grouped GEMM" in example three of the
+ * CUTLASS Python interface walkthrough; "Combine custom epilogues with
+ * grouped operations" under Next Steps of "Custom Epilogue Example"):
+ * n_problems independent problems of different sizes,
+ *   outs_g = epilogue(A_g @ B_g, aux_g, scalars),  g = 0 .. n_problems-1,
+ * with one DAG, one set of types and one set of scalars for all of them,
+ * computed by a single persistent launch over the tiles of every problem.
+ * Each problem is laid out like one batch of gemm_epi_run: A_g (M,K), B_g
+ * (K,N), Load tensors and outputs (M,N), row vectors (N,), column vectors
+ * (M,), row-major and packed; the same 16-byte rules apply per problem.
+ */
+typedef struct {
+  int64_t M, N, K; /* all > 0 */
+} ge_problem;
+
+#define GE_MAX_GROUPS 4096 /* problems in one grouped plan */
+
+/*
+ * Build a grouped plan.  Validation as gemm_epi_plan_create_ex, per problem;
+ * opts may be NULL (cluster_n 2 is not available for grouped plans:
+ * GE_ERR_UNSUPPORTED).  The plan allocates its tables: four problem tables
+ * in device memory and their pinned host staging (1.5 KiB per problem each)
+ * and the launch's tile order (16 bytes per output tile), which it uploads
+ * once with a synchronous copy (GE_ERR_CUDA if any of that fails).  Errors:
+ * those of gemm_epi_plan_create_ex, and GE_ERR_SHAPE when n_problems is
+ * outside 1..GE_MAX_GROUPS or the problems have more than 2^24 output tiles.
+ */
+int gemm_epi_grouped_plan_create(gemm_epi_plan **plan, int32_t n_problems,
+                                 const ge_problem *problems, const ge_dtypes *dtypes,
+                                 const ge_dag *dag, const ge_options *opts);
+
+/*
+ * Run a grouped plan on `stream`.  Host arrays of device pointers:
+ *   A, B     n_problems entries each
+ *   aux      n_problems * n_aux entries, problem-major: aux[g*n_aux + slot]
+ *            (NULL allowed when the DAG reads no aux slot)
+ *   outs     n_problems * n_out entries: outs[g*n_out + slot]
+ *   scalars  host fp32, n_scalar values shared by every problem
+ * The problem table (tensor maps and vector pointers) is built on the host
+ * and copied to the device with the launch.  When every pointer equals the
+ * previous run's, that table is reused and nothing is copied; otherwise the
+ * next of four tables is rebuilt, which first waits (on the host) for the
+ * run that last used that table to finish.  Errors: GE_ERR_INVALID (NULL or
+ * not a grouped plan), GE_ERR_MISSING_ARG, GE_ERR_MISALIGNED, GE_ERR_CUDA.
+ */
+int gemm_epi_grouped_run(gemm_epi_plan *plan, const void *const *A, const void *const *B,
+                         const void *const *aux, const float *scalars, void *const *outs,
+                         void *stream);
+
+/* Free a plan (NULL is ignored).  Does not synchronise, except that a
+ * grouped plan first waits for the runs still reading its tables. */
 void gemm_epi_plan_destroy(gemm_epi_plan *plan);
 
 /* Fill `info` with the plan's choices.  Errors: GE_ERR_INVALID. */

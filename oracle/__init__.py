@@ -161,6 +161,21 @@ def gemm_epilogue(L, M, N, K, ab_dtype, A, B, aux, aux_dtypes, scalars, dag, out
     return outs, (pres if want_pre else None)
 
 
+def grouped_gemm_epilogue(problems, ab_dtype, As, Bs, auxs, aux_dtypes, scalars, dag, out_dtypes,
+                          threads=0, lib_handle=None):
+    """A grouped GEMM by its definition: every problem ``g`` (sizes
+    ``problems[g] = (M, N, K)``) is an independent one-batch GEMM with the
+    shared epilogue DAG and scalars ("Grouped GEMM", example three of the
+    Python interface walkthrough).  ``auxs[g]`` lists problem g's aux
+    operands.  Returns one ``outs`` list (as gemm_epilogue) per problem."""
+    result = []
+    for (M, N, K), A, B, aux in zip(problems, As, Bs, auxs):
+        outs, _ = gemm_epilogue(1, M, N, K, ab_dtype, A, B, aux, aux_dtypes, scalars, dag,
+                                out_dtypes, threads=threads, lib_handle=lib_handle)
+        result.append(outs)
+    return result
+
+
 def gemm_accum(L, M, N, K, ab_dtype, A, B, rows=None, threads=0, lib_handle=None):
     """fp64 accumulator rows ``accum[l,i,:]`` (no epilogue)."""
     h = lib_handle or lib()

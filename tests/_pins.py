@@ -415,6 +415,47 @@ def pin_activation_identities(L_):
                           [-1.0, -0.375, -0.03125, 0.0, 0.125, 1.5, 4.0])
 
 
+def pin_grouped_closed_form(L_):
+    """A grouped GEMM is its problems computed independently: integer inputs,
+    each problem's D equals its own exact alpha*A_g@B_g + beta*C_g (numpy
+    float64 matmul of small integers, exact), the row bias and ReLU of the
+    ragged workload likewise, and reversing the problem order reverses the
+    outputs."""
+    import dataclasses
+    w = dataclasses.replace(W.GROUPED_BY_NAME["grouped_gemm_50"],
+                            problems=[(8, 16, 24), (24, 8, 40), (16, 32, 8)],
+                            scalars=[("alpha", 1.0), ("beta", 2.0)])
+    As, Bs, auxs, sc = W.make_grouped_inputs(w)
+    assert set(np.unique(As[0].double().numpy())) <= set(range(-3, 3))
+
+    def run(ws, As_, Bs_, auxs_):
+        return oracle.grouped_gemm_epilogue(
+            ws.problems, ws.ab, [W.to_codes(a) for a in As_], [W.to_codes(b) for b in Bs_],
+            [[W.to_codes(x) for x in per] for per in auxs_], [s[2] for s in ws.aux], sc, ws.dag,
+            [dt for _, dt in ws.outs], lib_handle=L_)
+
+    res = run(w, As, Bs, auxs)
+    for g in range(len(w.problems)):
+        ref = As[g].double().numpy() @ Bs[g].double().numpy() + 2 * auxs[g][0].double().numpy()
+        assert np.array_equal(np_decode(res[g][0], "f16"), ref), g
+    wr = dataclasses.replace(w, problems=w.problems[::-1])
+    rev = run(wr, As[::-1], Bs[::-1], auxs[::-1])
+    for g in range(len(w.problems)):
+        assert np.array_equal(rev[g][0], res[-1 - g][0])
+    w = dataclasses.replace(W.GROUPED_BY_NAME["grouped_bias_relu_ragged"],
+                            problems=[(5, 8, 9), (3, 16, 2), (9, 8, 17)])
+    As, Bs, auxs, sc = W.make_grouped_inputs(w)
+    res = oracle.grouped_gemm_epilogue(
+        w.problems, w.ab, [W.to_codes(a) for a in As], [W.to_codes(b) for b in Bs],
+        [[W.to_codes(x) for x in per] for per in auxs], [s[2] for s in w.aux], sc, w.dag,
+        [dt for _, dt in w.outs], lib_handle=L_)
+    for g in range(len(w.problems)):
+        t = (0.5 * (As[g].double().numpy() @ Bs[g].double().numpy()) +
+             auxs[g][0].double().numpy() + auxs[g][1].double().numpy()[None, :])
+        assert np.array_equal(np_decode(res[g][0], "bf16"), np.maximum(t, 0.0)), g
+        assert np.array_equal(res[g][1].astype(np.float64), t), g
+
+
 def pin_broadcast_closed_form(L_):
     """Row-broadcast bias indexed by column j, same vector for every row and
     batch: integer inputs, D = relu(0.5*A@B + C + bias), E = D*D rounded."""
@@ -534,6 +575,7 @@ def pin_rows_and_threads(L_):
 ALL_PINS = [pin_decode_exhaustive, pin_encode_roundtrip, pin_encode_midpoints,
             pin_encode_random_vs_table, pin_golden, pin_integer_closed_form,
             pin_broadcast_closed_form, pin_new_ops_closed_form, pin_activation_identities,
+            pin_grouped_closed_form,
             pin_fraction_brute_force,
             pin_special_cases,
             pin_relu_positive_zero, pin_rows_and_threads]

@@ -186,3 +186,42 @@ def test_plan_create_without_gpu_reports_arch():
     with pytest.raises(B.GemmEpiError) as e:
         B.gemm_epi_plan_create(1, 128, 128, 128, dt, B.make_dag(dag))
     assert e.value.status == B.GE_ERR_ARCH
+
+
+def _grouped_base():
+    w = W.GROUPED_BY_NAME["grouped_gemm_50"]
+    return B.make_dtypes(w.ab, [s[2] for s in w.aux], len(w.scalars),
+                         [dt for _, dt in w.outs]), B.make_dag(w.dag)
+
+
+def test_grouped_plan_create_checks_before_device():
+    dt, dag = _grouped_base()
+    cases = [([], B.GE_ERR_SHAPE),                                   # no problems
+             ([(128, 128, 128)] * (B.GE_MAX_GROUPS + 1), B.GE_ERR_SHAPE),
+             ([(128, 128, 128), (0, 128, 128)], B.GE_ERR_SHAPE),     # M = 0
+             ([(128, 128, 128), (128, 128, -8)], B.GE_ERR_SHAPE),    # K < 0
+             ([(128, 128, 128), (128, 128, 100)], B.GE_ERR_MISALIGNED),  # K*2 bytes
+             ([(64, 12, 64)], B.GE_ERR_MISALIGNED)]                  # N*2 bytes
+    for problems, want in cases:
+        with pytest.raises(B.GemmEpiError) as e:
+            B.gemm_epi_grouped_plan_create(problems, dt, dag)
+        assert e.value.status == want, (problems[:2], e.value.status)
+    bad = [("accum", 0, 0, 0), ("relu", 0, 0, 0)]  # D never stored
+    with pytest.raises(B.GemmEpiError) as e:
+        B.gemm_epi_grouped_plan_create([(128, 128, 128)], dt, B.make_dag(bad))
+    assert e.value.status == B.GE_ERR_NO_D
+
+
+def test_grouped_plan_create_without_gpu_reports_arch():
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a CUDA device is present")
+    dt, dag = _grouped_base()
+    with pytest.raises(B.GemmEpiError) as e:
+        B.gemm_epi_grouped_plan_create([(128, 256, 64), (256, 128, 128)], dt, dag)
+    assert e.value.status == B.GE_ERR_ARCH
+
+
+def test_grouped_run_rejects_null_plan():
+    assert B.lib.gemm_epi_grouped_run(None, None, None, None, None, None, None) == \
+        B.GE_ERR_INVALID
