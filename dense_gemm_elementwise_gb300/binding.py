@@ -18,6 +18,7 @@ GE_F16, GE_BF16, GE_F32 = 0, 1, 2
 GE_MAX_NODES, GE_MAX_AUX, GE_MAX_TMA_AUX, GE_MAX_OUT, GE_MAX_SCALARS = 16, 8, 4, 4, 16
 GE_DEBUG_SKIP_FIRST_LOAD = 1
 GE_DEBUG_FORCE_INTERPRETER = 2
+GE_ROW_MAJOR, GE_COL_MAJOR = 0, 1
 
 STATUS = ["GE_OK", "GE_ERR_NO_ACCUM", "GE_ERR_NO_D", "GE_ERR_SSA", "GE_ERR_MISSING_ARG",
           "GE_ERR_UNSUPPORTED", "GE_ERR_MISALIGNED", "GE_ERR_ARCH", "GE_ERR_SHAPE",
@@ -60,7 +61,9 @@ class ge_options(ctypes.Structure):
     _fields_ = [("cta_group", ctypes.c_int32), ("tile_n", ctypes.c_int32),
                 ("stages", ctypes.c_int32), ("max_ctas", ctypes.c_int32),
                 ("raster_group", ctypes.c_int32), ("timeout_ms", ctypes.c_int32),
-                ("debug_flags", ctypes.c_uint32), ("cluster_n", ctypes.c_int32)]
+                ("debug_flags", ctypes.c_uint32), ("cluster_n", ctypes.c_int32),
+                ("a_major", ctypes.c_int32), ("b_major", ctypes.c_int32),
+                ("cd_major", ctypes.c_int32)]
 
 
 class ge_problem(ctypes.Structure):

@@ -129,6 +129,9 @@ struct KParams {
   uint32_t b_lbo, b_sbo;  // B smem descriptor strides (bytes)
   uint64_t timeout_ns;
   uint32_t debug_flags;
+  int32_t a_mn;             // A stored M-major ((L,K,M), M contiguous), else K-major
+  int32_t b_k;              // B stored K-major ((L,N,K), K contiguous), else N-major
+  int32_t cd_m;             // epilogue tensors and outputs M-major ((L,N,M)), else N-major
   const GroupDesc *groups;  // grouped GEMM: the problem table (else nullptr)
   const int4 *tile_info;    // grouped GEMM: per tile {problem entry, m block, n block, k blocks}
   int32_t num_groups;
@@ -146,6 +149,7 @@ struct EwParams {
   int32_t M;
   int32_t N;
   int32_t chunks_per_row;             // ceil(N / 8): one thread per 8 columns
+  int32_t cd_m;                       // aux tensors and outputs M-major ((L,N,M))
 };
 
 // Where a device-side wait gave up (second word of the status block).

@@ -123,6 +123,42 @@ __device__ __forceinline__ void box_store(uint8_t *box, int row, int half, const
   }
 }
 
+// Epilogue tensors stored M-major (each batch column-major): the staged box
+// is 32 columns of 32 rows, a column's 32 rows contiguous ([n][m], no
+// swizzle).  Lane = row touches one element per column, so every warp access
+// covers one contiguous 64- or 128-byte column without bank conflicts.
+__device__ __forceinline__ float widen16(uint16_t u, bool bf16) {
+  return bf16 ? __uint_as_float(static_cast<uint32_t>(u) << 16)
+              : __half2float(__ushort_as_half(static_cast<unsigned short>(u)));
+}
+
+template <int DT>
+__device__ __forceinline__ void col_box_load(const uint8_t *box, int row, int half, float (&t)[16]) {
+#pragma unroll
+  for (int e = 0; e < 16; ++e) {
+    const int n = 16 * half + e;
+    if constexpr (DT == GE_F32)
+      t[e] = reinterpret_cast<const float *>(box)[n * 32 + row];
+    else
+      t[e] = widen16(reinterpret_cast<const uint16_t *>(box)[n * 32 + row], DT == GE_BF16);
+  }
+}
+
+template <int DT>
+__device__ __forceinline__ void col_box_store(uint8_t *box, int row, int half, const float (&t)[16]) {
+#pragma unroll
+  for (int e = 0; e < 16; ++e) {
+    const int n = 16 * half + e;
+    if constexpr (DT == GE_F32) {
+      reinterpret_cast<float *>(box)[n * 32 + row] = t[e];
+    } else if constexpr (DT == GE_BF16) {
+      reinterpret_cast<__nv_bfloat16 *>(box)[n * 32 + row] = __float2bfloat16_rn(t[e]);
+    } else {
+      reinterpret_cast<__half *>(box)[n * 32 + row] = __float2half_rn(t[e]);
+    }
+  }
+}
+
 // ------------------------------------------------------- global row access --
 // C (8 or 16) elements of a row starting at column col0 (a multiple of 8).
 // Rows are multiples of 16 bytes and N is a multiple of 8, so each group of 8

@@ -188,10 +188,12 @@ struct FusedMem {
   const uint8_t *aux_stage;
   uint8_t *out_stage;
   int row, half, col0;
-  int grow;  // this lane's row within its batch (column-broadcast index)
+  int grow;     // this lane's row within its batch (column-broadcast index)
+  bool cd_m;    // staging boxes hold M-major tensors
   template <int DT>
   __device__ __forceinline__ void aux(uint32_t i, float (&t)[CH]) const {
-    box_load<DT>(aux_stage + p->aux_off[i], row, half, t);
+    if (cd_m) col_box_load<DT>(aux_stage + p->aux_off[i], row, half, t);
+    else box_load<DT>(aux_stage + p->aux_off[i], row, half, t);
   }
   template <int DT>
   __device__ __forceinline__ void bcast(uint32_t i, float (&t)[CH]) const {
@@ -205,7 +207,8 @@ struct FusedMem {
   }
   template <int DT>
   __device__ __forceinline__ void store(uint32_t o, const float (&t)[CH]) const {
-    box_store<DT>(out_stage + p->out_off[o], row, half, t);
+    if (cd_m) col_box_store<DT>(out_stage + p->out_off[o], row, half, t);
+    else box_store<DT>(out_stage + p->out_off[o], row, half, t);
   }
 };
 
@@ -301,7 +304,12 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_epi_kernel(const __grid_cons
               const uint32_t fb = mapa_shared(fb_local, leader);
               if (rank == 0) mbar_arrive_expect_tx(fb_local, p.tx_bytes);
               if constexpr (MC == 1) {
-                tma_load_3d_pair(sa, mA, fb, kb * BK, m0, l);
+                if (p.a_mn) {  // two 64-row atoms of the M-major A tile
+                  tma_load_3d_pair(sa, mA, fb, m0, kb * BK, l);
+                  tma_load_3d_pair(sa + 8192, mA, fb, m0 + 64, kb * BK, l);
+                } else {
+                  tma_load_3d_pair(sa, mA, fb, kb * BK, m0, l);
+                }
               } else {
                 // this pair fetches its share of the A rows and multicasts it to
                 // the CTA with the same rank in every pair of the cluster
@@ -311,15 +319,28 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_epi_kernel(const __grid_cons
                 tma_load_3d_pair_mc(sa + pair * T::kALoadRows * 128, mA, fb, kb * BK,
                                     m0 + pair * T::kALoadRows, l, mask);
               }
+              if (p.b_k) {
+                tma_load_3d_pair(sbb, mB, fb, kb * BK, n0, l);
+              } else {
 #pragma unroll
-              for (int j = 0; j < T::kBAtoms; ++j)
-                tma_load_3d_pair(sbb + j * 8192, mB, fb, n0 + 64 * j, kb * BK, l);
+                for (int j = 0; j < T::kBAtoms; ++j)
+                  tma_load_3d_pair(sbb + j * 8192, mB, fb, n0 + 64 * j, kb * BK, l);
+              }
             } else {
               mbar_arrive_expect_tx(fb_local, p.tx_bytes);
-              tma_load_3d(sa, mA, fb_local, kb * BK, m0, l);
+              if (p.a_mn) {
+                tma_load_3d(sa, mA, fb_local, m0, kb * BK, l);
+                tma_load_3d(sa + 8192, mA, fb_local, m0 + 64, kb * BK, l);
+              } else {
+                tma_load_3d(sa, mA, fb_local, kb * BK, m0, l);
+              }
+              if (p.b_k) {
+                tma_load_3d(sbb, mB, fb_local, kb * BK, n0, l);
+              } else {
 #pragma unroll
-              for (int j = 0; j < T::kBAtoms; ++j)
-                tma_load_3d(sbb + j * 8192, mB, fb_local, n0 + 64 * j, kb * BK, l);
+                for (int j = 0; j < T::kBAtoms; ++j)
+                  tma_load_3d(sbb + j * 8192, mB, fb_local, n0 + 64 * j, kb * BK, l);
+              }
             }
           }
           ++fills;
@@ -361,7 +382,14 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_epi_kernel(const __grid_cons
   } else if (warp == 1) {
     // ------------------------------------------------------- MMA issuer --
     if (lane == 0 && rank == 0) {
-      const uint32_t id = make_idesc_f16(p.ab_bf16 != 0, T::kMmaM, BN);
+      const uint32_t id = make_idesc_f16(p.ab_bf16 != 0, T::kMmaM, BN, p.a_mn != 0, p.b_k == 0);
+      // per-k step advance and strides of the two operands' smem descriptors:
+      // K-major tiles are 128-byte rows (k step 32 bytes, 8-row groups 1 KiB
+      // apart), MN-major tiles are 64-element atoms 8 KiB apart whose k rows
+      // are 128 bytes (k step 16 rows = 2 KiB)
+      const uint32_t a_step = p.a_mn ? 2048u : 32u, a_lbo = p.a_mn ? 8192u : 16u;
+      const uint32_t b_step = p.b_k ? 32u : 2048u, b_lbo = p.b_k ? 16u : p.b_lbo;
+      const uint32_t b_sbo = p.b_k ? 1024u : p.b_sbo;
       int stage = 0;
       uint32_t phase = 0;
       int abuf = 0;
@@ -386,8 +414,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_epi_kernel(const __grid_cons
           const uint32_t sbb = sb + p.off_B + stage * T::kBBytes;
 #pragma unroll
           for (int k = 0; k < BK / UMMA_K; ++k) {
-            const uint64_t ad = smem_desc_sw128(sa + 32u * k, 16u, 1024u);
-            const uint64_t bd = smem_desc_sw128(sbb + 2048u * k, p.b_lbo, p.b_sbo);
+            const uint64_t ad = smem_desc_sw128(sa + a_step * k, a_lbo, 1024u);
+            const uint64_t bd = smem_desc_sw128(sbb + b_step * k, b_lbo, b_sbo);
             umma_f16<CG>(d, ad, bd, id, (kb | k) != 0 ? 1u : 0u);
           }
           umma_commit<CG>(bar + kBarEmpty + 8 * stage, kAllMask);
@@ -458,7 +486,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_epi_kernel(const __grid_cons
       mbar_arrive_expect_tx(ab, p.aux_tx_bytes);
       const int x = pf_x0 + (gi - ii * T::kSteps) * EW;
       for (int a = 0; a < p.prog.n_tma_aux; ++a)
-        tma_load_3d(smem_u32(dst + p.aux_off[a]), &pf_maps[a], ab, x, pf_y, pf_l);
+        tma_load_3d(smem_u32(dst + p.aux_off[a]), &pf_maps[a], ab, p.cd_m ? pf_y : x,
+                    p.cd_m ? x : pf_y, pf_l);
     };
 
     for (int i = 0; ok && i < my_tiles; ++i) {
@@ -531,14 +560,15 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_epi_kernel(const __grid_cons
         const uint8_t *astage = aux_w + (g % SA) * p.aux_stage_bytes;
         const int c0 = n0 + s * EW;
         Epi::template run<CH>(p.prog, acc0, FusedMem{&p, bptr, cptr, pM, pN, astage, ostage, lane,
-                                                     0, c0, m0 + lane});
+                                                     0, c0, m0 + lane, p.cd_m != 0});
         Epi::template run<CH>(p.prog, acc1, FusedMem{&p, bptr, cptr, pM, pN, astage, ostage, lane,
-                                                     1, c0 + CH, m0 + lane});
+                                                     1, c0 + CH, m0 + lane, p.cd_m != 0});
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) {
           for (int o = 0; o < p.prog.n_out; ++o)
-            tma_store_3d(&out_maps[o], smem_u32(ostage + p.out_off[o]), c0, m0, l);
+            tma_store_3d(&out_maps[o], smem_u32(ostage + p.out_off[o]), p.cd_m ? m0 : c0,
+                         p.cd_m ? c0 : m0, l);
           bulk_commit_group();
         }
         obuf ^= 1;

@@ -252,6 +252,7 @@ struct gemm_epi_plan {
   ge_dtypes dt{};
   ge_dag dag{};
   ge_options opt{};
+  int a_mn = 0, b_k = 0, cd_m = 0;  // operand / epilogue majors (from the options)
   int device = 0, num_sms = 0, max_smem = 0;
   uint32_t *status = nullptr;
   EpiProgram prog{}, prog_acc{};
@@ -449,22 +450,77 @@ void fill_params(const gemm_epi_plan *pl, const Layout &Lo, const EpiProgram &P,
   const int tmo = pl->opt.timeout_ms ? pl->opt.timeout_ms : 1000;
   kp->timeout_ns = static_cast<uint64_t>(tmo) * 1000000ull;
   kp->debug_flags = pl->opt.debug_flags;
+  kp->a_mn = pl->a_mn;
+  kp->b_k = pl->b_k;
+  kp->cd_m = pl->cd_m;
 }
 
 // A box: the rows one CTA fetches per stage (all 128, or its share under multicast)
-bool encode_operands(const gemm_epi_plan *pl, KParams *kp, const void *A, const void *B) {
-  const uint64_t L = pl->L, M = pl->M, N = pl->N, K = pl->K;
+// A and B tensor maps of one (L, M, N, K) problem.  K-major A: (K, M, L), box
+// 64 x the rows one CTA fetches; M-major A: (M, K, L), box 64 x 64 (one of
+// the tile's two 64-row atoms); N-major B: (N, K, L), box 64 x 64 (one 64-column
+// atom); K-major B: (K, N, L), box 64 x the CTA's tile columns.
+bool encode_ab_maps(const gemm_epi_plan *pl, CUtensorMap *tA, CUtensorMap *tB, const void *A,
+                    const void *B, uint64_t L, uint64_t M, uint64_t N, uint64_t K) {
   const int ab = pl->dt.ab;
-  const uint32_t a_rows = static_cast<uint32_t>(BM / pl->lay.mc);
-  return encode3d(&kp->tmA, ab, A, K, M, L, BK, a_rows, CU_TENSOR_MAP_SWIZZLE_128B,
-                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B) &&
-         encode3d(&kp->tmB, ab, B, N, K, L, 64, BK, CU_TENSOR_MAP_SWIZZLE_128B,
-                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
+  const auto sw = CU_TENSOR_MAP_SWIZZLE_128B;
+  const auto l2 = CU_TENSOR_MAP_L2_PROMOTION_L2_256B;
+  const bool okA = pl->a_mn ? encode3d(tA, ab, A, M, K, L, 64, BK, sw, l2)
+                            : encode3d(tA, ab, A, K, M, L, BK,
+                                       static_cast<uint32_t>(BM / pl->lay.mc), sw, l2);
+  const bool okB = pl->b_k ? encode3d(tB, ab, B, K, N, L, BK,
+                                      static_cast<uint32_t>(pl->lay.bn / pl->lay.cg), sw, l2)
+                           : encode3d(tB, ab, B, N, K, L, 64, BK, sw, l2);
+  return okA && okB;
 }
 
-bool encode_epilogue_map(const gemm_epi_plan *pl, CUtensorMap *m, int dt, const void *ptr) {
-  return encode3d(m, dt, ptr, pl->N, pl->M, pl->L, EW, 32, epi_swizzle(dt),
-                  CU_TENSOR_MAP_L2_PROMOTION_L2_128B);
+bool encode_operands(const gemm_epi_plan *pl, KParams *kp, const void *A, const void *B) {
+  return encode_ab_maps(pl, &kp->tmA, &kp->tmB, A, B, pl->L, pl->M, pl->N, pl->K);
+}
+
+// An epilogue tensor's map: N-major (N, M, L) with 32 x 32 swizzled boxes, or
+// M-major (M, N, L) with 32 x 32 plain boxes.  The unfused path's fp32
+// workspace is always N-major (row_major).
+bool encode_epi_map(const gemm_epi_plan *pl, CUtensorMap *m, int dt, const void *ptr, uint64_t L,
+                    uint64_t M, uint64_t N, bool row_major = false) {
+  if (pl->cd_m && !row_major)
+    return encode3d(m, dt, ptr, M, N, L, 32, EW, CU_TENSOR_MAP_SWIZZLE_NONE,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_128B);
+  return encode3d(m, dt, ptr, N, M, L, EW, 32, epi_swizzle(dt), CU_TENSOR_MAP_L2_PROMOTION_L2_128B);
+}
+
+bool encode_epilogue_map(const gemm_epi_plan *pl, CUtensorMap *m, int dt, const void *ptr,
+                         bool row_major = false) {
+  return encode_epi_map(pl, m, dt, ptr, pl->L, pl->M, pl->N, row_major);
+}
+
+// Operand and epilogue majors from the options (all row-major without options).
+int read_majors(gemm_epi_plan *pl, const ge_options *o) {
+  if (!o) return GE_OK;
+  for (int v : {o->a_major, o->b_major, o->cd_major})
+    if (v != GE_ROW_MAJOR && v != GE_COL_MAJOR) return GE_ERR_INVALID;
+  pl->a_mn = o->a_major == GE_COL_MAJOR;
+  pl->b_k = o->b_major == GE_COL_MAJOR;
+  pl->cd_m = o->cd_major == GE_COL_MAJOR;
+  // A multicast splits the A tile by rows of a K-major tile
+  if (o->cluster_n == 2 && pl->a_mn) return GE_ERR_UNSUPPORTED;
+  return GE_OK;
+}
+
+// The contiguous dimension of every tensor must be whole 16-byte units.
+int check_alignment(const gemm_epi_plan *pl, const ge_dtypes *dt, int64_t M, int64_t N, int64_t K) {
+  const int64_t ea = esize(dt->ab);
+  if (((pl->a_mn ? M : K) * ea) % 16 != 0 || ((pl->b_k ? K : N) * ea) % 16 != 0)
+    return GE_ERR_MISALIGNED;
+  for (int o = 0; o < dt->n_out; ++o) {
+    if ((N * esize(dt->out[o])) % 16 != 0) return GE_ERR_MISALIGNED;
+    if (pl->cd_m && (M * esize(dt->out[o])) % 16 != 0) return GE_ERR_MISALIGNED;
+  }
+  for (int s = 0; s < dt->n_aux; ++s) {
+    if ((N * esize(dt->aux[s])) % 16 != 0) return GE_ERR_MISALIGNED;
+    if (pl->cd_m && (M * esize(dt->aux[s])) % 16 != 0) return GE_ERR_MISALIGNED;
+  }
+  return GE_OK;
 }
 
 int check_device(int *dev, int *sms, int *max_smem) {
@@ -546,15 +602,14 @@ int gemm_epi_plan_create_ex(gemm_epi_plan **plan, int64_t L, int64_t M, int64_t 
   if (M > (int64_t(1) << 31) - 1 || N > (int64_t(1) << 31) - 1 || K > (int64_t(1) << 31) - 1 ||
       L > (int64_t(1) << 31) - 1)
     return GE_ERR_SHAPE;
-  // rows of every 2-D / 3-D operand must be whole 16-byte units
-  if ((K * esize(dtypes->ab)) % 16 != 0 || (N * esize(dtypes->ab)) % 16 != 0) return GE_ERR_MISALIGNED;
-  for (int o = 0; o < dtypes->n_out; ++o)
-    if ((N * esize(dtypes->out[o])) % 16 != 0) return GE_ERR_MISALIGNED;
-  for (int s = 0; s < dtypes->n_aux; ++s)
-    if ((N * esize(dtypes->aux[s])) % 16 != 0) return GE_ERR_MISALIGNED;
-
   gemm_epi_plan *pl = new (std::nothrow) gemm_epi_plan();
   if (!pl) return GE_ERR_INVALID;
+  st = read_majors(pl, opts);
+  if (st == GE_OK) st = check_alignment(pl, dtypes, M, N, K);
+  if (st != GE_OK) {
+    delete pl;
+    return st;
+  }
   pl->L = L;
   pl->M = M;
   pl->N = N;
@@ -588,6 +643,7 @@ int gemm_epi_plan_create_ex(gemm_epi_plan **plan, int64_t L, int64_t M, int64_t 
   }
   fill_params(pl, pl->lay, pl->prog, &pl->kp);
   fill_params(pl, pl->lay_acc, pl->prog_acc, &pl->kp_acc);
+  pl->kp_acc.cd_m = 0;  // the unfused path's fp32 workspace is N-major
   if (log_enabled()) log_plan(pl);
   *plan = pl;
   return GE_OK;
@@ -671,7 +727,7 @@ int gemm_epi_run_unfused(gemm_epi_plan *pl, const void *A, const void *B, const 
   if (!(pl->acc_maps_ok && pl->aA == A && pl->aB == B && pl->aWs == workspace)) {
     pl->acc_maps_ok = false;
     if (!encode_operands(pl, &ka, A, B)) return GE_ERR_CUDA;
-    if (!encode_epilogue_map(pl, &ka.tmOut[0], GE_F32, workspace)) return GE_ERR_CUDA;
+    if (!encode_epilogue_map(pl, &ka.tmOut[0], GE_F32, workspace, true)) return GE_ERR_CUDA;
     pl->aA = A;
     pl->aB = B;
     pl->aWs = workspace;
@@ -694,6 +750,7 @@ int gemm_epi_run_unfused(gemm_epi_plan *pl, const void *A, const void *B, const 
   ep.rows = pl->L * pl->M;
   ep.N = static_cast<int32_t>(pl->N);
   ep.chunks_per_row = static_cast<int32_t>((pl->N + kEwCols - 1) / kEwCols);
+  ep.cd_m = pl->cd_m;
   const int64_t units = ep.rows * ep.chunks_per_row;
   const int64_t blocks = (units + kEwThreads - 1) / kEwThreads;
   const int grid = static_cast<int>(std::min<int64_t>(blocks, int64_t(pl->num_sms) * 16));
@@ -861,24 +918,19 @@ void fill_group_shapes(gemm_epi_plan *pl) {
 bool build_group_table(gemm_epi_plan *pl, int s, const void *const *A, const void *const *B,
                        const void *const *aux, void *const *outs) {
   const EpiProgram &P = pl->prog;
-  const int n = pl->n_groups, na = pl->dt.n_aux, no = pl->dt.n_out, ab = pl->dt.ab;
+  const int n = pl->n_groups, na = pl->dt.n_aux, no = pl->dt.n_out;
   for (int j = 0; j < n; ++j) {
     const int g = pl->order[j];
     const ge_problem &pr = pl->problems[g];
     GroupDesc &d = pl->h_desc[s * n + j];
     const uint64_t M = pr.M, N = pr.N, K = pr.K;
-    if (!encode3d(&d.tmA, ab, A[g], K, M, 1, BK, BM, CU_TENSOR_MAP_SWIZZLE_128B,
-                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B) ||
-        !encode3d(&d.tmB, ab, B[g], N, K, 1, 64, BK, CU_TENSOR_MAP_SWIZZLE_128B,
-                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B))
-      return false;
+    if (!encode_ab_maps(pl, &d.tmA, &d.tmB, A[g], B[g], 1, M, N, K)) return false;
     for (int t = 0; t < P.n_tma_aux; ++t)
-      if (!encode3d(&d.tmAux[t], P.tma_aux_dtype[t], aux[g * na + P.tma_aux_slot[t]], N, M, 1, EW,
-                    32, epi_swizzle(P.tma_aux_dtype[t]), CU_TENSOR_MAP_L2_PROMOTION_L2_128B))
+      if (!encode_epi_map(pl, &d.tmAux[t], P.tma_aux_dtype[t], aux[g * na + P.tma_aux_slot[t]], 1,
+                          M, N))
         return false;
     for (int o = 0; o < no; ++o)
-      if (!encode3d(&d.tmOut[o], P.out_dtype[o], outs[g * no + o], N, M, 1, EW, 32,
-                    epi_swizzle(P.out_dtype[o]), CU_TENSOR_MAP_L2_PROMOTION_L2_128B))
+      if (!encode_epi_map(pl, &d.tmOut[o], P.out_dtype[o], outs[g * no + o], 1, M, N))
         return false;
     for (int b = 0; b < P.n_bcast; ++b) d.bcast_ptr[b] = aux[g * na + P.bcast_slot[b]];
     for (int b = 0; b < P.n_cbcast; ++b) d.cbcast_ptr[b] = aux[g * na + P.cbcast_slot[b]];
@@ -930,15 +982,16 @@ int gemm_epi_grouped_plan_create(gemm_epi_plan **plan, int32_t n_problems,
     if (pr.M > (int64_t(1) << 31) - 1 || pr.N > (int64_t(1) << 31) - 1 ||
         pr.K > (int64_t(1) << 31) - 1)
       return GE_ERR_SHAPE;
-    if ((pr.K * esize(dtypes->ab)) % 16 != 0 || (pr.N * esize(dtypes->ab)) % 16 != 0)
-      return GE_ERR_MISALIGNED;
-    for (int o = 0; o < dtypes->n_out; ++o)
-      if ((pr.N * esize(dtypes->out[o])) % 16 != 0) return GE_ERR_MISALIGNED;
-    for (int s = 0; s < dtypes->n_aux; ++s)
-      if ((pr.N * esize(dtypes->aux[s])) % 16 != 0) return GE_ERR_MISALIGNED;
   }
   gemm_epi_plan *pl = new (std::nothrow) gemm_epi_plan();
   if (!pl) return GE_ERR_INVALID;
+  st = read_majors(pl, opts);
+  for (int g = 0; st == GE_OK && g < n_problems; ++g)
+    st = check_alignment(pl, dtypes, problems[g].M, problems[g].N, problems[g].K);
+  if (st != GE_OK) {
+    delete pl;
+    return st;
+  }
   pl->n_groups = n_problems;
   pl->problems.assign(problems, problems + n_problems);
   pl->L = 1;

@@ -287,10 +287,12 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo
 }
 
 // Instruction descriptor, kind::f16: D fp32 (bits 4-5 = 1), A/B type (bits 7-9,
-// 10-12: 0 fp16, 1 bf16), A K-major (bit 15 = 0), B MN-major (bit 16 = 1),
-// N >> 3 (bits 17-22), M >> 4 (bits 24-28).
-__host__ __device__ constexpr uint32_t make_idesc_f16(bool bf16, int m, int n) {
-  return (1u << 4) | ((bf16 ? 1u : 0u) << 7) | ((bf16 ? 1u : 0u) << 10) | (0u << 15) | (1u << 16) |
+// 10-12: 0 fp16, 1 bf16), A major (bit 15: 0 K-major, 1 MN-major), B major
+// (bit 16: 0 K-major, 1 MN-major), N >> 3 (bits 17-22), M >> 4 (bits 24-28).
+__host__ __device__ constexpr uint32_t make_idesc_f16(bool bf16, int m, int n, bool a_mn = false,
+                                                      bool b_mn = true) {
+  return (1u << 4) | ((bf16 ? 1u : 0u) << 7) | ((bf16 ? 1u : 0u) << 10) |
+         ((a_mn ? 1u : 0u) << 15) | ((b_mn ? 1u : 0u) << 16) |
          (static_cast<uint32_t>(n >> 3) << 17) | (static_cast<uint32_t>(m >> 4) << 24);
 }
 

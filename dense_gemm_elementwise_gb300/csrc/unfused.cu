@@ -4,6 +4,9 @@
 // (interpreter or catalog executor), and writes the outputs.  One thread
 // handles 8 consecutive columns of one row (16-byte accesses); consecutive
 // threads take consecutive column groups, so every warp access is contiguous.
+// With M-major epilogue tensors consecutive threads take consecutive rows
+// instead, so that each of a thread's 8 column accesses is contiguous across
+// the warp.
 #include <utility>
 
 #include "catalog.cuh"
@@ -16,8 +19,19 @@ struct GlobalMem {
   const EwParams *p;
   int64_t row;
   int col0;
+  // element (row, col) of an M-major (L, N, M) tensor, row = l*M + i
+  __device__ __forceinline__ int64_t col_index(int col) const {
+    const int64_t l = row / p->M, i = row - l * p->M;
+    return (l * p->N + col) * p->M + i;
+  }
   template <int DT>
   __device__ __forceinline__ void aux(uint32_t i, float (&t)[kEwCols]) const {
+    if (p->cd_m) {
+#pragma unroll
+      for (int e = 0; e < kEwCols; ++e)
+        t[e] = col0 + e < p->N ? load_one<DT>(p->aux_ptr[i], col_index(col0 + e)) : 0.f;
+      return;
+    }
     const char *base = static_cast<const char *>(p->aux_ptr[i]) + row * p->N * (DT == GE_F32 ? 4 : 2);
     row_load<DT, kEwCols>(base, col0, p->N, t);
   }
@@ -33,6 +47,18 @@ struct GlobalMem {
   }
   template <int DT>
   __device__ __forceinline__ void store(uint32_t o, const float (&t)[kEwCols]) const {
+    if (p->cd_m) {
+#pragma unroll
+      for (int e = 0; e < kEwCols; ++e) {
+        if (col0 + e >= p->N) break;
+        const int64_t k = col_index(col0 + e);
+        if constexpr (DT == GE_F32) static_cast<float *>(p->out_ptr[o])[k] = t[e];
+        else if constexpr (DT == GE_BF16)
+          static_cast<__nv_bfloat16 *>(p->out_ptr[o])[k] = __float2bfloat16_rn(t[e]);
+        else static_cast<__half *>(p->out_ptr[o])[k] = __float2half_rn(t[e]);
+      }
+      return;
+    }
     char *base = static_cast<char *>(p->out_ptr[o]) + row * p->N * (DT == GE_F32 ? 4 : 2);
     row_store<DT, kEwCols>(base, col0, p->N, t);
   }
@@ -45,8 +71,16 @@ __global__ void __launch_bounds__(kEwThreads) epilogue_elementwise_kernel(
   const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
   for (int64_t u = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; u < units;
        u += stride) {
-    const int64_t row = u / p.chunks_per_row;
-    const int col0 = static_cast<int>(u - row * p.chunks_per_row) * kEwCols;
+    int64_t row;
+    int col0;
+    if (p.cd_m) {
+      const int64_t c = u / p.rows;
+      row = u - c * p.rows;
+      col0 = static_cast<int>(c) * kEwCols;
+    } else {
+      row = u / p.chunks_per_row;
+      col0 = static_cast<int>(u - row * p.chunks_per_row) * kEwCols;
+    }
     float acc[kEwCols];
     row_load<GE_F32, kEwCols>(p.acc + row * p.N, col0, p.N, acc);
     Epi::template run<kEwCols>(p.prog, acc, GlobalMem{&p, row, col0});

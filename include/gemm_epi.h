@@ -109,7 +109,11 @@ typedef struct {
   int32_t out[GE_MAX_OUT];      /* type of each output slot                    */
 } ge_dtypes;
 
-/* Optional tuning knobs; zero-initialise for automatic choices. */
+/* Storage order of a matrix operand ("Custom Epilogue Example", step
+ * "Define tensor arguments": a_major, b_major, cd_major). */
+typedef enum { GE_ROW_MAJOR = 0, GE_COL_MAJOR = 1 } ge_major;
+
+/* Optional knobs; zero-initialise for automatic choices and row-major data. */
 typedef struct {
   int32_t cta_group;    /* 0 auto, 1 = one CTA per MMA tile, 2 = CTA pair (2x1 cluster) */
   int32_t tile_n;       /* 0 auto, else the MMA N: 64, 128 or 256                       */
@@ -122,6 +126,20 @@ typedef struct {
                            computing adjacent N tiles and sharing A by TMA multicast
                            (cta_group 2, tile_n 256).  Opt-in: on GB300 only 36 such
                            clusters fit (144 SMs), which offsets the traffic saved.     */
+  /* Storage order, packed in every case (GE_ERR_INVALID for other values):
+   *   a_major   GE_ROW_MAJOR: A is (L,M,K), K contiguous ("K-major");
+   *             GE_COL_MAJOR: stored (L,K,M), M contiguous ("M-major")
+   *   b_major   GE_ROW_MAJOR: B is (L,K,N), N contiguous ("N-major");
+   *             GE_COL_MAJOR: stored (L,N,K), K contiguous ("K-major")
+   *   cd_major  every Load tensor and every output, alike (the pages'
+   *             same-major rule for epilogue tensors): GE_ROW_MAJOR (L,M,N),
+   *             N contiguous; GE_COL_MAJOR stored (L,N,M), M contiguous.
+   *             Row and column vectors are unaffected.
+   * The contiguous dimension of each tensor must be whole 16-byte units
+   * (GE_ERR_MISALIGNED).  cluster_n 2 needs a K-major A (GE_ERR_UNSUPPORTED). */
+  int32_t a_major;
+  int32_t b_major;
+  int32_t cd_major;
 } ge_options;
 
 /* Test hook: the producer never loads the first k-block, so the MMA warp's

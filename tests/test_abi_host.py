@@ -225,3 +225,25 @@ def test_grouped_plan_create_without_gpu_reports_arch():
 def test_grouped_run_rejects_null_plan():
     assert B.lib.gemm_epi_grouped_run(None, None, None, None, None, None, None) == \
         B.GE_ERR_INVALID
+
+
+def test_majors_checked_before_device():
+    """Storage orders: bad values, the contiguous dimension of each tensor
+    (per its major) in whole 16-byte units, multicast needing a K-major A."""
+    dt, dag = _base()
+    cases = [(dict(a_major=1), (1, 100, 128, 128), B.GE_ERR_MISALIGNED),
+             (dict(b_major=1), (1, 128, 128, 100), B.GE_ERR_MISALIGNED),
+             (dict(b_major=1), (1, 128, 12, 128), B.GE_ERR_MISALIGNED),   # C, D rows still N
+             (dict(cd_major=1), (1, 100, 128, 128), B.GE_ERR_MISALIGNED),
+             (dict(cd_major=-1), (1, 128, 128, 128), B.GE_ERR_INVALID),
+             (dict(b_major=3), (1, 128, 128, 128), B.GE_ERR_INVALID),
+             (dict(a_major=1, cluster_n=2), (1, 128, 128, 128), B.GE_ERR_UNSUPPORTED)]
+    for kw, (L, M, N, K), want in cases:
+        with pytest.raises(B.GemmEpiError) as e:
+            B.gemm_epi_plan_create(L, M, N, K, dt, B.make_dag(dag), B.ge_options(**kw))
+        assert e.value.status == want, (kw, e.value.status)
+    gdt, gdag = _grouped_base()
+    with pytest.raises(B.GemmEpiError) as e:
+        B.gemm_epi_grouped_plan_create([(128, 128, 128), (100, 128, 128)], gdt, gdag,
+                                       B.ge_options(a_major=1))
+    assert e.value.status == B.GE_ERR_MISALIGNED
