@@ -63,7 +63,7 @@ class ge_options(ctypes.Structure):
                 ("raster_group", ctypes.c_int32), ("timeout_ms", ctypes.c_int32),
                 ("debug_flags", ctypes.c_uint32), ("cluster_n", ctypes.c_int32),
                 ("a_major", ctypes.c_int32), ("b_major", ctypes.c_int32),
-                ("cd_major", ctypes.c_int32)]
+                ("cd_major", ctypes.c_int32), ("epi_warps", ctypes.c_int32)]
 
 
 class ge_problem(ctypes.Structure):
@@ -74,7 +74,7 @@ class ge_plan_info(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in
                 ("cta_group", "tile_m", "tile_n", "tile_k", "stages", "epi_chunk", "aux_stages",
                  "grid", "num_tiles", "smem_bytes", "n_instr", "n_regs", "num_sms",
-                 "epi_variant", "cluster_n")]
+                 "epi_variant", "cluster_n", "epi_warps")]
 
 
 class GemmEpiError(RuntimeError):

@@ -87,8 +87,15 @@ struct EpiProgram {
 constexpr int BM = 128;      // accumulator rows per CTA (TMEM lanes)
 constexpr int BK = 64;       // 16-bit elements per k-block: one 128-byte swizzle row
 constexpr int UMMA_K = 16;   // K of one tcgen05.mma.kind::f16
-constexpr int kEpiWarps = 4;
-constexpr int kThreads = 64 + 32 * kEpiWarps;  // producer warp, MMA warp, epilogue warps
+// Epilogue warps: 4 (one per TMEM lane quarter) or 8 (two per quarter, each
+// taking every other 32-column step of the tile).  A CTA has a producer warp,
+// an MMA warp and the epilogue warps.
+constexpr int kMaxEpiWarps = 8;
+__host__ __device__ constexpr int threads_for(int epi_warps) { return 64 + 32 * epi_warps; }
+// Output staging buffers per epilogue warp: two (a step's outputs are written
+// while the previous step's TMA store still reads its buffer) with 4 warps;
+// one with 8, where the quarter's other warp keeps the stores flowing.
+__host__ __device__ constexpr int out_bufs_for(int epi_warps) { return epi_warps == 8 ? 1 : 2; }
 constexpr int kMaxStages = 8;
 constexpr int kMaxAuxStages = 8;
 

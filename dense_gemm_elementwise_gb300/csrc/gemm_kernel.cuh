@@ -65,11 +65,11 @@ constexpr uint32_t kBarFull = 0;                       // kMaxStages x 8
 constexpr uint32_t kBarEmpty = 64;                     // kMaxStages x 8
 constexpr uint32_t kBarTmemFull = 128;                 // 2 x 8
 constexpr uint32_t kBarTmemEmpty = 144;                // 2 x 8
-constexpr uint32_t kBarAux = 160;                      // kEpiWarps x kMaxAuxStages x 8
-constexpr uint32_t kBarDrain = kBarAux + 8 * kEpiWarps * kMaxAuxStages;  // 416
-constexpr uint32_t kTmemSlot = kBarDrain + 8;          // 424
-constexpr uint32_t kAbortFlag = kTmemSlot + 4;         // 428
-constexpr uint32_t kBarBlockBytes = 512;
+constexpr uint32_t kBarAux = 160;                      // kMaxEpiWarps x kMaxAuxStages x 8
+constexpr uint32_t kBarDrain = kBarAux + 8 * kMaxEpiWarps * kMaxAuxStages;  // 672
+constexpr uint32_t kTmemSlot = kBarDrain + 8;          // 680
+constexpr uint32_t kAbortFlag = kTmemSlot + 4;         // 684
+constexpr uint32_t kBarBlockBytes = 1024;
 static_assert(kAbortFlag + 4 <= kBarBlockBytes, "barrier block overflow");
 
 __device__ __forceinline__ void tile_coords(int num_m_blk, int num_n_blk, int G, int t, int &l,
@@ -213,7 +213,11 @@ struct FusedMem {
 };
 
 template <int CG, int BN, int MC, class Epi>
-__global__ void __launch_bounds__(kThreads, 1) gemm_epi_kernel(const __grid_constant__ KParams p) {
+__global__ void __launch_bounds__(threads_for(Epi::kWarps), 1)
+    gemm_epi_kernel(const __grid_constant__ KParams p) {
+  constexpr int kEpiWarps = Epi::kWarps;
+  constexpr int kSplit = kEpiWarps / 4;  // warps per TMEM lane quarter
+  static_assert(kEpiWarps == 4 || kEpiWarps == 8, "4 or 8 epilogue warps");
   using T = TileCfg<CG, BN, MC>;
   extern __shared__ uint8_t smem_raw[];
   // 1024-byte alignment of the shared-window address (swizzle atoms)
@@ -447,13 +451,17 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_epi_kernel(const __grid_cons
     // --------------------------------------------------------- epilogue --
     const int e = warp - 2;  // staging slot
     const int q = warp & 3;  // TMEM lane quarter this warp may access
+    const int ch = e / 4;    // which of the quarter's warps: takes steps ch, ch + kSplit, ...
+    constexpr int kStepsW = T::kSteps / kSplit;  // this warp's steps per tile
+    static_assert(T::kSteps % kSplit == 0, "steps split evenly between a quarter's warps");
     const uint32_t tq = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
     uint8_t *aux_w = smem + p.off_aux + e * p.aux_stages * p.aux_stage_bytes;
-    uint8_t *out_w = smem + p.off_out + e * 2 * p.out_stage_bytes;
+    constexpr int kOutBufs = out_bufs_for(kEpiWarps);
+    uint8_t *out_w = smem + p.off_out + e * kOutBufs * p.out_stage_bytes;
     const uint32_t auxbar_w = bar_aux + 8u * e * kMaxAuxStages;
     const bool has_aux = p.prog.n_tma_aux > 0;
     const int SA = p.aux_stages;
-    const int total = my_tiles * T::kSteps;
+    const int total = my_tiles * kStepsW;
     int issued = 0, g = 0, abuf = 0, obuf = 0;
     uint32_t aphase = 0;
     bool ok = true;
@@ -465,7 +473,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_epi_kernel(const __grid_cons
 
     // TMA loads of every Load tensor for this warp's 32 rows of step gi
     auto issue_aux = [&](int gi) {
-      const int ii = gi / T::kSteps;
+      const int ii = gi / kStepsW;
       if (ii != pf_tile) {
         const TileRef tr = pf_tc.next();  // tiles are entered in order, one at a time
         pf_l = tr.l;
@@ -484,7 +492,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_epi_kernel(const __grid_cons
       uint8_t *dst = aux_w + as * p.aux_stage_bytes;
       fence_proxy_async_smem();
       mbar_arrive_expect_tx(ab, p.aux_tx_bytes);
-      const int x = pf_x0 + (gi - ii * T::kSteps) * EW;
+      const int x = pf_x0 + ((gi - ii * kStepsW) * kSplit + ch) * EW;
       for (int a = 0; a < p.prog.n_tma_aux; ++a)
         tma_load_3d(smem_u32(dst + p.aux_off[a]), &pf_maps[a], ab, p.cd_m ? pf_y : x,
                     p.cd_m ? x : pf_y, pf_l);
@@ -525,7 +533,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_epi_kernel(const __grid_cons
         }
       }
       tc_fence_after();
-      for (int s = 0; s < T::kSteps; ++s, ++g) {
+      for (int s = ch; s < T::kSteps; s += kSplit, ++g) {
         if (has_aux && lane == 0) {
           while (issued < total && issued < g + SA) issue_aux(issued++);
         }
@@ -535,7 +543,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_epi_kernel(const __grid_cons
         tmem_ld16(tq + col, acc0);
         tmem_ld16(tq + col + CH, acc1);
         tmem_wait_ld();
-        if (s == T::kSteps - 1) {
+        if (s + kSplit >= T::kSteps) {
           // accumulator fully read: hand it back to the MMA warp
           tc_fence_before();
           __syncwarp();
@@ -553,8 +561,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_epi_kernel(const __grid_cons
             break;
           }
         }
-        // the staging buffer written two steps ago has been read by its store
-        if (lane == 0) bulk_wait_group_read<1>();
+        // the staging buffer about to be written has been read by its last store
+        if (lane == 0) bulk_wait_group_read<kOutBufs - 1>();
         __syncwarp();
         uint8_t *ostage = out_w + obuf * p.out_stage_bytes;
         const uint8_t *astage = aux_w + (g % SA) * p.aux_stage_bytes;
@@ -571,7 +579,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_epi_kernel(const __grid_cons
                          p.cd_m ? c0 : m0, l);
           bulk_commit_group();
         }
-        obuf ^= 1;
+        if constexpr (kOutBufs == 2) obuf ^= 1;
       }
       abuf ^= 1;
       if (abuf == 0) aphase ^= 1u;

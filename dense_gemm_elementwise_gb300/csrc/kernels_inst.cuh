@@ -10,19 +10,27 @@
 
 namespace ge {
 
+// epi < 0: the interpreter (4 epilogue warps only); else catalog entry epi
+// with 4 or 8 epilogue warps
 template <int CG, int BN, int MC, size_t... K>
-const void *pick_gemm_kernel(int epi, std::index_sequence<K...>) {
-  static const void *const table[] = {
-      reinterpret_cast<const void *>(&gemm_epi_kernel<CG, BN, MC, EpiStatic<catalog::Prog<K>>>)...};
-  if (epi < 0) return reinterpret_cast<const void *>(&gemm_epi_kernel<CG, BN, MC, EpiInterp>);
-  return epi < static_cast<int>(sizeof...(K)) ? table[epi] : nullptr;
+const void *pick_gemm_kernel(int epi, int warps, std::index_sequence<K...>) {
+  static const void *const table4[] = {reinterpret_cast<const void *>(
+      &gemm_epi_kernel<CG, BN, MC, EpiStatic<catalog::Prog<K>, 4>>)...};
+  static const void *const table8[] = {reinterpret_cast<const void *>(
+      &gemm_epi_kernel<CG, BN, MC, EpiStatic<catalog::Prog<K>, 8>>)...};
+  if (epi < 0)
+    return warps == 4 ? reinterpret_cast<const void *>(&gemm_epi_kernel<CG, BN, MC, EpiInterp>)
+                      : nullptr;
+  if (epi >= static_cast<int>(sizeof...(K))) return nullptr;
+  return warps == 4 ? table4[epi] : warps == 8 ? table8[epi] : nullptr;
 }
 
 }  // namespace ge
 
 #define GE_INSTANTIATE_GEMM(CG, BN, MC, NAME)                                              \
   namespace ge {                                                                           \
-  const void *NAME(int epi) {                                                              \
-    return pick_gemm_kernel<CG, BN, MC>(epi, std::make_index_sequence<catalog::kCount>{}); \
+  const void *NAME(int epi, int warps) {                                                   \
+    return pick_gemm_kernel<CG, BN, MC>(epi, warps,                                       \
+                                        std::make_index_sequence<catalog::kCount>{});     \
   }                                                                                        \
   }

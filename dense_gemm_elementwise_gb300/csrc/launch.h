@@ -2,7 +2,8 @@
 //
 // Every handle is a __global__ function usable with cudaFuncSetAttribute and
 // cudaLaunchKernelExC.  `epi` selects the epilogue executor: -1 the
-// interpreter, k >= 0 the straight-line kernel of catalog entry k.
+// interpreter, k >= 0 the straight-line kernel of catalog entry k; `warps`
+// the epilogue warps (4, or 8 for catalog entries).  nullptr if not built.
 #pragma once
 
 #include <cuda_runtime_api.h>
@@ -12,12 +13,12 @@
 namespace ge {
 
 // fused GEMM + epilogue, (cta_group, BN) in {(1,64), (1,128), (1,256), (2,128), (2,256)}
-const void *gemm_kernel_cg1_n64(int epi);
-const void *gemm_kernel_cg1_n128(int epi);
-const void *gemm_kernel_cg1_n256(int epi);
-const void *gemm_kernel_cg2_n128(int epi);
-const void *gemm_kernel_cg2_n256(int epi);
-const void *gemm_kernel_cg2_n256_mc2(int epi);  // 4-CTA cluster, A multicast across 2 pairs
+const void *gemm_kernel_cg1_n64(int epi, int warps);
+const void *gemm_kernel_cg1_n128(int epi, int warps);
+const void *gemm_kernel_cg1_n256(int epi, int warps);
+const void *gemm_kernel_cg2_n128(int epi, int warps);
+const void *gemm_kernel_cg2_n256(int epi, int warps);
+const void *gemm_kernel_cg2_n256_mc2(int epi, int warps);  // 4-CTA cluster, A multicast
 
 // unfused comparison path: elementwise epilogue over an fp32 accumulator
 const void *ew_kernel(int epi);

@@ -170,6 +170,7 @@ bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 struct Layout {
   int cg = 0, bn = 0, stages = 0, aux_stages = 0, grid = 0, num_tiles = 0;
   int mc = 1;         // CTA pairs per cluster sharing A (multicast)
+  int warps = 4;      // epilogue warps (4 or 8)
   int smem = 0;       // dynamic smem requested at launch
   int smem_used = 0;  // bytes the layout occupies
   int num_m_blk = 0, num_n_blk = 0, num_kb = 0, raster_group = 0;
@@ -179,7 +180,7 @@ struct Layout {
   uint32_t tx_bytes = 0, aux_tx_bytes = 0;
 };
 
-constexpr int kBarBlock = 512;
+constexpr int kBarBlock = 1024;
 constexpr int kAlignSlack = 1024;
 
 // Shared-memory layout for (cg, bn) and a program; stages = 0 picks the most
@@ -187,7 +188,7 @@ constexpr int kAlignSlack = 1024;
 // leaves min_main mainloop stages.  Returns GE_ERR_SMEM if fewer than 2 (or the
 // requested count) fit.
 int make_layout(Layout *Lo, int cg, int bn, int want_stages, const EpiProgram &P, int max_smem,
-                int max_aux = 4, int min_main = 5) {
+                int max_aux = 4, int min_main = 5, int warps = 4) {
   const uint32_t a_bytes = BM * BK * 2;
   const uint32_t b_bytes = static_cast<uint32_t>(bn / cg) * BK * 2;
   uint32_t aux_stage = 0, out_stage = 0;
@@ -200,16 +201,19 @@ int make_layout(Layout *Lo, int cg, int bn, int want_stages, const EpiProgram &P
     out_stage += 32u * EW * esize(P.out_dtype[o]);
   }
   auto stages_with = [&](int sa) {
-    const int64_t epi = int64_t(kEpiWarps) * sa * aux_stage + int64_t(kEpiWarps) * 2 * out_stage;
+    const int64_t epi = int64_t(warps) * sa * aux_stage + int64_t(warps) * out_bufs_for(warps) * out_stage;
     const int64_t room = int64_t(max_smem) - kAlignSlack - kBarBlock - epi;
     const int s = room > 0 ? static_cast<int>(room / (a_bytes + b_bytes)) : 0;
     return std::min(s, kMaxStages);
   };
+  // 4 warps: at least 2 aux stages; 8 warps (each warp's steps twice as far
+  // apart in time) may go down to 1
+  const int min_sa = warps == 8 ? 1 : 2;
   int sa = 1, stages = stages_with(1);
   if (P.n_tma_aux > 0) {
-    sa = 2;
-    stages = stages_with(2);
-    for (int cand = std::min(max_aux, kMaxAuxStages); cand > 2; --cand)
+    sa = min_sa;
+    stages = stages_with(min_sa);
+    for (int cand = std::min(max_aux, kMaxAuxStages); cand > min_sa; --cand)
       if (stages_with(cand) >= min_main) {
         sa = cand;
         stages = stages_with(cand);
@@ -230,8 +234,9 @@ int make_layout(Layout *Lo, int cg, int bn, int want_stages, const EpiProgram &P
   Lo->off_A = 0;
   Lo->off_B = stages * a_bytes;
   Lo->off_aux = Lo->off_B + stages * b_bytes;
-  Lo->off_out = Lo->off_aux + kEpiWarps * sa * aux_stage;
-  Lo->off_bar = Lo->off_out + kEpiWarps * 2 * out_stage;
+  Lo->off_out = Lo->off_aux + warps * sa * aux_stage;
+  Lo->off_bar = Lo->off_out + warps * out_bufs_for(warps) * out_stage;
+  Lo->warps = warps;
   Lo->smem_used = static_cast<int>(Lo->off_bar + kBarBlock + kAlignSlack);
   // Always request the whole opt-in shared memory: exactly one CTA per SM, so
   // co-resident CTAs never compete for TMEM columns (a CTA blocked in
@@ -295,20 +300,20 @@ struct gemm_epi_plan {
 
 namespace {
 
-const void *gemm_kernel(int cg, int bn, int mc, int epi) {
-  if (mc == 2) return (cg == 2 && bn == 256) ? gemm_kernel_cg2_n256_mc2(epi) : nullptr;
-  if (cg == 1 && bn == 64) return gemm_kernel_cg1_n64(epi);
-  if (cg == 1 && bn == 128) return gemm_kernel_cg1_n128(epi);
-  if (cg == 1 && bn == 256) return gemm_kernel_cg1_n256(epi);
-  if (cg == 2 && bn == 128) return gemm_kernel_cg2_n128(epi);
-  if (cg == 2 && bn == 256) return gemm_kernel_cg2_n256(epi);
+const void *gemm_kernel(int cg, int bn, int mc, int epi, int warps) {
+  if (mc == 2) return (cg == 2 && bn == 256) ? gemm_kernel_cg2_n256_mc2(epi, warps) : nullptr;
+  if (cg == 1 && bn == 64) return gemm_kernel_cg1_n64(epi, warps);
+  if (cg == 1 && bn == 128) return gemm_kernel_cg1_n128(epi, warps);
+  if (cg == 1 && bn == 256) return gemm_kernel_cg1_n256(epi, warps);
+  if (cg == 2 && bn == 128) return gemm_kernel_cg2_n128(epi, warps);
+  if (cg == 2 && bn == 256) return gemm_kernel_cg2_n256(epi, warps);
   return nullptr;
 }
 
 cudaLaunchConfig_t launch_config(const Layout &Lo, cudaStream_t s, cudaLaunchAttribute *attr) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(Lo.grid));
-  cfg.blockDim = dim3(kThreads);
+  cfg.blockDim = dim3(static_cast<unsigned>(threads_for(Lo.warps)));
   cfg.dynamicSmemBytes = static_cast<size_t>(Lo.smem);
   cfg.stream = s;
   cfg.attrs = nullptr;
@@ -325,7 +330,7 @@ cudaLaunchConfig_t launch_config(const Layout &Lo, cudaStream_t s, cudaLaunchAtt
 }
 
 cudaError_t launch_gemm(const Layout &Lo, int epi, const KParams &kp, cudaStream_t s) {
-  const void *fn = gemm_kernel(Lo.cg, Lo.bn, Lo.mc, epi);
+  const void *fn = gemm_kernel(Lo.cg, Lo.bn, Lo.mc, epi, Lo.warps);
   if (!fn) return cudaErrorInvalidDeviceFunction;
   cudaLaunchAttribute attr[1];
   cudaLaunchConfig_t cfg = launch_config(Lo, s, attr);
@@ -349,6 +354,18 @@ double est_cycles(const gemm_epi_plan *pl, int cg, int bn, int mc, int units) {
   const double per_tile = kb * std::max(mma, fill);
   const int64_t waves = (tiles + units - 1) / units;
   return waves * per_tile + (bn / CH) * 300.0;
+}
+
+// Epilogue warps: the option, else 8 for built-in epilogues (two warps per
+// lane quarter overlap each other's waits: measured equal or faster on every
+// workload, up to 1.5x where the epilogue outweighs a short mainloop) and 4
+// for the interpreter (its registers do not fit 8 warps beside the others).
+int pick_epi_warps(const gemm_epi_plan *pl, int *warps) {
+  const int w = pl->opt.epi_warps;
+  if (w != 0 && w != 4 && w != 8) return GE_ERR_INVALID;
+  if (w == 8 && pl->epi < 0) return GE_ERR_UNSUPPORTED;
+  *warps = w ? w : (pl->epi >= 0 ? 8 : 4);
+  return GE_OK;
 }
 
 int configure(gemm_epi_plan *pl) {
@@ -379,7 +396,10 @@ int configure(gemm_epi_plan *pl) {
   if (best < 0) return GE_ERR_INVALID;  // e.g. cta_group 2 with tile_n 64
   const int cg = cand[best][0], bn = cand[best][1], mc = cand[best][2];
 
-  int st = make_layout(&pl->lay, cg, bn, o.stages, pl->prog, pl->max_smem);
+  int warps = 0;
+  int st = pick_epi_warps(pl, &warps);
+  if (st != GE_OK) return st;
+  st = make_layout(&pl->lay, cg, bn, o.stages, pl->prog, pl->max_smem, 4, 5, warps);
   if (st != GE_OK) return st;
   st = make_layout(&pl->lay_acc, cg, bn, o.stages, pl->prog_acc, pl->max_smem);
   if (st != GE_OK) return st;
@@ -397,7 +417,7 @@ int configure(gemm_epi_plan *pl) {
     int sms = pl->num_sms;
     if (o.max_ctas) sms = std::min(sms, o.max_ctas);
     int units = std::max(1, sms / (cg * mc));
-    const void *fn = gemm_kernel(cg, bn, mc, Lo == &pl->lay ? pl->epi : pl->epi_acc);
+    const void *fn = gemm_kernel(cg, bn, mc, Lo == &pl->lay ? pl->epi : pl->epi_acc, Lo->warps);
     if (!fn) return GE_ERR_INVALID;
     if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, Lo->smem) != cudaSuccess)
       return GE_ERR_CUDA;
@@ -673,6 +693,7 @@ int gemm_epi_plan_info(const gemm_epi_plan *pl, ge_plan_info *info) {
   info->num_sms = pl->num_sms;
   info->epi_variant = pl->epi;
   info->cluster_n = pl->lay.mc;
+  info->epi_warps = pl->lay.warps;
   return GE_OK;
 }
 
@@ -772,24 +793,25 @@ namespace {
 // model of est_cycles) or the epilogue, whichever is slower, since the two
 // overlap across consecutive tiles, plus a fixed cost per tile.  The epilogue
 // and fixed terms are fitted to measured launches of many short problems,
-// whose tiles are short: 900 clocks per 16-column chunk, 4000 per tile.
-double grouped_tile_cycles(int64_t K, int cg, int bn) {
+// whose tiles are short: 900 clocks per 16-column chunk with 4 epilogue
+// warps (half that with 8), 4000 per tile.
+double grouped_tile_cycles(int64_t K, int cg, int bn, int warps) {
   const int64_t kb = (K + BK - 1) / BK;
   const double fill = double((BM + bn / cg) * BK * 2) / 48.0;
   const double main = kb * std::max(2.0 * bn, fill);
-  return std::max(main, (bn / CH) * 900.0) + 4000.0;
+  return std::max(main, (bn / CH) * 900.0 * 4.0 / warps) + 4000.0;
 }
 
 // The launch deals the tiles (problems with the most k-blocks first) round
 // robin to the units; it lasts about as long as the busiest unit.
 double est_cycles_grouped(const gemm_epi_plan *pl, const std::vector<int> &order, int cg, int bn,
-                          int units) {
+                          int units, int warps) {
   std::vector<double> busy(static_cast<size_t>(units), 0.0);
   int64_t t = 0;
   for (int g : order) {
     const ge_problem &pr = pl->problems[g];
     const int64_t tiles = ((pr.M + BM * cg - 1) / (BM * cg)) * ((pr.N + bn - 1) / bn);
-    const double c = grouped_tile_cycles(pr.K, cg, bn);
+    const double c = grouped_tile_cycles(pr.K, cg, bn, warps);
     // whole rounds of the deal add c to every unit; the rest to the next ones
     const int64_t rounds = tiles / units, rest = tiles % units;
     for (int u = 0; u < units; ++u) busy[u] += rounds * c;
@@ -818,6 +840,9 @@ int configure_grouped(gemm_epi_plan *pl) {
   std::stable_sort(pl->order.begin(), pl->order.end(), [&](int a, int b) {
     return pl->problems[a].K > pl->problems[b].K;
   });
+  int warps = 0;
+  int st = pick_epi_warps(pl, &warps);
+  if (st != GE_OK) return st;
   int best = -1;
   double best_c = 0;
   for (int c = 0; c < 5; ++c) {
@@ -825,7 +850,7 @@ int configure_grouped(gemm_epi_plan *pl) {
     if (o.cta_group && o.cta_group != cg) continue;
     if (o.tile_n && o.tile_n != bn) continue;
     if (sms < cg) continue;
-    const double cost = est_cycles_grouped(pl, pl->order, cg, bn, sms / cg);
+    const double cost = est_cycles_grouped(pl, pl->order, cg, bn, sms / cg, warps);
     if (best < 0 || cost < best_c * 0.98) {
       best = c;
       best_c = cost;
@@ -836,8 +861,8 @@ int configure_grouped(gemm_epi_plan *pl) {
   // short problems make short tiles, whose epilogue would wait on aux loads
   // issued only a few steps ahead: prefetch up to two tiles' steps of aux
   // data, keeping 4 mainloop stages
-  int st = make_layout(&pl->lay, cg, bn, o.stages, pl->prog, pl->max_smem,
-                       std::min(kMaxAuxStages, 2 * bn / EW), 4);
+  st = make_layout(&pl->lay, cg, bn, o.stages, pl->prog, pl->max_smem,
+                   std::min(kMaxAuxStages, 2 * bn / EW), 4, warps);
   if (st != GE_OK) return st;
   Layout &Lo = pl->lay;
   Lo.mc = 1;
@@ -849,7 +874,7 @@ int configure_grouped(gemm_epi_plan *pl) {
   }
   if (tiles > (int64_t(1) << 24)) return GE_ERR_SHAPE;  // the tile table: 16 bytes a tile
   Lo.num_tiles = static_cast<int>(tiles);
-  const void *fn = gemm_kernel(cg, bn, 1, pl->epi);
+  const void *fn = gemm_kernel(cg, bn, 1, pl->epi, Lo.warps);
   if (!fn) return GE_ERR_INVALID;
   if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, Lo.smem) != cudaSuccess)
     return GE_ERR_CUDA;

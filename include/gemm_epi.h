@@ -140,6 +140,11 @@ typedef struct {
   int32_t a_major;
   int32_t b_major;
   int32_t cd_major;
+  /* 0 auto (8 for built-in epilogues, 4 for the interpreter), else the
+   * epilogue warps per CTA: 4 (one per accumulator lane quarter) or 8 (two
+   * per quarter, each taking every other 32-column step; built-in
+   * epilogues only, GE_ERR_UNSUPPORTED for the interpreter).               */
+  int32_t epi_warps;
 } ge_options;
 
 /* Test hook: the producer never loads the first k-block, so the MMA warp's
@@ -161,6 +166,7 @@ typedef struct {
   int32_t num_sms;
   int32_t epi_variant;                        /* built-in epilogue used, -1: interpreter */
   int32_t cluster_n;                          /* CTA pairs sharing A per cluster         */
+  int32_t epi_warps;                          /* epilogue warps per CTA (4 or 8)         */
 } ge_plan_info;
 
 typedef struct gemm_epi_plan gemm_epi_plan;

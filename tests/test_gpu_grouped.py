@@ -224,3 +224,13 @@ def test_grouped_device_wait_timeout_is_reported():
     finally:
         G.close()
     run_and_check(w)
+
+
+def test_grouped_eight_epilogue_warps():
+    """A built-in epilogue (alpha*accum + beta*C) with two warps per lane
+    quarter over problems of every size."""
+    w = W.GROUPED_BY_NAME["grouped_gemm_50"]
+    w = dataclasses.replace(w, scalars=[("alpha", 1.0), ("beta", 2.0)])
+    for cg, bn in [(1, 128), (2, 256), (1, 64)]:
+        info = run_and_check(w, B.ge_options(epi_warps=8, cta_group=cg, tile_n=bn))
+        assert (info["cta_group"], info["tile_n"]) == (cg, bn) and info["epi_variant"] >= 0

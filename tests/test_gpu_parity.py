@@ -364,3 +364,51 @@ def test_leaky_relu_forms(w, variant):
     _gpu.compare(w, gpu, _gpu.oracle_rows(w, inputs))
     unf, _ = _gpu.run_gpu(w, inputs, unfused=True, options=opts(variant))
     _gpu.bitwise_equal(gpu, unf)
+
+
+# ------------------------------------------------ eight epilogue warps --
+
+@pytest.mark.parametrize("w", CATALOG_CASES[:4] + [small(W.CONFIGS[4], 2, 264, 520, 136)] +
+                         [x for x in CATALOG_CASES if x.name in ("complex_gelu_tanh",
+                                                                  "row_col_bias_f16")],
+                         ids=lambda w: w.name)
+@pytest.mark.parametrize("variant", [(1, 64, 1), (1, 256, 1), (2, 128, 1), (2, 256, 1),
+                                     (2, 256, 2)], ids=vid)
+def test_eight_epilogue_warps_bitwise(w, variant):
+    """Two warps per accumulator lane quarter, each taking every other
+    32-column step: the same bits as four warps, and the oracle's values."""
+    inputs = W.make_inputs(w)
+    base = dict(cta_group=variant[0], tile_n=variant[1], cluster_n=variant[2])
+    four, i4 = _gpu.run_gpu(w, inputs, options=B.ge_options(epi_warps=4, **base))
+    eight, i8 = _gpu.run_gpu(w, inputs, options=B.ge_options(epi_warps=8, **base))
+    assert i8["epi_variant"] >= 0
+    _gpu.bitwise_equal(four, eight)
+    _gpu.compare(w, eight, _gpu.oracle_rows(w, inputs))
+
+
+def test_eight_epilogue_warps_rules():
+    w = small(W.CONFIGS[0], 1, 256, 256, 256)
+    dt, dag = _gpu.dtypes_of(w), B.make_dag(w.dag)
+    for opt, want in [(dict(epi_warps=8, debug_flags=B.GE_DEBUG_FORCE_INTERPRETER),
+                       B.GE_ERR_UNSUPPORTED), (dict(epi_warps=6), B.GE_ERR_INVALID)]:
+        with pytest.raises(B.GemmEpiError) as e:
+            B.gemm_epi_plan_create(1, 256, 256, 256, dt, dag, B.ge_options(**opt))
+        assert e.value.status == want
+
+
+def test_eight_epilogue_warps_timeout_is_reported():
+    w = small(W.CONFIGS[0], 1, 256, 256, 256)
+    inputs = W.make_inputs(w)
+    A, Bm, aux, sc = inputs
+    opt = B.ge_options(timeout_ms=50, debug_flags=B.GE_DEBUG_SKIP_FIRST_LOAD, max_ctas=2,
+                       cta_group=2, tile_n=256, epi_warps=8)
+    outs = [torch.empty(1, 256, 256, dtype=torch.float16, device="cuda") for _ in range(2)]
+    plan = B.gemm_epi_plan_create(1, 256, 256, 256, _gpu.dtypes_of(w), B.make_dag(w.dag), opt)
+    try:
+        assert B.gemm_epi_run(plan, A.cuda(), Bm.cuda(), [aux[0].cuda()], sc, outs) == B.GE_OK
+        torch.cuda.synchronize()
+        assert B.gemm_epi_last_error(plan) == B.GE_ERR_TIMEOUT
+    finally:
+        B.gemm_epi_plan_destroy(plan)
+    gpu, _ = _gpu.run_gpu(w, inputs, options=B.ge_options(epi_warps=8))
+    _gpu.compare(w, gpu, _gpu.oracle_rows(w, inputs))
