@@ -401,7 +401,9 @@ int configure(gemm_epi_plan *pl) {
   if (st != GE_OK) return st;
   st = make_layout(&pl->lay, cg, bn, o.stages, pl->prog, pl->max_smem, 4, 5, warps);
   if (st != GE_OK) return st;
-  st = make_layout(&pl->lay_acc, cg, bn, o.stages, pl->prog_acc, pl->max_smem);
+  // the unfused path's GEMM stores fp32 accum: a built-in epilogue on 8 warps
+  st = make_layout(&pl->lay_acc, cg, bn, o.stages, pl->prog_acc, pl->max_smem, 4, 5,
+                   pl->epi_acc >= 0 ? 8 : 4);
   if (st != GE_OK) return st;
 
   for (Layout *Lo : {&pl->lay, &pl->lay_acc}) {
