@@ -478,15 +478,17 @@ __device__ __forceinline__ void run_static_from(float (&r)[kRegs][C], const floa
 }
 
 // Epilogue selectors used as kernel template arguments.
-// kWarps: epilogue warps of the fused kernels built with the selector.  The
-// interpreter needs too many registers for 8 warps beside the other two.
-struct EpiInterp {
-  static constexpr int kWarps = 4;
+// kWarps: epilogue warps of the fused kernels built with the selector (the
+// unfused elementwise kernel ignores it).
+template <int W = 4>
+struct EpiInterpW {
+  static constexpr int kWarps = W;
   template <int C, class Mem>
   __device__ __forceinline__ static void run(const EpiProgram &P, const float (&acc)[C], const Mem &mem) {
     run_program<C>(P, acc, mem);
   }
 };
+using EpiInterp = EpiInterpW<4>;
 
 template <class SP, int W = 4>
 struct EpiStatic {

@@ -3,7 +3,7 @@
 // Every handle is a __global__ function usable with cudaFuncSetAttribute and
 // cudaLaunchKernelExC.  `epi` selects the epilogue executor: -1 the
 // interpreter, k >= 0 the straight-line kernel of catalog entry k; `warps`
-// the epilogue warps (4, or 8 for catalog entries).  nullptr if not built.
+// the epilogue warps (4 or 8).  nullptr if not built.
 #pragma once
 
 #include <cuda_runtime_api.h>

@@ -356,15 +356,16 @@ double est_cycles(const gemm_epi_plan *pl, int cg, int bn, int mc, int units) {
   return waves * per_tile + (bn / CH) * 300.0;
 }
 
-// Epilogue warps: the option, else 8 for built-in epilogues (two warps per
-// lane quarter overlap each other's waits: measured equal or faster on every
-// workload, up to 1.5x where the epilogue outweighs a short mainloop) and 4
-// for the interpreter (its registers do not fit 8 warps beside the others).
+// Epilogue warps: the option, else 8.  Two warps per lane quarter overlap
+// each other's waits: with built-in epilogues measured equal or faster on
+// every workload (up to 1.5x where the epilogue outweighs a short
+// mainloop); with the interpreter, which then spills a few registers, 1.13x
+// to 1.27x faster on transcendental and multi-output epilogues and 4 %
+// slower on a cheap one.
 int pick_epi_warps(const gemm_epi_plan *pl, int *warps) {
   const int w = pl->opt.epi_warps;
   if (w != 0 && w != 4 && w != 8) return GE_ERR_INVALID;
-  if (w == 8 && pl->epi < 0) return GE_ERR_UNSUPPORTED;
-  *warps = w ? w : (pl->epi >= 0 ? 8 : 4);
+  *warps = w ? w : 8;
   return GE_OK;
 }
 

@@ -140,10 +140,9 @@ typedef struct {
   int32_t a_major;
   int32_t b_major;
   int32_t cd_major;
-  /* 0 auto (8 for built-in epilogues, 4 for the interpreter), else the
-   * epilogue warps per CTA: 4 (one per accumulator lane quarter) or 8 (two
-   * per quarter, each taking every other 32-column step; built-in
-   * epilogues only, GE_ERR_UNSUPPORTED for the interpreter).               */
+  /* 0 auto (8), else the epilogue warps per CTA: 4 (one per accumulator
+   * lane quarter) or 8 (two per quarter, each taking every other 32-column
+   * step).  Results are identical either way; GE_ERR_INVALID otherwise.   */
   int32_t epi_warps;
 } ge_options;
 

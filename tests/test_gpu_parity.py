@@ -389,11 +389,27 @@ def test_eight_epilogue_warps_bitwise(w, variant):
 def test_eight_epilogue_warps_rules():
     w = small(W.CONFIGS[0], 1, 256, 256, 256)
     dt, dag = _gpu.dtypes_of(w), B.make_dag(w.dag)
-    for opt, want in [(dict(epi_warps=8, debug_flags=B.GE_DEBUG_FORCE_INTERPRETER),
-                       B.GE_ERR_UNSUPPORTED), (dict(epi_warps=6), B.GE_ERR_INVALID)]:
-        with pytest.raises(B.GemmEpiError) as e:
-            B.gemm_epi_plan_create(1, 256, 256, 256, dt, dag, B.ge_options(**opt))
-        assert e.value.status == want
+    with pytest.raises(B.GemmEpiError) as e:
+        B.gemm_epi_plan_create(1, 256, 256, 256, dt, dag, B.ge_options(epi_warps=6))
+    assert e.value.status == B.GE_ERR_INVALID
+
+
+@pytest.mark.parametrize("w", [small(W.CONFIGS[4], 2, 264, 520, 136)] +
+                         [x for x in CATALOG_CASES if x.name in ("act_sigmoid", "clamp_f16",
+                                                                  "aux_normalize_f16")],
+                         ids=lambda w: w.name)
+@pytest.mark.parametrize("variant", [(1, 128, 1), (2, 256, 1)], ids=vid)
+def test_interpreter_eight_warps_bitwise(w, variant):
+    """The interpreter on 8 warps: the same bits as on 4 and as the
+    built-in kernels."""
+    inputs = W.make_inputs(w)
+    base = dict(cta_group=variant[0], tile_n=variant[1], cluster_n=variant[2],
+                debug_flags=B.GE_DEBUG_FORCE_INTERPRETER)
+    four, i4 = _gpu.run_gpu(w, inputs, options=B.ge_options(epi_warps=4, **base))
+    eight, i8 = _gpu.run_gpu(w, inputs, options=B.ge_options(epi_warps=8, **base))
+    assert i4["epi_variant"] == -1 and i8["epi_warps"] == 8
+    _gpu.bitwise_equal(four, eight)
+    _gpu.compare(w, eight, _gpu.oracle_rows(w, inputs))
 
 
 def test_eight_epilogue_warps_timeout_is_reported():
