@@ -23,7 +23,7 @@ namespace ge {
 // ---------------------------------------------------------------------------
 constexpr int CH = 16;        // columns one program evaluation covers per thread
 constexpr int EW = 32;        // columns of one fused-epilogue step (TMA box width)
-constexpr int kRegs = 4;      // vector registers of the epilogue program
+constexpr int kRegs = 8;      // vector registers of the epilogue program (at most)
 constexpr int kMaxIns = 48;   // instructions in one program
 
 enum EpiOp : uint32_t {

@@ -3,15 +3,16 @@
 // A program (program.cuh) is evaluated for CH consecutive columns of one
 // output row per thread.  Two executors evaluate the same instruction list:
 //
-//   run_program<CH>          the interpreter: one uniform dispatch per
-//                            instruction per CH columns (any DAG the plan
-//                            compiler accepts);
+//   run_program4<CH>         the interpreter: one uniform dispatch per
+//   run_programR<CH, R>      instruction per CH columns (any DAG the plan
+//                            compiler accepts; programs needing more than 4
+//                            registers use the R = kRegs variant);
 //   run_static_from<SP,..>   the catalog executor: the instruction list is a
 //                            compile-time constant, every dispatch is resolved
 //                            by `if constexpr`, leaving straight-line fp32 code.
 //
-// All register-array indices are compile-time constants, so values stay in
-// registers.  Multiplies and adds are __fmul_rn/__fadd_rn (never contracted
+// All register-array indices are compile-time constants (a run-time register
+// number selects among them through a switch), so values stay in registers.  Multiplies and adds are __fmul_rn/__fadd_rn (never contracted
 // into an FMA); ReLU returns +0 for x <= 0; a store rounds once to nearest
 // even.  The memory policy `Mem` supplies aux tensors and broadcast vectors
 // and takes the stores: swizzled shared-memory TMA boxes in the fused kernel,
@@ -266,11 +267,13 @@ __host__ __device__ constexpr bool is_activation_op(uint32_t op) {
 }
 
 // ------------------------------------------------------------ interpreter --
+// Four program registers: every operation has its own switch over the
+// destination register (fewest live values, no spills at 4 warps).
 template <int C, class Mem>
-__device__ __forceinline__ void run_program(const EpiProgram &P, const float (&acc)[C], const Mem &mem) {
-  float r[kRegs][C];
+__device__ __forceinline__ void run_program4(const EpiProgram &P, const float (&acc)[C], const Mem &mem) {
+  float r[4][C];
 #pragma unroll
-  for (int i = 0; i < kRegs; ++i)
+  for (int i = 0; i < 4; ++i)
 #pragma unroll
     for (int e = 0; e < C; ++e) r[i][e] = 0.f;
 
@@ -405,6 +408,108 @@ __device__ __forceinline__ void run_program(const EpiProgram &P, const float (&a
   }
 }
 
+// More program registers (up to kRegs): a register is selected at run time: a register is read into, or
+// written from, a plain vector through one switch, so each operation's code
+// exists once, whatever register it works on.
+#define GE_REG_CASE(I, STMT) \
+  case I:                    \
+    if constexpr (I < R) {   \
+      STMT;                  \
+    }                        \
+    break;
+
+template <int R, int C>
+__device__ __forceinline__ void reg_read(const float (&r)[R][C], uint32_t k, float (&t)[C]) {
+  switch (k) {
+    GE_REG_CASE(0, vcopy(t, r[0])) GE_REG_CASE(1, vcopy(t, r[1])) GE_REG_CASE(2, vcopy(t, r[2]))
+    GE_REG_CASE(3, vcopy(t, r[3])) GE_REG_CASE(4, vcopy(t, r[4])) GE_REG_CASE(5, vcopy(t, r[5]))
+    GE_REG_CASE(6, vcopy(t, r[6])) GE_REG_CASE(7, vcopy(t, r[7]))
+    default: break;
+  }
+}
+
+template <int R, int C>
+__device__ __forceinline__ void reg_write(float (&r)[R][C], uint32_t k, const float (&t)[C]) {
+  switch (k) {
+    GE_REG_CASE(0, vcopy(r[0], t)) GE_REG_CASE(1, vcopy(r[1], t)) GE_REG_CASE(2, vcopy(r[2], t))
+    GE_REG_CASE(3, vcopy(r[3], t)) GE_REG_CASE(4, vcopy(r[4], t)) GE_REG_CASE(5, vcopy(r[5], t))
+    GE_REG_CASE(6, vcopy(r[6], t)) GE_REG_CASE(7, vcopy(r[7], t))
+    default: break;
+  }
+}
+#undef GE_REG_CASE
+
+// R: program registers the kernel holds (kRegs for programs that need more
+// than 4)
+template <int C, int R, class Mem>
+__device__ __forceinline__ void run_programR(const EpiProgram &P, const float (&acc)[C], const Mem &mem) {
+  static_assert(R <= kRegs, "program registers");
+  float r[R][C];
+#pragma unroll
+  for (int i = 0; i < R; ++i)
+#pragma unroll
+    for (int e = 0; e < C; ++e) r[i][e] = 0.f;
+
+#pragma unroll 1
+  for (int pc = 0; pc < P.n_ins; ++pc) {
+    const uint32_t w = P.ins[pc];
+    const uint32_t op = w & 0xFFu, dst = (w >> 8) & 0xFFu, src = (w >> 16) & 0xFFu, idx = w >> 24;
+    float t[C];
+    switch (src) {
+      case SRC_REG: reg_read(r, idx, t); break;
+      case SRC_ACC: vcopy(t, acc); break;
+      case SRC_AUX: GE_DISPATCH_DTYPE(P.tma_aux_dtype[idx], mem.template aux<DT_>(idx, t)); break;
+      case SRC_BCAST: GE_DISPATCH_DTYPE(P.bcast_dtype[idx], mem.template bcast<DT_>(idx, t)); break;
+      case SRC_CBCAST: GE_DISPATCH_DTYPE(P.cbcast_dtype[idx], mem.template cbcast<DT_>(idx, t)); break;
+      case SRC_SCALAR: {
+        const float s = P.scalars[idx];
+#pragma unroll
+        for (int e = 0; e < C; ++e) t[e] = s;
+      } break;
+      default:
+#pragma unroll
+        for (int e = 0; e < C; ++e) t[e] = 0.f;
+        break;
+    }
+    if (op == OP_STORE) {
+      GE_DISPATCH_DTYPE(P.out_dtype[dst], mem.template store<DT_>(dst, t));
+      continue;
+    }
+    // u: the destination register's value, updated in place
+    float u[C];
+    if (op != OP_MOV && !is_activation_op(op)) reg_read(r, dst, u);
+#define GE_EACH(EXPR)                                      \
+  {                                                        \
+    _Pragma("unroll") for (int e = 0; e < C; ++e) {        \
+      const float x = u[e];                                \
+      (void)x;                                             \
+      u[e] = (EXPR);                                       \
+    }                                                      \
+  }
+    switch (op) {
+      case OP_MOV: vcopy(u, t); break;
+      case OP_MUL: GE_EACH(__fmul_rn(x, t[e])) break;
+      case OP_ADD: GE_EACH(__fadd_rn(x, t[e])) break;
+      case OP_RELU: GE_EACH(x > 0.f ? x : 0.f) break;
+      case OP_SUB: GE_EACH(__fsub_rn(x, t[e])) break;
+      case OP_RSUB: GE_EACH(__fsub_rn(t[e], x)) break;
+      case OP_DIV: GE_EACH(__fdiv_rn(x, t[e])) break;
+      case OP_RDIV: GE_EACH(__fdiv_rn(t[e], x)) break;
+      case OP_MIN: GE_EACH(fminf(x, t[e])) break;
+      case OP_MAX: GE_EACH(fmaxf(x, t[e])) break;
+      case OP_LEAKY: GE_EACH(x > 0.f ? x : __fmul_rn(t[e], x)) break;
+      case OP_RLEAKY: GE_EACH(t[e] > 0.f ? t[e] : __fmul_rn(x, t[e])) break;
+      case OP_SIGMOID: vcopy(u, t); activation_vec<OP_SIGMOID>(u); break;
+      case OP_TANH: vcopy(u, t); activation_vec<OP_TANH>(u); break;
+      case OP_GELU: vcopy(u, t); activation_vec<OP_GELU>(u); break;
+      case OP_SILU: vcopy(u, t); activation_vec<OP_SILU>(u); break;
+      default: vcopy(u, t); activation_vec<OP_HARDSWISH>(u); break;
+    }
+#undef GE_EACH
+    reg_write(r, dst, u);
+  }
+}
+
 // ---------------------------------------------------- catalog (static) --
 template <class SP, int PC, int C, class Mem>
 __device__ __forceinline__ void run_static_from(float (&r)[kRegs][C], const float (&acc)[C],
@@ -480,12 +585,13 @@ __device__ __forceinline__ void run_static_from(float (&r)[kRegs][C], const floa
 // Epilogue selectors used as kernel template arguments.
 // kWarps: epilogue warps of the fused kernels built with the selector (the
 // unfused elementwise kernel ignores it).
-template <int W = 4>
+template <int W = 4, int R = 4>
 struct EpiInterpW {
   static constexpr int kWarps = W;
   template <int C, class Mem>
   __device__ __forceinline__ static void run(const EpiProgram &P, const float (&acc)[C], const Mem &mem) {
-    run_program<C>(P, acc, mem);
+    if constexpr (R == 4) run_program4<C>(P, acc, mem);
+    else run_programR<C, R>(P, acc, mem);
   }
 };
 using EpiInterp = EpiInterpW<4>;

@@ -10,17 +10,22 @@
 
 namespace ge {
 
-// epi < 0: the interpreter, else catalog entry epi; 4 or 8 epilogue warps
+// epi -1 / -2: the interpreter holding 4 / 8 program registers, else catalog
+// entry epi; 4 or 8 epilogue warps
 template <int CG, int BN, int MC, size_t... K>
 const void *pick_gemm_kernel(int epi, int warps, std::index_sequence<K...>) {
   static const void *const table4[] = {reinterpret_cast<const void *>(
       &gemm_epi_kernel<CG, BN, MC, EpiStatic<catalog::Prog<K>, 4>>)...};
   static const void *const table8[] = {reinterpret_cast<const void *>(
       &gemm_epi_kernel<CG, BN, MC, EpiStatic<catalog::Prog<K>, 8>>)...};
-  if (epi < 0)
-    return warps == 4   ? reinterpret_cast<const void *>(&gemm_epi_kernel<CG, BN, MC, EpiInterpW<4>>)
-           : warps == 8 ? reinterpret_cast<const void *>(&gemm_epi_kernel<CG, BN, MC, EpiInterpW<8>>)
+  if (epi == -1)
+    return warps == 4   ? reinterpret_cast<const void *>(&gemm_epi_kernel<CG, BN, MC, EpiInterpW<4, 4>>)
+           : warps == 8 ? reinterpret_cast<const void *>(&gemm_epi_kernel<CG, BN, MC, EpiInterpW<8, 4>>)
                         : nullptr;
+  if (epi == -2)
+    return warps == 4 ? reinterpret_cast<const void *>(&gemm_epi_kernel<CG, BN, MC, EpiInterpW<4, 8>>)
+                      : nullptr;
+  if (epi < 0) return nullptr;
   if (epi >= static_cast<int>(sizeof...(K))) return nullptr;
   return warps == 4 ? table4[epi] : warps == 8 ? table8[epi] : nullptr;
 }

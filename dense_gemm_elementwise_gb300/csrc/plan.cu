@@ -117,6 +117,15 @@ int match_catalog(const EpiProgram &P) {
   }
 }
 
+// Executor of a compiled program: its catalog entry (k >= 0) unless the
+// interpreter is forced, else the interpreter holding 4 (-1) or all kRegs
+// (-2) program registers.
+int pick_executor(const EpiProgram &P, bool force_interpreter) {
+  const int k = force_interpreter ? -1 : match_catalog(P);
+  if (k >= 0) return k;
+  return P.n_regs > 4 ? -2 : -1;
+}
+
 // accumulator-only program of the unfused path's GEMM: out 0 (fp32) = accum
 EpiProgram program_store_accum() { return catalog::Prog<0>::P; }
 
@@ -365,7 +374,9 @@ double est_cycles(const gemm_epi_plan *pl, int cg, int bn, int mc, int units) {
 int pick_epi_warps(const gemm_epi_plan *pl, int *warps) {
   const int w = pl->opt.epi_warps;
   if (w != 0 && w != 4 && w != 8) return GE_ERR_INVALID;
-  *warps = w ? w : 8;
+  // the 8-register interpreter holds twice the program registers: 4 warps
+  if (w == 8 && pl->epi == -2) return GE_ERR_UNSUPPORTED;
+  *warps = w ? w : (pl->epi == -2 ? 4 : 8);
   return GE_OK;
 }
 
@@ -648,8 +659,8 @@ int gemm_epi_plan_create_ex(gemm_epi_plan **plan, int64_t L, int64_t M, int64_t 
   if (st == GE_OK) {
     pl->prog_acc = program_store_accum();
     const bool interp = (pl->opt.debug_flags & GE_DEBUG_FORCE_INTERPRETER) != 0u;
-    pl->epi = interp ? -1 : match_catalog(pl->prog);
-    pl->epi_acc = interp ? -1 : match_catalog(pl->prog_acc);
+    pl->epi = pick_executor(pl->prog, interp);
+    pl->epi_acc = pick_executor(pl->prog_acc, interp);
     st = check_device(&pl->device, &pl->num_sms, &pl->max_smem);
   }
   if (st == GE_OK) {
@@ -1033,7 +1044,7 @@ int gemm_epi_grouped_plan_create(gemm_epi_plan **plan, int32_t n_problems,
   }
   if (st == GE_OK) {
     const bool interp = (pl->opt.debug_flags & GE_DEBUG_FORCE_INTERPRETER) != 0u;
-    pl->epi = interp ? -1 : match_catalog(pl->prog);
+    pl->epi = pick_executor(pl->prog, interp);
     st = check_device(&pl->device, &pl->num_sms, &pl->max_smem);
   }
   if (st == GE_OK) {

@@ -91,7 +91,9 @@ template <size_t... K>
 static const void *pick_ew(int epi, std::index_sequence<K...>) {
   static const void *const table[] = {reinterpret_cast<const void *>(
       &epilogue_elementwise_kernel<EpiStatic<catalog::Prog<K>>>)...};
-  if (epi < 0) return reinterpret_cast<const void *>(&epilogue_elementwise_kernel<EpiInterp>);
+  if (epi == -1) return reinterpret_cast<const void *>(&epilogue_elementwise_kernel<EpiInterpW<4, 4>>);
+  if (epi == -2) return reinterpret_cast<const void *>(&epilogue_elementwise_kernel<EpiInterpW<4, 8>>);
+  if (epi < 0) return nullptr;
   return epi < static_cast<int>(sizeof...(K)) ? table[epi] : nullptr;
 }
 

@@ -135,8 +135,10 @@ def test_activation_nodes():
     assert B.gemm_epi_validate(dt, B.make_dag(ok)) == B.GE_OK
 
 
-def test_program_register_limit():
-    """Five values live at once exceed the epilogue program's 4 registers."""
+def test_program_register_counts():
+    """Five values live at once: more than the 4 registers of the compact
+    interpreter, within the 8 the program may use (16 nodes cannot keep more
+    than 7 values live), so the DAG is accepted."""
     g = W.Dag()
     acc = g.accum()
     sc = g.scalar(0)
@@ -146,7 +148,7 @@ def test_program_register_limit():
         s = g.add(s, v)
     g.store(s, 0)
     dt = B.make_dtypes("f16", ["f16"] * 4, 1, ["f16"])
-    assert B.gemm_epi_validate(dt, B.make_dag(g.nodes)) == B.GE_ERR_UNSUPPORTED
+    assert B.gemm_epi_validate(dt, B.make_dag(g.nodes)) == B.GE_OK
     # the same sum accumulated as it goes needs only two
     g = W.Dag()
     sc = g.scalar(0)

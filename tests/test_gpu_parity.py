@@ -428,3 +428,30 @@ def test_eight_epilogue_warps_timeout_is_reported():
         B.gemm_epi_plan_destroy(plan)
     gpu, _ = _gpu.run_gpu(w, inputs, options=B.ge_options(epi_warps=8))
     _gpu.compare(w, gpu, _gpu.oracle_rows(w, inputs))
+
+
+def test_program_with_more_than_four_registers():
+    """Five values live at once: the interpreter variant with 8 program
+    registers (plan epi_variant -2, 4 epilogue warps), fused and unfused,
+    bit-exact on integer inputs."""
+    g = W.Dag()
+    acc = g.accum()
+    sc = g.scalar(0)
+    vals = [g.mul(acc, sc)] + [g.mul(g.load(i), sc) for i in range(4)]
+    s = vals[0]
+    for v in vals[1:]:
+        s = g.add(s, v)
+    g.store(s, 0)
+    w = W.Workload(name="five_live", L=2, M=200, N=264, K=136, ab="f16",
+                   aux=[("C%d" % i, "tensor", "f16") for i in range(4)], scalars=[("s", 2.0)],
+                   outs=[("D", "f16")], dag=g.nodes, dist="randint", seed=37, exact=True)
+    inputs = W.make_inputs(w)
+    gpu, info = _gpu.run_gpu(w, inputs)
+    assert info["epi_variant"] == -2 and info["epi_warps"] == 4 and info["n_regs"] == 5
+    _gpu.compare(w, gpu, _gpu.oracle_rows(w, inputs))
+    unf, _ = _gpu.run_gpu(w, inputs, unfused=True)
+    _gpu.bitwise_equal(gpu, unf)
+    with pytest.raises(B.GemmEpiError) as e:
+        B.gemm_epi_plan_create(w.L, w.M, w.N, w.K, _gpu.dtypes_of(w), B.make_dag(w.dag),
+                               B.ge_options(epi_warps=8))
+    assert e.value.status == B.GE_ERR_UNSUPPORTED
