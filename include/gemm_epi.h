@@ -220,7 +220,9 @@ int gemm_epi_validate(const ge_dtypes *dtypes, const ge_dag *dag);
  *   outs      n_out device pointers, each (L,M,N) of its output type
  * Errors: GE_ERR_INVALID (also for a grouped plan), _MISSING_ARG,
  * _MISALIGNED, _CUDA (launch failed).  A device-side timeout is reported
- * later by gemm_epi_last_error.  The unfused entry points below reject
+ * later by gemm_epi_last_error.  Tensor maps are encoded on the host when
+ * a pointer differs from the previous run's; a run with the same pointers
+ * only launches, so it can be captured into a CUDA graph.  The unfused entry points below reject
  * grouped plans the same way.
  */
 int gemm_epi_run(gemm_epi_plan *plan, const void *A, const void *B, const void *const *aux,

@@ -455,3 +455,40 @@ def test_program_with_more_than_four_registers():
         B.gemm_epi_plan_create(w.L, w.M, w.N, w.K, _gpu.dtypes_of(w), B.make_dag(w.dag),
                                B.ge_options(epi_warps=8))
     assert e.value.status == B.GE_ERR_UNSUPPORTED
+
+
+def test_run_captured_in_cuda_graph():
+    """gemm_epi_run only launches once its tensor maps are encoded (first
+    run), so it can be captured into a CUDA graph and replayed; replays give
+    the plain run's bits, including after the inputs change in place."""
+    w = small(W.CONFIGS[4], 2, 264, 520, 136)
+    inputs = W.make_inputs(w)
+    A, Bm, aux, sc = inputs
+    dev = torch.device("cuda")
+    Ad, Bd, auxd = A.to(dev), Bm.to(dev), [a.to(dev) for a in aux]
+    outs = [torch.empty(w.L, w.M, w.N, dtype=W.TORCH_DTYPE[dt], device=dev) for _, dt in w.outs]
+    plan = B.gemm_epi_plan_create(w.L, w.M, w.N, w.K, _gpu.dtypes_of(w), B.make_dag(w.dag))
+    s = torch.cuda.Stream()
+    try:
+        B.gemm_epi_run(plan, Ad, Bd, auxd, sc, outs, stream=s)
+        torch.cuda.synchronize()
+        plain = [o.clone() for o in outs]
+        call = B.prepare_run(plan, Ad, Bd, auxd, sc, outs, stream=s)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=s):
+            assert call() == B.GE_OK
+        for o in outs:
+            o.zero_()
+        for _ in range(3):
+            graph.replay()
+        torch.cuda.synchronize()
+        _gpu.bitwise_equal([o.cpu() for o in outs], [p.cpu() for p in plain])
+        # new values in the same buffers: the replay reads them
+        Ad.neg_()
+        graph.replay()
+        torch.cuda.synchronize()
+        assert B.gemm_epi_last_error(plan) == B.GE_OK
+        neg = (W.make_inputs(w)[0].neg(), Bm, aux, sc)
+        _gpu.compare(w, [o.cpu() for o in outs], _gpu.oracle_rows(w, neg))
+    finally:
+        B.gemm_epi_plan_destroy(plan)
