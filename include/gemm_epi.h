@@ -11,13 +11,15 @@
  * Aux, cells [2]-[5]) and "How the epilogue fusion API works" (the epilogue
  * as a DAG of AccFetch, Load, compute and Store nodes).  The node set here is
  * that figure's plus Scalar, row and column Broadcast (section "Row and
- * column broadcasts"), subtraction, division, minimum and maximum, and ReLU
+ * column broadcasts"), subtraction, division, minimum and maximum, ReLU
  * (section "Defining an epilogue via a Python function": supported
- * operations; "Custom Epilogue Example", section "Activation Functions").
+ * operations; "Custom Epilogue Example", section "Activation Functions") and
+ * the activation registry of the legacy interface (sigmoid, tanh, GELU,
+ * SiLU, hardswish, leaky ReLU).
  *
  * Conventions shared by every entry point
  * ---------------------------------------
- *  * Layouts are row-major and packed:
+ *  * Layouts are row-major and packed (other storage orders: ge_options):
  *      A      (L, M, K)   K contiguous
  *      B      (L, K, N)   N contiguous
  *      aux tensors and outputs (L, M, N), N contiguous
@@ -28,8 +30,9 @@
  *    operand must be a multiple of 16 bytes long ("Custom Epilogue Example",
  *    section "Constraints": contiguous dimensions 16-byte aligned).
  *  * The caller owns all device memory (A, B, aux, outputs, the unfused
- *    workspace).  A plan owns only host state; creating one allocates no
- *    device memory.  Plans are not thread-safe: use one plan per host thread.
+ *    workspace).  A batched plan owns only host state; creating one
+ *    allocates no device memory (grouped plans own their problem tables).
+ *    Plans are not thread-safe: use one plan per host thread.
  *  * `stream` is a cudaStream_t passed as void* (NULL = legacy default
  *    stream).  Runs are asynchronous on that stream; nothing synchronises.
  *  * The epilogue runs in fp32: every intermediate stays fp32 and only a
