@@ -2,16 +2,18 @@
 //
 // One CTA per SM (or one 2x1 cluster per SM pair with cta_group::2), looping
 // over output tiles in a static round-robin order.  Warp roles:
-//   warp 0      TMA producer: A (K-major) and B (N-major) k-blocks into an
+//   warp 0      TMA producer: A and B k-blocks (K-major or MN-major) into an
 //               S-stage shared-memory ring, full/empty mbarriers per stage.
 //   warp 1      TMEM allocator and MMA issuer: one thread issues
 //               tcgen05.mma (fp16/bf16 -> fp32) into one of two TMEM
 //               accumulators; tcgen05.commit frees ring stages and publishes
 //               finished accumulators.
-//   warps 2-5   epilogue: tcgen05.ld of 32-column steps, aux tensors staged
-//               per warp by TMA (prefetched ahead, across tiles), the epilogue
-//               program in fp32 (interpreted, or straight-line for catalog
-//               entries), rounding, TMA stores from swizzled staging.
+//   warps 2..   epilogue, 4 or 8 warps (Epi::kWarps; with 8, the two warps of
+//               a TMEM lane quarter take alternate 32-column steps):
+//               tcgen05.ld of 32-column steps, aux tensors staged per warp by
+//               TMA (prefetched ahead, across tiles), the epilogue program in
+//               fp32 (interpreted, or straight-line for catalog entries),
+//               rounding, TMA stores from staging boxes.
 // The two TMEM accumulators let the epilogue of tile i overlap the mainloop of
 // tile i+1.  Ragged M/N/K edges are handled by TMA: out-of-range loads read
 // zeros, out-of-range stores are dropped.
