@@ -63,7 +63,8 @@ class ge_options(ctypes.Structure):
                 ("raster_group", ctypes.c_int32), ("timeout_ms", ctypes.c_int32),
                 ("debug_flags", ctypes.c_uint32), ("cluster_n", ctypes.c_int32),
                 ("a_major", ctypes.c_int32), ("b_major", ctypes.c_int32),
-                ("cd_major", ctypes.c_int32), ("epi_warps", ctypes.c_int32)]
+                ("cd_major", ctypes.c_int32), ("epi_warps", ctypes.c_int32),
+                ("specialize", ctypes.c_int32)]
 
 
 class ge_problem(ctypes.Structure):

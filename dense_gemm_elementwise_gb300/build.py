@@ -17,7 +17,7 @@ CSRC = os.path.join(HERE, "csrc")
 OBJ = os.path.join(HERE, "_build")
 LIBDIR = os.path.join(HERE, "lib")
 LIB = os.path.join(LIBDIR, "libgemm_epi.so")
-UNITS = ["plan", "unfused", "k_cg1_n64", "k_cg1_n128", "k_cg1_n256", "k_cg2_n128", "k_cg2_n256",
+UNITS = ["plan", "unfused", "jit", "k_cg1_n64", "k_cg1_n128", "k_cg1_n256", "k_cg2_n128", "k_cg2_n256",
          "k_cg2_n256_mc2"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
@@ -68,7 +68,8 @@ def build(force: bool = False, verbose: bool = False) -> str:
         for _, log in results:
             sys.stderr.write(log)
     tmp = LIB + ".tmp.%d" % os.getpid()
-    cmd = [nvcc()] + ARCH + ["-shared", "-Xcompiler", "-fPIC", "-o", tmp] + [o for o, _ in results]
+    cmd = [nvcc()] + ARCH + ["-shared", "-Xcompiler", "-fPIC", "-o", tmp] + [o for o, _ in results] + \
+        ["-ldl"]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError("link failed:\n%s%s" % (r.stdout, r.stderr))

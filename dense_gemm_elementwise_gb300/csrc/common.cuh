@@ -2,10 +2,18 @@
 // the compiled epilogue program and the kernel parameter block.
 #pragma once
 
+#include "gemm_epi.h"
+
+#ifdef __CUDACC_RTC__
+// compiled at run time (kernels specialised for one epilogue program): the
+// tensor-map type with the driver header's size and alignment
+typedef struct CUtensorMap_st {
+  alignas(128) unsigned long long opaque[16];
+} CUtensorMap;
+#else
 #include <cuda.h>  // CUtensorMap (type only; the driver is reached through cudart)
 #include <stdint.h>
-
-#include "gemm_epi.h"
+#endif
 
 namespace ge {
 

@@ -22,7 +22,6 @@
 
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
-#include <stdint.h>
 
 #include "common.cuh"
 

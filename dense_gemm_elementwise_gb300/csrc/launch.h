@@ -8,6 +8,8 @@
 
 #include <cuda_runtime_api.h>
 
+#include <string>
+
 #include "common.cuh"
 
 namespace ge {
@@ -19,6 +21,12 @@ const void *gemm_kernel_cg1_n256(int epi, int warps);
 const void *gemm_kernel_cg2_n128(int epi, int warps);
 const void *gemm_kernel_cg2_n256(int epi, int warps);
 const void *gemm_kernel_cg2_n256_mc2(int epi, int warps);  // 4-CTA cluster, A multicast
+
+// a fused kernel compiled at run time for program P (nullptr, with the
+// compiler's log in *log, if the runtime compiler is missing or fails)
+const void *jit_gemm_kernel(const EpiProgram &P, int cg, int bn, int mc, int warps,
+                            std::string *log);
+bool jit_available();
 
 // unfused comparison path: elementwise epilogue over an fp32 accumulator
 const void *ew_kernel(int epi);

@@ -180,6 +180,7 @@ struct Layout {
   int cg = 0, bn = 0, stages = 0, aux_stages = 0, grid = 0, num_tiles = 0;
   int mc = 1;         // CTA pairs per cluster sharing A (multicast)
   int warps = 4;      // epilogue warps (4 or 8)
+  const void *fn = nullptr;  // the kernel (chosen by configure)
   int smem = 0;       // dynamic smem requested at launch
   int smem_used = 0;  // bytes the layout occupies
   int num_m_blk = 0, num_n_blk = 0, num_kb = 0, raster_group = 0;
@@ -270,7 +271,8 @@ struct gemm_epi_plan {
   int device = 0, num_sms = 0, max_smem = 0;
   uint32_t *status = nullptr;
   EpiProgram prog{}, prog_acc{};
-  int epi = -1, epi_acc = -1;  // catalog entries (-1: interpreter)
+  int epi = -1, epi_acc = -1;  // catalog entries (-1, -2: interpreter; -3: compiled at plan time)
+  int interp_epi = -1;          // the interpreter variant for this program (-1 or -2)
   Layout lay, lay_acc;
   KParams kp{}, kp_acc{};
   // pointers the cached tensor maps were encoded for
@@ -309,6 +311,12 @@ struct gemm_epi_plan {
 
 namespace {
 
+// epi code of a kernel compiled at plan time for the plan's own program
+constexpr int kEpiSpecialized = -3;
+// internal status: the runtime compiler failed (the plan falls back to the
+// interpreter); never returned through the ABI
+constexpr int GE_ERR_JIT = -100;
+
 const void *gemm_kernel(int cg, int bn, int mc, int epi, int warps) {
   if (mc == 2) return (cg == 2 && bn == 256) ? gemm_kernel_cg2_n256_mc2(epi, warps) : nullptr;
   if (cg == 1 && bn == 64) return gemm_kernel_cg1_n64(epi, warps);
@@ -317,6 +325,18 @@ const void *gemm_kernel(int cg, int bn, int mc, int epi, int warps) {
   if (cg == 2 && bn == 128) return gemm_kernel_cg2_n128(epi, warps);
   if (cg == 2 && bn == 256) return gemm_kernel_cg2_n256(epi, warps);
   return nullptr;
+}
+
+const void *resolve_kernel(gemm_epi_plan *pl, int cg, int bn, int mc, int epi, int warps,
+                           const EpiProgram *P) {
+  (void)pl;
+  if (epi != kEpiSpecialized) return gemm_kernel(cg, bn, mc, epi, warps);
+  std::string log;
+  const void *fn = jit_gemm_kernel(*P, cg, bn, mc, warps, &log);
+  if (!fn && log_enabled())
+    std::fprintf(stderr, "[gemm_epi] run-time compilation failed, using the interpreter: %s\n",
+                 log.c_str());
+  return fn;
 }
 
 cudaLaunchConfig_t launch_config(const Layout &Lo, cudaStream_t s, cudaLaunchAttribute *attr) {
@@ -339,7 +359,8 @@ cudaLaunchConfig_t launch_config(const Layout &Lo, cudaStream_t s, cudaLaunchAtt
 }
 
 cudaError_t launch_gemm(const Layout &Lo, int epi, const KParams &kp, cudaStream_t s) {
-  const void *fn = gemm_kernel(Lo.cg, Lo.bn, Lo.mc, epi, Lo.warps);
+  (void)epi;
+  const void *fn = Lo.fn;
   if (!fn) return cudaErrorInvalidDeviceFunction;
   cudaLaunchAttribute attr[1];
   cudaLaunchConfig_t cfg = launch_config(Lo, s, attr);
@@ -433,8 +454,10 @@ int configure(gemm_epi_plan *pl) {
     int sms = pl->num_sms;
     if (o.max_ctas) sms = std::min(sms, o.max_ctas);
     int units = std::max(1, sms / (cg * mc));
-    const void *fn = gemm_kernel(cg, bn, mc, Lo == &pl->lay ? pl->epi : pl->epi_acc, Lo->warps);
-    if (!fn) return GE_ERR_INVALID;
+    const void *fn = resolve_kernel(pl, cg, bn, mc, Lo == &pl->lay ? pl->epi : pl->epi_acc,
+                                    Lo->warps, Lo == &pl->lay ? &pl->prog : &pl->prog_acc);
+    if (!fn) return pl->epi == kEpiSpecialized && Lo == &pl->lay ? GE_ERR_JIT : GE_ERR_INVALID;
+    Lo->fn = fn;
     if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, Lo->smem) != cudaSuccess)
       return GE_ERR_CUDA;
     if (cg * mc > 1) {
@@ -614,7 +637,9 @@ void log_plan(const gemm_epi_plan *pl) {
                (long long)pl->L, (long long)pl->M, (long long)pl->N, (long long)pl->K, Lo.cg, Lo.mc,
                BM * Lo.cg, Lo.bn, BK, Lo.stages, Lo.aux_stages, Lo.grid, Lo.num_tiles, Lo.smem_used,
                pl->prog.n_ins, pl->prog.n_regs,
-               pl->epi >= 0 ? catalog::kEntries[pl->epi].name : "interpreter");
+               pl->epi >= 0                 ? catalog::kEntries[pl->epi].name
+               : pl->epi == kEpiSpecialized ? "compiled for this program"
+                                            : "interpreter");
 }
 
 }  // namespace
@@ -662,8 +687,11 @@ int gemm_epi_plan_create_ex(gemm_epi_plan **plan, int64_t L, int64_t M, int64_t 
     pl->prog_acc = program_store_accum();
     const bool interp = (pl->opt.debug_flags & GE_DEBUG_FORCE_INTERPRETER) != 0u;
     pl->epi = pick_executor(pl->prog, interp);
+    pl->interp_epi = pl->prog.n_regs > 4 ? -2 : -1;
     pl->epi_acc = pick_executor(pl->prog_acc, interp);
     st = check_device(&pl->device, &pl->num_sms, &pl->max_smem);
+    if (st == GE_OK && pl->epi < 0 && !interp && pl->opt.specialize >= 0 && jit_available())
+      pl->epi = kEpiSpecialized;
   }
   if (st == GE_OK) {
     void *sym = nullptr;
@@ -671,6 +699,10 @@ int gemm_epi_plan_create_ex(gemm_epi_plan **plan, int64_t L, int64_t M, int64_t 
     pl->status = static_cast<uint32_t *>(sym);
   }
   if (st == GE_OK) st = configure(pl);
+  if (st == GE_ERR_JIT) {  // the runtime compiler failed: the interpreter
+    pl->epi = pl->interp_epi;
+    st = configure(pl);
+  }
   if (st == GE_OK && !encode_fn()) st = GE_ERR_CUDA;
   if (st != GE_OK) {
     cudaGetLastError();
@@ -796,7 +828,8 @@ int gemm_epi_run_unfused(gemm_epi_plan *pl, const void *A, const void *B, const 
   cfg.blockDim = dim3(kEwThreads);
   cfg.stream = s;
   void *args[] = {&ep};
-  e = cudaLaunchKernelExC(&cfg, ew_kernel(pl->epi), args);
+  e = cudaLaunchKernelExC(&cfg, ew_kernel(pl->epi == kEpiSpecialized ? pl->interp_epi : pl->epi),
+                         args);
   return e == cudaSuccess ? GE_OK : GE_ERR_CUDA;
 }
 
@@ -890,8 +923,9 @@ int configure_grouped(gemm_epi_plan *pl) {
   }
   if (tiles > (int64_t(1) << 24)) return GE_ERR_SHAPE;  // the tile table: 16 bytes a tile
   Lo.num_tiles = static_cast<int>(tiles);
-  const void *fn = gemm_kernel(cg, bn, 1, pl->epi, Lo.warps);
-  if (!fn) return GE_ERR_INVALID;
+  const void *fn = resolve_kernel(pl, cg, bn, 1, pl->epi, Lo.warps, &pl->prog);
+  if (!fn) return pl->epi == kEpiSpecialized ? GE_ERR_JIT : GE_ERR_INVALID;
+  Lo.fn = fn;
   if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, Lo.smem) != cudaSuccess)
     return GE_ERR_CUDA;
   int units = std::max(1, sms / cg);
@@ -1047,7 +1081,10 @@ int gemm_epi_grouped_plan_create(gemm_epi_plan **plan, int32_t n_problems,
   if (st == GE_OK) {
     const bool interp = (pl->opt.debug_flags & GE_DEBUG_FORCE_INTERPRETER) != 0u;
     pl->epi = pick_executor(pl->prog, interp);
+    pl->interp_epi = pl->prog.n_regs > 4 ? -2 : -1;
     st = check_device(&pl->device, &pl->num_sms, &pl->max_smem);
+    if (st == GE_OK && pl->epi < 0 && !interp && pl->opt.specialize >= 0 && jit_available())
+      pl->epi = kEpiSpecialized;
   }
   if (st == GE_OK) {
     void *sym = nullptr;
@@ -1055,6 +1092,10 @@ int gemm_epi_grouped_plan_create(gemm_epi_plan **plan, int32_t n_problems,
     pl->status = static_cast<uint32_t *>(sym);
   }
   if (st == GE_OK) st = configure_grouped(pl);
+  if (st == GE_ERR_JIT) {
+    pl->epi = pl->interp_epi;
+    st = configure_grouped(pl);
+  }
   if (st == GE_OK && !encode_fn()) st = GE_ERR_CUDA;
   if (st == GE_OK) {
     const size_t bytes = sizeof(GroupDesc) * size_t(kGroupSlots) * size_t(n_problems);

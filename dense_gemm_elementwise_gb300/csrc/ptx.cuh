@@ -3,8 +3,7 @@
 // Every wrapper is a single documented PTX instruction (PTX ISA 8.7+).
 #pragma once
 
-#include <cuda.h>
-#include <stdint.h>
+#include "common.cuh"
 
 namespace ge {
 

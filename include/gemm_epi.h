@@ -44,8 +44,20 @@
 #ifndef GEMM_EPI_H
 #define GEMM_EPI_H
 
+#ifdef __CUDACC_RTC__
+/* the library compiling its own kernels at run time: no C library headers */
+typedef signed char int8_t;
+typedef short int16_t;
+typedef int int32_t;
+typedef long long int64_t;
+typedef unsigned char uint8_t;
+typedef unsigned short uint16_t;
+typedef unsigned int uint32_t;
+typedef unsigned long long uint64_t;
+#else
 #include <stddef.h>
 #include <stdint.h>
+#endif
 
 #ifdef __cplusplus
 extern "C" {
@@ -147,6 +159,15 @@ typedef struct {
    * lane quarter) or 8 (two per quarter, each taking every other 32-column
    * step).  Results are identical either way; GE_ERR_INVALID otherwise.   */
   int32_t epi_warps;
+  /* 0 (default): an epilogue outside the built-in set gets a fused kernel
+   * compiled for its program when the plan is made (the built-in kernels'
+   * straight-line code; results identical to the interpreter's), if the CUDA
+   * runtime compiler (libnvrtc) can be loaded and the library's sources are
+   * next to it; otherwise, or if that compilation fails, the interpreter.
+   * A compiled kernel is kept for the life of the process; compiling takes
+   * about half a second.  -1: always the interpreter.  The unfused path
+   * always interprets.                                                    */
+  int32_t specialize;
 } ge_options;
 
 /* Test hook: the producer never loads the first k-block, so the MMA warp's
@@ -166,7 +187,9 @@ typedef struct {
   int32_t grid, num_tiles, smem_bytes;
   int32_t n_instr, n_regs;                    /* compiled epilogue program             */
   int32_t num_sms;
-  int32_t epi_variant;                        /* built-in epilogue used, -1: interpreter */
+  int32_t epi_variant;                        /* built-in epilogue used; -1, -2: interpreter
+                                                 (4 / 8 program registers); -3: compiled for
+                                                 this program when the plan was made        */
   int32_t cluster_n;                          /* CTA pairs sharing A per cluster         */
   int32_t epi_warps;                          /* epilogue warps per CTA (4 or 8)         */
 } ge_plan_info;

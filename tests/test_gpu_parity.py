@@ -256,7 +256,7 @@ def test_reversed_sub_div_and_min(variant):
     w = _reverse_ops_workload()
     inputs = W.make_inputs(w)
     gpu, info = _gpu.run_gpu(w, inputs, options=opts(variant))
-    assert info["epi_variant"] == -1  # not a catalog entry: the interpreter
+    assert info["epi_variant"] < 0  # not a built-in epilogue
     _gpu.compare(w, gpu, _gpu.oracle_rows(w, inputs))
     unf, _ = _gpu.run_gpu(w, inputs, unfused=True, options=opts(variant))
     _gpu.bitwise_equal(gpu, unf)
@@ -446,15 +446,19 @@ def test_program_with_more_than_four_registers():
                    aux=[("C%d" % i, "tensor", "f16") for i in range(4)], scalars=[("s", 2.0)],
                    outs=[("D", "f16")], dag=g.nodes, dist="randint", seed=37, exact=True)
     inputs = W.make_inputs(w)
-    gpu, info = _gpu.run_gpu(w, inputs)
+    gpu, info = _gpu.run_gpu(w, inputs, options=B.ge_options(specialize=-1))
     assert info["epi_variant"] == -2 and info["epi_warps"] == 4 and info["n_regs"] == 5
     _gpu.compare(w, gpu, _gpu.oracle_rows(w, inputs))
     unf, _ = _gpu.run_gpu(w, inputs, unfused=True)
     _gpu.bitwise_equal(gpu, unf)
     with pytest.raises(B.GemmEpiError) as e:
         B.gemm_epi_plan_create(w.L, w.M, w.N, w.K, _gpu.dtypes_of(w), B.make_dag(w.dag),
-                               B.ge_options(epi_warps=8))
+                               B.ge_options(epi_warps=8, specialize=-1))
     assert e.value.status == B.GE_ERR_UNSUPPORTED
+    # compiled for this program: all 8 registers in straight-line code, 8 warps
+    spec, info = _gpu.run_gpu(w, inputs)
+    assert info["epi_variant"] == -3 and info["epi_warps"] == 8
+    _gpu.bitwise_equal(gpu, spec)
 
 
 def test_run_captured_in_cuda_graph():
