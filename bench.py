@@ -25,6 +25,7 @@ Under torchrun (N > 1) every rank runs an independent replica on its own GPU
 (the problem has no exchange step); value = all ranks' FLOPs / max time.
 """
 import argparse
+import atexit
 import hashlib
 import json
 import os
@@ -97,52 +98,97 @@ def ncu_traffic(workload):
 # ------------------------------------------------------------ clocks ---
 
 class ClockSampler:
-    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    """nvidia-smi samples every 50 ms, each stamped with the tool's own
+    timestamp.  The sampler starts before the inputs are made, so the tool's
+    start-up (up to a second or two) is over well before the timed region;
+    window(t0, t1) keeps the samples taken between two time.time() marks.
+    Lines are read by a thread as they come (line-buffered through stdbuf
+    where it exists), so none are lost when the tool is stopped."""
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    REASONS = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
 
     def __init__(self, gpu_index):
         self.proc = None
         self.gpu = gpu_index
+        self.lines = []
+        self.thread = None
 
     def start(self):
+        import shutil
+        import threading
+        cmd = ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.FIELDS,
+               "--format=csv,noheader,nounits", "-lms", "50"]
+        if shutil.which("stdbuf"):
+            cmd = ["stdbuf", "-oL"] + cmd
         try:
-            self.proc = subprocess.Popen(
-                ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.FIELDS,
-                 "--format=csv,noheader,nounits", "-lms", "50"],
-                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
+                                         text=True)
         except OSError:
             self.proc = None
+            return self
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+        atexit.register(self.stop)  # never leave the tool running
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line))
 
     def stop(self):
-        if self.proc is None:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        if self.proc is None or self.proc.poll() is not None:
+            return
         self.proc.terminate()
         try:
-            out, _ = self.proc.communicate(timeout=5)
+            self.proc.wait(timeout=5)
         except subprocess.TimeoutExpired:
             self.proc.kill()
-            out, _ = self.proc.communicate()
-        sm, smax, power, reasons = [], [], [], set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for line in out.splitlines():
+            self.proc.wait()
+        self.thread.join(timeout=5)
+
+    def _samples(self):
+        import datetime
+        out = []
+        for received, line in list(self.lines):
             parts = [p.strip() for p in line.split(",")]
-            if len(parts) < 8:
+            if len(parts) < 9:
                 continue
             try:
-                sm.append(float(parts[0]))
-                smax.append(float(parts[1]))
-                power.append(float(parts[2]))
+                t = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+            except ValueError:
+                t = received  # unknown timestamp format: the time the line arrived
+            try:
+                sm, smax, pw = float(parts[1]), float(parts[2]), float(parts[3])
             except ValueError:
                 continue
-            for n, v in zip(names, parts[4:8]):
-                if v.lower().startswith("active"):
-                    reasons.add(n)
-        return {"sm_mhz": statistics.median(sm) if sm else None,
-                "sm_max_mhz": max(smax) if smax else None,
-                "reasons": sorted(reasons), "samples": len(sm),
-                "power_w_median": statistics.median(power) if power else None,
-                "power_w_max": max(power) if power else None}
+            active = [n for n, v in zip(self.REASONS, parts[5:9]) if v.lower().startswith("active")]
+            out.append((t, sm, smax, pw, active))
+        return out
+
+    def window(self, t0, t1):
+        """Statistics of the samples taken in [t0, t1] (wall clock).  A region
+        shorter than the sampling period may hold none: then the nearest
+        samples within 0.25 s of it are used, and "window" says so."""
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        samples = self._samples()
+        inside = [x for x in samples if t0 <= x[0] <= t1]
+        where = "timed region"
+        if not inside:
+            inside = [x for x in samples if t0 - 0.25 <= x[0] <= t1 + 0.25]
+            where = "timed region +- 0.25 s (no sample inside it)"
+        if not inside:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no nvidia-smi sample"],
+                    "samples": 0, "samples_total": len(samples)}
+        return {"sm_mhz": statistics.median(x[1] for x in inside),
+                "sm_max_mhz": max(x[2] for x in inside),
+                "reasons": sorted({r for x in inside for r in x[4]}),
+                "samples": len(inside), "window": where,
+                "window_s": round(t1 - t0, 3),
+                "power_w_median": statistics.median(x[3] for x in inside),
+                "power_w_max": max(x[3] for x in inside)}
 
 
 # ------------------------------------------------------------ helpers ---
@@ -254,6 +300,7 @@ def run_ours(args, w):
     torch.cuda.set_device(local)
     dev_ = torch.device("cuda", local)
     stream = torch.cuda.Stream(device=dev_)
+    clocks = ClockSampler(local).start()
     inputs = W.make_inputs(w)
     A, Bm, aux, scalars = inputs
     Ad, Bd = A.to(dev_), Bm.to(dev_)
@@ -304,11 +351,12 @@ def run_ours(args, w):
     torch.cuda.synchronize()
     if B.gemm_epi_last_error(plan) != B.GE_OK:
         raise RuntimeError("device-side timeout during warm-up")
-    clocks = ClockSampler(local)
-    clocks.start()
-    time.sleep(0.2)
+    t_begin = time.time()
     ms = timed(fused, args.steps)
-    clk = clocks.stop()
+    t_end = time.time()
+    time.sleep(0.1)  # the first sample after the region is in
+    clocks.stop()
+    clk = clocks.window(t_begin, t_end)
     ms_max = max_over_ranks(ms, world)
     if B.gemm_epi_last_error(plan) != B.GE_OK:
         raise RuntimeError("device-side timeout during the timed region")
@@ -485,6 +533,7 @@ def run_grouped(args, w):
     torch.cuda.set_device(local)
     dev_ = torch.device("cuda", local)
     stream = torch.cuda.Stream(device=dev_)
+    clocks = ClockSampler(local).start()
     inputs = W.make_grouped_inputs(w)
     As, Bs, auxs, scalars = inputs
     Ad = [a.to(dev_) for a in As]
@@ -541,11 +590,12 @@ def run_grouped(args, w):
     torch.cuda.synchronize()
     if B.gemm_epi_last_error(plan) != B.GE_OK:
         raise RuntimeError("device-side timeout during warm-up")
-    clocks = ClockSampler(local)
-    clocks.start()
-    time.sleep(0.2)
+    t_begin = time.time()
     ms = timed(grouped, args.steps)
-    clk = clocks.stop()
+    t_end = time.time()
+    time.sleep(0.1)
+    clocks.stop()
+    clk = clocks.window(t_begin, t_end)
     ms_max = max_over_ranks(ms, world)
     if B.gemm_epi_last_error(plan) != B.GE_OK:
         raise RuntimeError("device-side timeout during the timed region")

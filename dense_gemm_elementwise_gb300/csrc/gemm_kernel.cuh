@@ -392,10 +392,18 @@ __global__ void __launch_bounds__(threads_for(Epi::kWarps), 1)
       // per-k step advance and strides of the two operands' smem descriptors:
       // K-major tiles are 128-byte rows (k step 32 bytes, 8-row groups 1 KiB
       // apart), MN-major tiles are 64-element atoms 8 KiB apart whose k rows
-      // are 128 bytes (k step 16 rows = 2 KiB)
+      // are 128 bytes (k step 16 rows = 2 KiB).  The descriptors of stage 0 are
+      // built once; a stage or k step only moves the start address, whose
+      // field (address >> 4, bits 0-13) is added to directly: shared-memory
+      // addresses stay below 256 KiB, so the sum never carries out of it.
+      // This keeps the issuing thread to a few adds per MMA, well ahead of
+      // the tensor pipe.
       const uint32_t a_step = p.a_mn ? 2048u : 32u, a_lbo = p.a_mn ? 8192u : 16u;
       const uint32_t b_step = p.b_k ? 32u : 2048u, b_lbo = p.b_k ? 16u : p.b_lbo;
       const uint32_t b_sbo = p.b_k ? 1024u : p.b_sbo;
+      const uint64_t a_desc0 = smem_desc_sw128(sb + p.off_A, a_lbo, 1024u);
+      const uint64_t b_desc0 = smem_desc_sw128(sb + p.off_B, b_lbo, b_sbo);
+      const uint32_t a_k16 = a_step >> 4, b_k16 = b_step >> 4;
       int stage = 0;
       uint32_t phase = 0;
       int abuf = 0;
@@ -416,14 +424,11 @@ __global__ void __launch_bounds__(threads_for(Epi::kWarps), 1)
             break;
           }
           tc_fence_after();
-          const uint32_t sa = sb + p.off_A + stage * T::kABytes;
-          const uint32_t sbb = sb + p.off_B + stage * T::kBBytes;
+          const uint64_t ad = a_desc0 + static_cast<uint32_t>(stage * (T::kABytes >> 4));
+          const uint64_t bd = b_desc0 + static_cast<uint32_t>(stage * (T::kBBytes >> 4));
 #pragma unroll
-          for (int k = 0; k < BK / UMMA_K; ++k) {
-            const uint64_t ad = smem_desc_sw128(sa + a_step * k, a_lbo, 1024u);
-            const uint64_t bd = smem_desc_sw128(sbb + b_step * k, b_lbo, b_sbo);
-            umma_f16<CG>(d, ad, bd, id, (kb | k) != 0 ? 1u : 0u);
-          }
+          for (int k = 0; k < BK / UMMA_K; ++k)
+            umma_f16<CG>(d, ad + a_k16 * k, bd + b_k16 * k, id, (kb | k) != 0 ? 1u : 0u);
           umma_commit<CG>(bar + kBarEmpty + 8 * stage, kAllMask);
           if (++stage == p.stages) {
             stage = 0;

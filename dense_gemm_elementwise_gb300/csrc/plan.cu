@@ -370,8 +370,8 @@ cudaError_t launch_gemm(const Layout &Lo, int epi, const KParams &kp, cudaStream
 
 // Rough cost model in SM clocks: waves x per-tile mainloop, where a k-block
 // costs the larger of its tensor-core time (2*BN clocks for 128 x BN x 64 at
-// 8192 flop/clk/SM; the pipe's measured rate is ~15 % lower for every tile
-// shape, which leaves the ranking unchanged) and its operand fill time at
+// 8192 flop/clk/SM, the rate the pipe sustains when fed back to back) and
+// its operand fill time at
 // ~48 B/clk/SM of L2 bandwidth when every SM is busy (measured: per-SM
 // throughput drops by a third from 38 to 152 active SMs with 32 KiB per
 // k-block).  With A multicast (mc = 2)
