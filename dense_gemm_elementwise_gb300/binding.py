@@ -18,6 +18,7 @@ GE_F16, GE_BF16, GE_F32 = 0, 1, 2
 GE_MAX_NODES, GE_MAX_AUX, GE_MAX_TMA_AUX, GE_MAX_OUT, GE_MAX_SCALARS = 16, 8, 4, 4, 16
 GE_DEBUG_SKIP_FIRST_LOAD = 1
 GE_DEBUG_FORCE_INTERPRETER = 2
+GE_DEBUG_NO_TAIL_SPLIT = 4
 GE_ROW_MAJOR, GE_COL_MAJOR = 0, 1
 
 STATUS = ["GE_OK", "GE_ERR_NO_ACCUM", "GE_ERR_NO_D", "GE_ERR_SSA", "GE_ERR_MISSING_ARG",

@@ -134,12 +134,15 @@ struct KParams {
   int32_t L, M, N, K;
   int32_t ab_bf16;                     // A/B are bf16 (else fp16)
   int32_t num_m_blk, num_n_blk, num_tiles, num_kb;
+  int32_t num_full;  // tiles [0, num_full) are full width; each later pair of
+                     // tiles is the two column halves of one split tile
   int32_t raster_group;
   int32_t stages, aux_stages;
   uint32_t off_A, off_B, off_aux, off_out, off_bar;  // byte offsets in dynamic smem
   uint32_t aux_stage_bytes, out_stage_bytes;          // one epilogue warp, one stage
   uint32_t aux_off[GE_MAX_TMA_AUX], out_off[GE_MAX_OUT];
   uint32_t tx_bytes;      // bytes one k-block stage receives (both CTAs of a pair)
+  uint32_t tx_bytes_half; // the same for a half-width tile
   uint32_t aux_tx_bytes;  // bytes one epilogue warp's aux stage receives
   uint32_t b_lbo, b_sbo;  // B smem descriptor strides (bytes)
   uint64_t timeout_ns;

@@ -89,10 +89,12 @@ __device__ __forceinline__ void tile_coords(int num_m_blk, int num_n_blk, int G,
   nb = rr / gsize;
 }
 
-// A tile of the launch: its batch and block coordinates, its k-block count and,
-// for a grouped GEMM, the problem it belongs to.
+// A tile of the launch: its batch and block coordinates, its k-block count,
+// which column half it covers if it is half of a split tile and, for a
+// grouped GEMM, the problem it belongs to.
 struct TileRef {
   int l, mb, nb, num_kb;
+  int half;             // -1: the whole BN columns; 0 / 1: the first / second BN/2
   const GroupDesc *gd;  // nullptr: the batched problem described by KParams
 };
 
@@ -100,8 +102,17 @@ struct TileRef {
 // for a grouped one.
 __device__ __forceinline__ TileRef locate(const KParams &p, int t) {
   TileRef r;
+  r.half = -1;
   if (p.groups == nullptr) {
-    tile_coords(p.num_m_blk, p.num_n_blk, p.raster_group, t, r.l, r.mb, r.nb);
+    // tiles past num_full come in pairs: the two column halves of full tile
+    // num_full + (t - num_full) / 2 (the last wave, split so that twice as
+    // many CTAs share it)
+    int tt = t;
+    if (t >= p.num_full) {
+      tt = p.num_full + ((t - p.num_full) >> 1);
+      r.half = (t - p.num_full) & 1;
+    }
+    tile_coords(p.num_m_blk, p.num_n_blk, p.raster_group, tt, r.l, r.mb, r.nb);
     r.num_kb = p.num_kb;
     r.gd = nullptr;
   } else {
@@ -293,7 +304,12 @@ __global__ void __launch_bounds__(threads_for(Epi::kWarps), 1)
           ready_gd = tr.gd;
         }
         const int m0 = mb * T::kMmaM + static_cast<int>(rank) * BM;
-        const int n0 = nb * BN + static_cast<int>(rank) * T::kBnLocal;
+        // a half tile: BN/2 columns, BN/(2 CG) of them (half the B atoms) per CTA
+        const bool half = tr.half >= 0;
+        const int n0 = nb * BN + (tr.half > 0 ? BN / 2 : 0) +
+                       static_cast<int>(rank) * (half ? T::kBnLocal / 2 : T::kBnLocal);
+        const int b_atoms = half ? T::kBAtoms / 2 : T::kBAtoms;
+        const uint32_t tx = half ? p.tx_bytes_half : p.tx_bytes;
         for (int kb = 0; kb < tr.num_kb; ++kb) {
           if (!wt.wait(bar + kBarEmpty + 8 * stage, phase ^ 1u, SITE_PRODUCER_EMPTY)) {
             ok = false;
@@ -308,7 +324,7 @@ __global__ void __launch_bounds__(threads_for(Epi::kWarps), 1)
             const uint32_t sbb = sb + p.off_B + stage * T::kBBytes;
             if constexpr (CG == 2) {
               const uint32_t fb = mapa_shared(fb_local, leader);
-              if (rank == 0) mbar_arrive_expect_tx(fb_local, p.tx_bytes);
+              if (rank == 0) mbar_arrive_expect_tx(fb_local, tx);
               if constexpr (MC == 1) {
                 if (p.a_mn) {  // two 64-row atoms of the M-major A tile
                   tma_load_3d_pair(sa, mA, fb, m0, kb * BK, l);
@@ -330,10 +346,10 @@ __global__ void __launch_bounds__(threads_for(Epi::kWarps), 1)
               } else {
 #pragma unroll
                 for (int j = 0; j < T::kBAtoms; ++j)
-                  tma_load_3d_pair(sbb + j * 8192, mB, fb, n0 + 64 * j, kb * BK, l);
+                  if (j < b_atoms) tma_load_3d_pair(sbb + j * 8192, mB, fb, n0 + 64 * j, kb * BK, l);
               }
             } else {
-              mbar_arrive_expect_tx(fb_local, p.tx_bytes);
+              mbar_arrive_expect_tx(fb_local, tx);
               if (p.a_mn) {
                 tma_load_3d(sa, mA, fb_local, m0, kb * BK, l);
                 tma_load_3d(sa + 8192, mA, fb_local, m0 + 64, kb * BK, l);
@@ -345,7 +361,7 @@ __global__ void __launch_bounds__(threads_for(Epi::kWarps), 1)
               } else {
 #pragma unroll
                 for (int j = 0; j < T::kBAtoms; ++j)
-                  tma_load_3d(sbb + j * 8192, mB, fb_local, n0 + 64 * j, kb * BK, l);
+                  if (j < b_atoms) tma_load_3d(sbb + j * 8192, mB, fb_local, n0 + 64 * j, kb * BK, l);
               }
             }
           }
@@ -389,6 +405,7 @@ __global__ void __launch_bounds__(threads_for(Epi::kWarps), 1)
     // ------------------------------------------------------- MMA issuer --
     if (lane == 0 && rank == 0) {
       const uint32_t id = make_idesc_f16(p.ab_bf16 != 0, T::kMmaM, BN, p.a_mn != 0, p.b_k == 0);
+      const uint32_t id_half = make_idesc_f16(p.ab_bf16 != 0, T::kMmaM, BN / 2, p.a_mn != 0, p.b_k == 0);
       // per-k step advance and strides of the two operands' smem descriptors:
       // K-major tiles are 128-byte rows (k step 32 bytes, 8-row groups 1 KiB
       // apart), MN-major tiles are 64-element atoms 8 KiB apart whose k rows
@@ -411,7 +428,9 @@ __global__ void __launch_bounds__(threads_for(Epi::kWarps), 1)
       bool ok = true;
       TileCursor tc(p, unit, n_units, my_tiles);
       for (int i = 0; ok && i < my_tiles; ++i) {
-        const int num_kb = tc.next().num_kb;
+        const TileRef tr = tc.next();
+        const int num_kb = tr.num_kb;
+        const uint32_t idt = tr.half < 0 ? id : id_half;
         if (!wt.wait<CG == 2>(bar + kBarTmemEmpty + 8 * abuf, aphase ^ 1u, SITE_MMA_TMEM_EMPTY)) {
           ok = false;
           break;
@@ -428,7 +447,7 @@ __global__ void __launch_bounds__(threads_for(Epi::kWarps), 1)
           const uint64_t bd = b_desc0 + static_cast<uint32_t>(stage * (T::kBBytes >> 4));
 #pragma unroll
           for (int k = 0; k < BK / UMMA_K; ++k)
-            umma_f16<CG>(d, ad + a_k16 * k, bd + b_k16 * k, id, (kb | k) != 0 ? 1u : 0u);
+            umma_f16<CG>(d, ad + a_k16 * k, bd + b_k16 * k, idt, (kb | k) != 0 ? 1u : 0u);
           umma_commit<CG>(bar + kBarEmpty + 8 * stage, kAllMask);
           if (++stage == p.stages) {
             stage = 0;
@@ -461,6 +480,9 @@ __global__ void __launch_bounds__(threads_for(Epi::kWarps), 1)
     const int ch = e / 4;    // which of the quarter's warps: takes steps ch, ch + kSplit, ...
     constexpr int kStepsW = T::kSteps / kSplit;  // this warp's steps per tile
     static_assert(T::kSteps % kSplit == 0, "steps split evenly between a quarter's warps");
+    // a half tile has half the steps (the host splits tiles only where that
+    // is a whole, nonzero number per warp)
+    constexpr int kHalfW = kStepsW / 2 > 0 ? kStepsW / 2 : 1;
     const uint32_t tq = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
     uint8_t *aux_w = smem + p.off_aux + e * p.aux_stages * p.aux_stage_bytes;
     constexpr int kOutBufs = out_bufs_for(kEpiWarps);
@@ -468,7 +490,10 @@ __global__ void __launch_bounds__(threads_for(Epi::kWarps), 1)
     const uint32_t auxbar_w = bar_aux + 8u * e * kMaxAuxStages;
     const bool has_aux = p.prog.n_tma_aux > 0;
     const int SA = p.aux_stages;
-    const int total = my_tiles * kStepsW;
+    // this CTA's full tiles come first, then its half tiles
+    const int q_full = unit < p.num_full ? min((p.num_full - 1 - unit) / n_units + 1, my_tiles) : 0;
+    const int full_steps = q_full * kStepsW;
+    const int total = full_steps + (my_tiles - q_full) * kHalfW;
     int issued = 0, g = 0, abuf = 0, obuf = 0;
     uint32_t aphase = 0;
     bool ok = true;
@@ -480,12 +505,13 @@ __global__ void __launch_bounds__(threads_for(Epi::kWarps), 1)
 
     // TMA loads of every Load tensor for this warp's 32 rows of step gi
     auto issue_aux = [&](int gi) {
-      const int ii = gi / kStepsW;
+      const int ii = gi < full_steps ? gi / kStepsW : q_full + (gi - full_steps) / kHalfW;
+      const int first = ii <= q_full ? ii * kStepsW : full_steps + (ii - q_full) * kHalfW;
       if (ii != pf_tile) {
         const TileRef tr = pf_tc.next();  // tiles are entered in order, one at a time
         pf_l = tr.l;
         pf_tile = ii;
-        pf_x0 = (tr.nb * MC + pair) * BN;
+        pf_x0 = (tr.nb * MC + pair) * BN + (tr.half > 0 ? BN / 2 : 0);
         pf_y = tr.mb * T::kMmaM + static_cast<int>(rank) * BM + q * 32;
         if (tr.gd && pf_maps != tr.gd->tmAux)
           for (int a = 0; a < p.prog.n_tma_aux; ++a) {
@@ -499,7 +525,7 @@ __global__ void __launch_bounds__(threads_for(Epi::kWarps), 1)
       uint8_t *dst = aux_w + as * p.aux_stage_bytes;
       fence_proxy_async_smem();
       mbar_arrive_expect_tx(ab, p.aux_tx_bytes);
-      const int x = pf_x0 + ((gi - ii * kStepsW) * kSplit + ch) * EW;
+      const int x = pf_x0 + ((gi - first) * kSplit + ch) * EW;
       for (int a = 0; a < p.prog.n_tma_aux; ++a)
         tma_load_3d(smem_u32(dst + p.aux_off[a]), &pf_maps[a], ab, p.cd_m ? pf_y : x,
                     p.cd_m ? x : pf_y, pf_l);
@@ -509,7 +535,8 @@ __global__ void __launch_bounds__(threads_for(Epi::kWarps), 1)
       const TileRef tr = tc.next();
       const int l = tr.l, mb = tr.mb, nb = tr.nb * MC + pair;
       const int m0 = mb * T::kMmaM + static_cast<int>(rank) * BM + q * 32;
-      const int n0 = nb * BN;
+      const int n0 = nb * BN + (tr.half > 0 ? BN / 2 : 0);
+      const int steps = tr.half < 0 ? T::kSteps : T::kSteps / 2;  // 32-column steps of this tile
       const CUtensorMap *out_maps = tr.gd ? tr.gd->tmOut : p.tmOut;
       const void *const *bptr = tr.gd ? tr.gd->bcast_ptr : p.bcast_ptr;
       const void *const *cptr = tr.gd ? tr.gd->cbcast_ptr : p.cbcast_ptr;
@@ -540,7 +567,7 @@ __global__ void __launch_bounds__(threads_for(Epi::kWarps), 1)
         }
       }
       tc_fence_after();
-      for (int s = ch; s < T::kSteps; s += kSplit, ++g) {
+      for (int s = ch; s < steps; s += kSplit, ++g) {
         if (has_aux && lane == 0) {
           while (issued < total && issued < g + SA) issue_aux(issued++);
         }
@@ -550,7 +577,7 @@ __global__ void __launch_bounds__(threads_for(Epi::kWarps), 1)
         tmem_ld16(tq + col, acc0);
         tmem_ld16(tq + col + CH, acc1);
         tmem_wait_ld();
-        if (s + kSplit >= T::kSteps) {
+        if (s + kSplit >= steps) {
           // accumulator fully read: hand it back to the MMA warp
           tc_fence_before();
           __syncwarp();

@@ -184,6 +184,7 @@ struct Layout {
   int smem = 0;       // dynamic smem requested at launch
   int smem_used = 0;  // bytes the layout occupies
   int num_m_blk = 0, num_n_blk = 0, num_kb = 0, raster_group = 0;
+  int num_full = 0;   // tiles launched full width (the rest: halves of split tiles)
   uint32_t off_A = 0, off_B = 0, off_aux = 0, off_out = 0, off_bar = 0;
   uint32_t aux_stage_bytes = 0, out_stage_bytes = 0;
   uint32_t aux_off[GE_MAX_TMA_AUX] = {}, out_off[GE_MAX_OUT] = {};
@@ -368,6 +369,18 @@ cudaError_t launch_gemm(const Layout &Lo, int epi, const KParams &kp, cudaStream
   return cudaLaunchKernelExC(&cfg, fn, args);
 }
 
+// Whether the last wave of `tiles` full tiles on `units` CTAs (pairs) is split
+// into half-width tiles: when it would leave at least half of them idle, its
+// r tiles become 2r halves (one per CTA at most), so the wave takes about
+// half as long.  Needs whole 32-column epilogue steps per warp in a half
+// (BN >= 128), whole 64-column B atoms per CTA in a half (BN / cg >= 128, or
+// K-major B, which loads whole boxes), and no A multicast (whose cluster
+// shares a tile's A rows between pairs).
+bool split_tail(int64_t tiles, int64_t units, int cg, int bn, int mc, bool b_k) {
+  const int64_t r = tiles % units;
+  return r > 0 && 2 * r <= units && mc == 1 && bn >= 128 && (b_k || bn / cg >= 128);
+}
+
 // Rough cost model in SM clocks: waves x per-tile mainloop, where a k-block
 // costs the larger of its tensor-core time (2*BN clocks for 128 x BN x 64 at
 // 8192 flop/clk/SM, the rate the pipe sustains when fed back to back) and
@@ -384,7 +397,9 @@ double est_cycles(const gemm_epi_plan *pl, int cg, int bn, int mc, int units) {
   const double mma = 2.0 * bn;
   const double fill = double((BM / mc + bn / cg) * BK * 2) / 48.0;
   const double per_tile = kb * std::max(mma, fill);
-  const int64_t waves = (tiles + units - 1) / units;
+  const bool split = (pl->opt.debug_flags & GE_DEBUG_NO_TAIL_SPLIT) == 0u &&
+                     split_tail(tiles, units, cg, bn, mc, pl->b_k != 0);
+  const double waves = split ? double(tiles / units) + 0.5 : double((tiles + units - 1) / units);
   return waves * per_tile + (bn / CH) * 300.0;
 }
 
@@ -469,7 +484,14 @@ int configure(gemm_epi_plan *pl) {
         units = std::min(units, clusters);
       cudaGetLastError();
     }
-    units = static_cast<int>(std::min<int64_t>(units, tiles));
+    Lo->num_full = Lo->num_tiles;
+    if ((o.debug_flags & GE_DEBUG_NO_TAIL_SPLIT) == 0u &&
+        split_tail(tiles, units, cg, bn, mc, pl->b_k != 0)) {
+      const int64_t r = tiles % units;
+      Lo->num_full = static_cast<int>(tiles - r);
+      Lo->num_tiles = static_cast<int>(tiles + r);
+    }
+    units = static_cast<int>(std::min<int64_t>(units, Lo->num_tiles));
     Lo->grid = units * cg * mc;
   }
   return GE_OK;
@@ -487,6 +509,7 @@ void fill_params(const gemm_epi_plan *pl, const Layout &Lo, const EpiProgram &P,
   kp->num_m_blk = Lo.num_m_blk;
   kp->num_n_blk = Lo.num_n_blk;
   kp->num_tiles = Lo.num_tiles;
+  kp->num_full = Lo.num_full;
   kp->num_kb = Lo.num_kb;
   kp->raster_group = Lo.raster_group;
   kp->stages = Lo.stages;
@@ -501,6 +524,10 @@ void fill_params(const gemm_epi_plan *pl, const Layout &Lo, const EpiProgram &P,
   for (int i = 0; i < GE_MAX_TMA_AUX; ++i) kp->aux_off[i] = Lo.aux_off[i];
   for (int i = 0; i < GE_MAX_OUT; ++i) kp->out_off[i] = Lo.out_off[i];
   kp->tx_bytes = Lo.tx_bytes;
+  // a half tile: half the B bytes per CTA (N-major B), or the same whole
+  // boxes (K-major B)
+  const uint32_t b_bytes = static_cast<uint32_t>(Lo.bn / std::max(Lo.cg, 1)) * BK * 2;
+  kp->tx_bytes_half = pl->b_k ? Lo.tx_bytes : Lo.tx_bytes - static_cast<uint32_t>(Lo.cg) * (b_bytes / 2);
   kp->aux_tx_bytes = Lo.aux_tx_bytes;
   // B tile in shared memory: 64-column (128-byte) swizzle atoms of 64 k-rows
   // (8 KiB apart), 8-row groups 1 KiB apart
@@ -923,6 +950,7 @@ int configure_grouped(gemm_epi_plan *pl) {
   }
   if (tiles > (int64_t(1) << 24)) return GE_ERR_SHAPE;  // the tile table: 16 bytes a tile
   Lo.num_tiles = static_cast<int>(tiles);
+  Lo.num_full = Lo.num_tiles;  // grouped tiles are never split
   const void *fn = resolve_kernel(pl, cg, bn, 1, pl->epi, Lo.warps, &pl->prog);
   if (!fn) return pl->epi == kEpiSpecialized ? GE_ERR_JIT : GE_ERR_INVALID;
   Lo.fn = fn;

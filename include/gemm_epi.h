@@ -180,6 +180,13 @@ typedef struct {
  * used to test that the two executors agree. */
 #define GE_DEBUG_FORCE_INTERPRETER 2u
 
+/* Keep every tile of a batched launch full width.  By default, when the last
+ * wave of tiles would leave at least half of the CTAs (pairs) idle, each of
+ * its tiles is split into two half-width tiles; results are identical either
+ * way (each output element's sum runs over K in the same order), so tests
+ * compare the two schedules. */
+#define GE_DEBUG_NO_TAIL_SPLIT 4u
+
 /* What a plan chose (for logs, tests and the benchmark). */
 typedef struct {
   int32_t cta_group, tile_m, tile_n, tile_k;  /* tile_m/tile_n: output tile of one MMA */
