@@ -496,3 +496,21 @@ def test_run_captured_in_cuda_graph():
         _gpu.compare(w, [o.cpu() for o in outs], _gpu.oracle_rows(w, neg))
     finally:
         B.gemm_epi_plan_destroy(plan)
+
+
+def test_epilogue_warps_follow_the_mainloop_length():
+    """Compiled epilogues take 4 warps when 4 warps' epilogue of a tile fits
+    in half of its mainloop (long K), else 8; the option overrides."""
+    def warps(w, **opt):
+        plan = B.gemm_epi_plan_create(w.L, w.M, w.N, w.K, _gpu.dtypes_of(w), B.make_dag(w.dag),
+                                      B.ge_options(**opt) if opt else None)
+        try:
+            return B.gemm_epi_plan_info(plan)["epi_warps"]
+        finally:
+            B.gemm_epi_plan_destroy(plan)
+    cfg4, cfg5 = W.CONFIGS[3], W.CONFIGS[4]
+    assert warps(cfg4) == 4                                   # K = 8192: 128 k-blocks a tile
+    assert warps(dataclasses.replace(cfg4, K=1024)) == 8      # 16 k-blocks a tile
+    assert warps(cfg5) == 8                                   # K = 2048, three epilogue tensors
+    assert warps(cfg4, epi_warps=8) == 8
+    assert warps(cfg4, debug_flags=B.GE_DEBUG_FORCE_INTERPRETER) == 8
