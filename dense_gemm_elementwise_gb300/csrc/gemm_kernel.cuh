@@ -16,7 +16,9 @@
 //               rounding, TMA stores from staging boxes.
 // The two TMEM accumulators let the epilogue of tile i overlap the mainloop of
 // tile i+1.  Ragged M/N/K edges are handled by TMA: out-of-range loads read
-// zeros, out-of-range stores are dropped.
+// zeros, out-of-range stores are dropped.  When the host splits the last wave
+// (KParams::num_full), each of its tiles runs as two half-width tiles: MMA N
+// = BN/2, half of each CTA's B atoms, half of the epilogue steps.
 //
 // A grouped launch (KParams::groups set) runs many problems of different
 // sizes: tile t is looked up in a per-tile table (problem, m/n block, k

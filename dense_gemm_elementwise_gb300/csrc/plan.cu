@@ -389,14 +389,18 @@ bool split_tail(int64_t tiles, int64_t units, int cg, int bn, int mc, bool b_k) 
 // throughput drops by a third from 38 to 152 active SMs with 32 KiB per
 // k-block).  With A multicast (mc = 2)
 // a CTA fetches only half of its A rows.
+double est_kblock_cycles(int cg, int bn, int mc) {
+  const double mma = 2.0 * bn;
+  const double fill = double((BM / mc + bn / cg) * BK * 2) / 48.0;
+  return std::max(mma, fill);
+}
+
 double est_cycles(const gemm_epi_plan *pl, int cg, int bn, int mc, int units) {
   const int64_t mt = (pl->M + BM * cg - 1) / (BM * cg);
   const int64_t nt = (pl->N + int64_t(bn) * mc - 1) / (int64_t(bn) * mc);
   const int64_t tiles = pl->L * mt * nt;
   const int64_t kb = (pl->K + BK - 1) / BK;
-  const double mma = 2.0 * bn;
-  const double fill = double((BM / mc + bn / cg) * BK * 2) / 48.0;
-  const double per_tile = kb * std::max(mma, fill);
+  const double per_tile = kb * est_kblock_cycles(cg, bn, mc);
   const bool split = (pl->opt.debug_flags & GE_DEBUG_NO_TAIL_SPLIT) == 0u &&
                      split_tail(tiles, units, cg, bn, mc, pl->b_k != 0);
   const double waves = split ? double(tiles / units) + 0.5 : double((tiles + units - 1) / units);
@@ -474,8 +478,7 @@ int configure(gemm_epi_plan *pl) {
 
   int warps = 0;
   const int64_t kb = (pl->K + BK - 1) / BK;
-  const double per_kb = std::max(2.0 * bn, double((BM / mc + bn / cg) * BK * 2) / 48.0);
-  int st = pick_epi_warps(pl, &warps, bn, double(kb) * per_kb);
+  int st = pick_epi_warps(pl, &warps, bn, double(kb) * est_kblock_cycles(cg, bn, mc));
   if (st != GE_OK) return st;
   st = make_layout(&pl->lay, cg, bn, o.stages, pl->prog, pl->max_smem, 4, 5, warps);
   if (st != GE_OK) return st;
