@@ -253,6 +253,22 @@ def cpu_baseline(w, inputs, target_s=10.0):
                       % (rows, w.L * w.M, w.N, w.K, t)}
 
 
+def workload_config(w, world):
+    """The workload's identity: the same keys in both arms' lines."""
+    return {"workload": w.name, "L": w.L, "M": w.M, "N": w.N, "K": w.K,
+            "ab_dtype": w.ab, "acc_dtype": "f32", "epilogue_dtype": "f32",
+            "outs": [n + ":" + dt for n, dt in w.outs],
+            "parallelism": "replicas" if world > 1 else "single"}
+
+
+def grouped_config(w, world):
+    return {"workload": w.name, "problems": len(w.problems), "ab_dtype": w.ab,
+            "acc_dtype": "f32", "epilogue_dtype": "f32",
+            "outs": [n + ":" + dt for n, dt in w.outs],
+            "flops_per_step": w.flops(), "alg_bytes_per_step": w.alg_bytes(),
+            "parallelism": "replicas" if world > 1 else "single"}
+
+
 # ------------------------------------------------------- reference arm ---
 
 def run_reference(args, w):
@@ -283,7 +299,7 @@ def run_reference(args, w):
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "f64", "data": "synthetic",
-            "config": {"workload": w.name, "L": w.L, "M": w.M, "N": w.N, "K": w.K},
+            "config": workload_config(w, args.gpus),
             "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads,
                              "kind": "oracle", "sample": sample},
             "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
@@ -465,15 +481,12 @@ def run_ours(args, w):
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_max,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "f16", "data": "synthetic",
-        "config": {"workload": w.name, "L": w.L, "M": w.M, "N": w.N, "K": w.K,
-                   "ab_dtype": w.ab, "acc_dtype": "f32", "epilogue_dtype": "f32",
-                   "outs": [n + ":" + dt for n, dt in w.outs],
-                   "l2": ("flushed before every timed step: 512 MiB write, then 256 MiB read "
-                          "(inputs %d MiB)" % (in_bytes >> 20) if flush_l2 else
-                          "no flush: inputs (%d MiB) larger than twice the L2" % (in_bytes >> 20)),
-                   "plan": info, "options": args.opt or "auto",
-                   "parallelism": "replicas" if world > 1 else "single"},
+        "dtype": w.ab, "data": "synthetic",
+        "config": dict(workload_config(w, world), **{
+            "l2": ("flushed before every timed step: 512 MiB write, then 256 MiB read "
+                   "(inputs %d MiB)" % (in_bytes >> 20) if flush_l2 else
+                   "no flush: inputs (%d MiB) larger than twice the L2" % (in_bytes >> 20)),
+            "plan": info, "options": args.opt or "auto"}),
         "pct_of_peak": 100.0 * achieved / peak,
         "roofline": roofline, "gpu_launches": args.steps, "clocks": clk,
         "unfused": unfused, "e2e": e2e, "cpu_baseline": cpu,
@@ -517,7 +530,7 @@ def run_grouped_reference(args, w):
         "impl": "reference", "metric": GROUPED_METRIC, "value": value, "unit": "TFLOP/s",
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-        "data": "synthetic", "config": {"workload": w.name, "problems": len(w.problems)},
+        "data": "synthetic", "config": grouped_config(w, args.gpus),
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
@@ -681,12 +694,9 @@ def run_grouped(args, w):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_max,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": w.ab, "data": "synthetic",
-        "config": {"workload": w.name, "problems": len(w.problems),
-                   "flops_per_step": flops, "alg_bytes_per_step": w.alg_bytes(),
-                   "l2": "flushed before every timed step: 512 MiB write, then 256 MiB read",
-                   "plan": info,
-                   "options": args.opt or "auto",
-                   "parallelism": "replicas" if world > 1 else "single"},
+        "config": dict(grouped_config(w, world), **{
+            "l2": "flushed before every timed step: 512 MiB write, then 256 MiB read",
+            "plan": info, "options": args.opt or "auto"}),
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                      "frac": achieved / peak, "traffic": None,
                      "peak_source": "%s bf16 dense burst" % pk_src},
