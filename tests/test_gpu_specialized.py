@@ -76,3 +76,17 @@ def test_plan_time_compilation_is_cached():
     finally:
         B.gemm_epi_plan_destroy(p1)
         B.gemm_epi_plan_destroy(p2)
+
+
+def test_specialized_four_warps_at_long_k():
+    """A long-K problem puts a compiled epilogue on 4 warps: the compiled
+    kernel is then the 4-warp instance, still bit-identical to the
+    interpreter and exact against the oracle."""
+    w = dataclasses.replace(EXAMPLES["relu_aux_store"], L=1, M=256, N=264, K=8192)
+    inputs = W.make_inputs(w)
+    spec, info = _gpu.run_gpu(w, inputs)
+    assert info["epi_variant"] == -3 and info["epi_warps"] == 4, info
+    interp, info2 = _gpu.run_gpu(w, inputs, options=B.ge_options(specialize=-1))
+    assert info2["epi_variant"] in (-1, -2)
+    _gpu.bitwise_equal(spec, interp)
+    _gpu.compare(w, spec, _gpu.oracle_rows(w, inputs))
