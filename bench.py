@@ -42,7 +42,7 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 METRIC = "fused GEMM+epilogue TFLOP/s and % of GB300 dense FP16 peak (1 GPU)"
-DEFAULT_WORKLOAD = "cfg4_alpha_beta_x_8192"
+DEFAULT_WORKLOAD = "alpha_beta_x_8192"
 L2_BYTES = 129 * 1000 * 1000  # GB300 L2
 FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0}
 

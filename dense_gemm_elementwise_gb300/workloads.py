@@ -318,25 +318,27 @@ def my_epilogue(L, M, N, K, seed=2025, name=None):
         cite="CUTLASS Operator API: Custom epilogue fusions for GEMMs, cells [2]-[5]")
 
 
-CONFIGS = [
-    my_epilogue(1, 128, 128, 128, name="cfg1_my_epilogue_128"),
-    my_epilogue(1, 1024, 1024, 1024, name="cfg2_my_epilogue_1024"),
+# The five workloads of the pages' examples (shapes, types, seeds and epilogues
+# as the workload table states them).
+WORKLOADS = [
+    my_epilogue(1, 128, 128, 128, name="my_epilogue_128"),
+    my_epilogue(1, 1024, 1024, 1024, name="my_epilogue_1024"),
     Workload(
-        name="cfg3_relu_2400x3232x4096", L=1, M=2400, N=3232, K=4096, ab="f16",
+        name="relu_2400x3232x4096", L=1, M=2400, N=3232, K=4096, ab="f16",
         aux=[("C", "tensor", "f16")], scalars=[("alpha", 1.0), ("beta", 2.0)],
         outs=[("D", "f16")], dag=dag_relu_linear(), dist="ceil_uniform", seed=1234,
         exact=True,
         cite="CUTLASS Python examples walkthrough: basic GEMM notebook (2400x3232x4096, "
              "beta=2) and epilogue notebook (fused ReLU)"),
     Workload(
-        name="cfg4_alpha_beta_x_8192", L=1, M=8192, N=8192, K=8192, ab="f16",
+        name="alpha_beta_x_8192", L=1, M=8192, N=8192, K=8192, ab="f16",
         aux=[("C", "tensor", "f16"), ("X", "tensor", "f16")],
         scalars=[("alpha", 2.0), ("beta", 1.0), ("x_factor", 3.0)],
         outs=[("D", "f16"), ("Y", "f16")], dag=dag_alpha_beta_x(), dist="normal", seed=2026,
         exact=False, sample_rows=64,
         cite="Custom Epilogue Example: Basic Example: Alpha-Beta Scaling; Running the Example"),
     Workload(
-        name="cfg5_bias_relu_square_L8", L=8, M=4096, N=4096, K=2048, ab="bf16",
+        name="bias_relu_square_8x4096x4096x2048", L=8, M=4096, N=4096, K=2048, ab="bf16",
         aux=[("C", "tensor", "bf16"), ("bias", "row", "f32")],
         scalars=[("alpha", 0.5), ("beta", 1.0)],
         outs=[("D", "bf16"), ("E", "bf16")], dag=dag_bias_relu_square(), dist="normal",
@@ -345,7 +347,10 @@ CONFIGS = [
              "Activation Functions, Multiple Outputs"),
 ]
 
-BY_NAME = {w.name: w for w in CONFIGS}
+MY_EPILOGUE_128, MY_EPILOGUE_1024, RELU_2400X3232X4096, ALPHA_BETA_X_8192, BIAS_RELU_SQUARE_L8 = \
+    WORKLOADS
+
+BY_NAME = {w.name: w for w in WORKLOADS}
 
 # Tolerance for the non-integer workloads: |gpu - ref| <= ATOL + RTOL*|ref|,
 # ref being the oracle's value rounded to the output type.

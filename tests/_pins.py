@@ -315,7 +315,7 @@ def _int_inputs(w):
 def pin_integer_closed_form(L_):
     """Integer inputs: the exact integer result, as the basic-GEMM notebook
     asserts (assert_array_equal(D, alpha*(A@B) + beta*C))."""
-    w = small(W.CONFIGS[0], L=2, M=24, N=40, K=56)
+    w = small(W.MY_EPILOGUE_128, L=2, M=24, N=40, K=56)
     (A, B, aux, sc), Ai, Bi, (Ci,) = _int_inputs(w)
     acc = np.einsum("lik,lkj->lij", Ai, Bi)  # exact int64
     aux_ref = 1 * acc + 2 * Ci
@@ -323,7 +323,7 @@ def pin_integer_closed_form(L_):
     assert np.array_equal(np_decode(Aux, "f16"), aux_ref.reshape(-1, w.N).astype(np.float64))
     assert np.array_equal(np_decode(D, "f16"), 0.5 * aux_ref.reshape(-1, w.N))
     # ceil(uniform(-4, 4)) inputs and the fused ReLU: D = max(A@B + 2*C, 0)
-    w3 = small(W.CONFIGS[2], L=2, M=20, N=24, K=72)
+    w3 = small(W.RELU_2400X3232X4096, L=2, M=20, N=24, K=72)
     (A, B, aux, sc), Ai, Bi, (Ci,) = _int_inputs(w3)
     ref = np.maximum(np.einsum("lik,lkj->lij", Ai, Bi) + 2 * Ci, 0).reshape(-1, w3.N)
     (D,), _ = run_oracle(L_, w3, A, B, aux, sc)
@@ -460,7 +460,7 @@ def pin_grouped_closed_form(L_):
 def pin_broadcast_closed_form(L_):
     """Row-broadcast bias indexed by column j, same vector for every row and
     batch: integer inputs, D = relu(0.5*A@B + C + bias), E = D*D rounded."""
-    w = small(W.CONFIGS[4], L=3, M=6, N=16, K=8, dist="randint")
+    w = small(W.BIAS_RELU_SQUARE_L8, L=3, M=6, N=16, K=8, dist="randint")
     (A, B, aux, sc), Ai, Bi, (Ci, biasi) = _int_inputs(w)
     acc = np.einsum("lik,lkj->lij", Ai, Bi)
     d = np.maximum(0.5 * acc + Ci + biasi[None, None, :], 0.0).reshape(-1, w.N)
@@ -510,14 +510,14 @@ def _exact_case(L_, w, rs):
 
 def pin_fraction_brute_force(L_):
     rs = np.random.RandomState(5)
-    cases = list(W.CONFIGS[1:]) + W.page_examples()
+    cases = list(W.WORKLOADS[1:]) + W.page_examples()
     for w in cases:
         _exact_case(L_, small(w, L=2, M=3, N=5, K=7), rs)
 
 
 def pin_special_cases(L_):
     # A = 0: accum = 0, so Aux = beta*C and D = extra_scalar*beta*C
-    w = small(W.CONFIGS[0], L=1, M=8, N=16, K=24)
+    w = small(W.MY_EPILOGUE_128, L=1, M=8, N=16, K=24)
     A, B, aux, sc = W.make_inputs(w)
     A = A * 0
     (D, Aux), _ = run_oracle(L_, w, A, B, aux, sc)
@@ -527,7 +527,7 @@ def pin_special_cases(L_):
     # B = identity (K = N): accum = A exactly; Y is A's codes and D rounds
     # 2A + C + 3X (exact in fp64 for fp16 operands) once
     import torch
-    w4 = small(W.CONFIGS[3], L=2, M=8, N=16, K=16)
+    w4 = small(W.ALPHA_BETA_X_8192, L=2, M=8, N=16, K=16)
     A, B, aux, sc = W.make_inputs(w4)
     B = torch.eye(16, dtype=torch.float16).expand(2, 16, 16).contiguous()
     (D, Y), _ = run_oracle(L_, w4, A, B, aux, sc)
@@ -541,7 +541,7 @@ def pin_relu_positive_zero(L_):
     """ReLU of a non-positive value is +0 ("where(d > 0, d, 0)"), including
     ReLU of -0: with negative scalars, a zero row of A and a zero row of C
     make alpha*accum + beta*C = (-0) + (-0) = -0 there."""
-    w = small(W.CONFIGS[2], L=1, M=16, N=16, K=16)
+    w = small(W.RELU_2400X3232X4096, L=1, M=16, N=16, K=16)
     A, B, aux, sc = W.make_inputs(w)
     A[0, 0, :] = 0
     aux[0][0, 0, :] = 0
@@ -561,7 +561,7 @@ def pin_relu_positive_zero(L_):
 def pin_rows_and_threads(L_):
     """A row subset equals the same rows of the full result; thread count
     does not change any bit."""
-    w = small(W.CONFIGS[3], L=2, M=12, N=24, K=40)
+    w = small(W.ALPHA_BETA_X_8192, L=2, M=12, N=24, K=40)
     A, B, aux, sc = W.make_inputs(w)
     full, _ = run_oracle(L_, w, A, B, aux, sc, threads=1)
     rows = np.array([0, 5, 11, 12, 23], dtype=np.int64)

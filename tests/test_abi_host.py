@@ -44,13 +44,13 @@ def _dt(w):
     return B.make_dtypes(w.ab, [s[2] for s in w.aux], len(w.scalars), [dt for _, dt in w.outs])
 
 
-@pytest.mark.parametrize("w", W.CONFIGS + W.page_examples(), ids=lambda w: w.name)
+@pytest.mark.parametrize("w", W.WORKLOADS + W.page_examples(), ids=lambda w: w.name)
 def test_workload_dags_validate(w):
     assert B.gemm_epi_validate(_dt(w), B.make_dag(w.dag)) == B.GE_OK
 
 
 def _base():
-    w = W.CONFIGS[0]
+    w = W.MY_EPILOGUE_128
     return _dt(w), list(w.dag)
 
 

@@ -198,7 +198,7 @@ def test_grouped_argument_errors():
         assert B.gemm_epi_unfused_workspace_bytes(G.plan) == 0
     finally:
         G.close()
-    wb = W.CONFIGS[0]
+    wb = W.MY_EPILOGUE_128
     plan = B.gemm_epi_plan_create(wb.L, wb.M, wb.N, wb.K, _gpu.dtypes_of(wb), B.make_dag(wb.dag))
     try:
         st = B.gemm_epi_grouped_run(plan, G.As, G.Bs, G.auxs, G.scalars, G.outs, check=False)

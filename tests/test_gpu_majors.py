@@ -52,13 +52,13 @@ def run_majors(w, inputs, majors, unfused=False, **opt):
     return [(o.transpose(-1, -2) if cd_major else o).contiguous().cpu() for o in outs]
 
 
-BASE = dataclasses.replace(W.CONFIGS[0], L=2, M=264, N=392, K=200, sample_rows=None)
+BASE = dataclasses.replace(W.MY_EPILOGUE_128, L=2, M=264, N=392, K=200, sample_rows=None)
 
 
 @pytest.mark.parametrize("majors", MAJORS, ids=mid)
 @pytest.mark.parametrize("variant", [(1, 128), (2, 256)], ids=lambda v: "cg%d_n%d" % v)
 def test_majors_exact(majors, variant):
-    """Integer inputs, the Aux/D epilogue of cfg1: bit-exact for every
+    """Integer inputs, the Aux/D epilogue of my_epilogue: bit-exact for every
     combination of majors, on a ragged shape spanning several tiles."""
     w = BASE
     inputs = W.make_inputs(w)
@@ -77,7 +77,7 @@ def test_majors_unfused_and_broadcasts(majors):
     unf = run_majors(w, inputs, majors, unfused=True)
     _gpu.bitwise_equal(fused, unf)
     _gpu.compare(w, fused, _gpu.oracle_rows(w, inputs))
-    w5 = dataclasses.replace(W.CONFIGS[4], L=2, M=200, N=264, K=136, dist="randint",
+    w5 = dataclasses.replace(W.BIAS_RELU_SQUARE_L8, L=2, M=200, N=264, K=136, dist="randint",
                              sample_rows=None)
     inputs = W.make_inputs(w5)
     fused = run_majors(w5, inputs, majors, cta_group=2, tile_n=256)
@@ -89,7 +89,7 @@ def test_majors_unfused_and_broadcasts(majors):
 def test_majors_normal_inputs_full_tiles():
     """N(0,1) inputs through the alpha-beta-x epilogue, column-major
     everything, several full 256x256 tiles: within the fp32 tolerance."""
-    w = dataclasses.replace(W.CONFIGS[3], L=1, M=1024, N=768, K=512, sample_rows=None)
+    w = dataclasses.replace(W.ALPHA_BETA_X_8192, L=1, M=1024, N=768, K=512, sample_rows=None)
     inputs = W.make_inputs(w)
     gpu = run_majors(w, inputs, (1, 1, 1))
     _gpu.compare(w, gpu, _gpu.oracle_rows(w, inputs))

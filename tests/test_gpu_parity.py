@@ -18,11 +18,12 @@ def small(w, L, M, N, K, **kw):
 
 # --------------------------------------------------- the five workloads --
 
-@pytest.mark.parametrize("w", W.CONFIGS, ids=lambda w: w.name)
+@pytest.mark.parametrize("w", W.WORKLOADS, ids=lambda w: w.name)
 def test_workload_parity(w):
-    """cfg1-3 on every element; cfg4/5 (the full 8192^3 and L=8 sizes, in the
-    launch configuration the benchmark times) on 64 seeded rows per batch,
-    including each batch's first and last row."""
+    """The three integer workloads on every element; the two N(0,1) ones
+    (the full 8192^3 and L=8 sizes, in the launch configuration the
+    benchmark times) on 64 seeded rows per batch, including each batch's
+    first and last row."""
     inputs = W.make_inputs(w)
     gpu, info = _gpu.run_gpu(w, inputs)
     rows = None if w.sample_rows is None else W.sample_rows(w)
@@ -31,7 +32,7 @@ def test_workload_parity(w):
 
 
 def test_plan_choices_for_headline_sizes():
-    w = W.BY_NAME["cfg4_alpha_beta_x_8192"]
+    w = W.BY_NAME["alpha_beta_x_8192"]
     plan = B.gemm_epi_plan_create(w.L, w.M, w.N, w.K, _gpu.dtypes_of(w), B.make_dag(w.dag))
     try:
         info = B.gemm_epi_plan_info(plan)
@@ -72,7 +73,7 @@ def test_ragged_shapes_exact(shape, variant):
     """Integer inputs: every kernel variant must be bit-exact on ragged M, N,
     K (TMA zero-fills loads and clips stores at the edges; with multicast an
     odd number of N tiles leaves the second pair's tile out of range)."""
-    w = small(W.CONFIGS[0], *shape)
+    w = small(W.MY_EPILOGUE_128, *shape)
     inputs = W.make_inputs(w)
     gpu, info = _gpu.run_gpu(w, inputs, options=opts(variant))
     assert (info["cta_group"], info["tile_n"], info["cluster_n"]) == variant
@@ -81,7 +82,7 @@ def test_ragged_shapes_exact(shape, variant):
 
 @pytest.mark.parametrize("variant", VARIANTS, ids=vid)
 def test_bf16_bias_relu_square_variants(variant):
-    w = small(W.CONFIGS[4], 2, 384, 520, 264)
+    w = small(W.BIAS_RELU_SQUARE_L8, 2, 384, 520, 264)
     inputs = W.make_inputs(w)
     gpu, _ = _gpu.run_gpu(w, inputs, options=opts(variant))
     _gpu.compare(w, gpu, _gpu.oracle_rows(w, inputs))
@@ -91,7 +92,7 @@ def test_bf16_bias_relu_square_variants(variant):
 @pytest.mark.parametrize("cluster_n", [1, 2])
 def test_few_stages(stages, cluster_n):
     """Short rings wrap the stage/phase bookkeeping many times per tile."""
-    w = small(W.CONFIGS[3], 1, 512, 1024, 1024)
+    w = small(W.ALPHA_BETA_X_8192, 1, 512, 1024, 1024)
     inputs = W.make_inputs(w)
     gpu, info = _gpu.run_gpu(w, inputs, options=B.ge_options(
         stages=stages, cta_group=2, tile_n=256, cluster_n=cluster_n))
@@ -103,7 +104,7 @@ def test_few_stages(stages, cluster_n):
 def test_small_grid_many_tiles_per_cta(cluster_n):
     """Four CTAs loop over many tiles: both TMEM accumulators, the aux
     prefetch across tile boundaries and the raster order all wrap."""
-    w = small(W.CONFIGS[3], 2, 1024, 768, 256)
+    w = small(W.ALPHA_BETA_X_8192, 2, 1024, 768, 256)
     inputs = W.make_inputs(w)
     gpu, info = _gpu.run_gpu(w, inputs, options=B.ge_options(
         max_ctas=4, raster_group=3, cta_group=2, tile_n=256, cluster_n=cluster_n))
@@ -113,8 +114,8 @@ def test_small_grid_many_tiles_per_cta(cluster_n):
 
 # ------------------------------------------------------------ unfused --
 
-@pytest.mark.parametrize("w", [W.CONFIGS[1], small(W.CONFIGS[4], 2, 256, 392, 520),
-                               small(W.CONFIGS[3], 1, 300, 264, 200)], ids=lambda w: w.name)
+@pytest.mark.parametrize("w", [W.MY_EPILOGUE_1024, small(W.BIAS_RELU_SQUARE_L8, 2, 256, 392, 520),
+                               small(W.ALPHA_BETA_X_8192, 1, 300, 264, 200)], ids=lambda w: w.name)
 def test_unfused_matches_fused_bitwise(w):
     """Same compiled program on the same fp32 accumulator: identical bits."""
     inputs = W.make_inputs(w)
@@ -125,7 +126,7 @@ def test_unfused_matches_fused_bitwise(w):
 
 
 def test_variants_agree_on_normal_inputs():
-    w = small(W.CONFIGS[3], 1, 512, 512, 2048)
+    w = small(W.ALPHA_BETA_X_8192, 1, 512, 512, 2048)
     inputs = W.make_inputs(w)
     base, _ = _gpu.run_gpu(w, inputs, options=opts(VARIANTS[4]))
     for v in VARIANTS[:4] + VARIANTS[5:]:
@@ -135,7 +136,7 @@ def test_variants_agree_on_normal_inputs():
 
 
 def test_repeated_runs_and_side_stream():
-    w = small(W.CONFIGS[0], 1, 384, 256, 512)
+    w = small(W.MY_EPILOGUE_128, 1, 384, 256, 512)
     inputs = W.make_inputs(w)
     s = torch.cuda.Stream()
     gpu, _ = _gpu.run_gpu(w, inputs, stream=s, repeat=3)
@@ -145,7 +146,7 @@ def test_repeated_runs_and_side_stream():
 # ------------------------------------------------------ error behaviour --
 
 def test_run_argument_errors():
-    w = small(W.CONFIGS[0], 1, 128, 128, 128)
+    w = small(W.MY_EPILOGUE_128, 1, 128, 128, 128)
     A, Bm, aux, sc = [x for x in W.make_inputs(w)]
     dev = torch.device("cuda")
     Ad, Bd, Cd = A.cuda(), Bm.cuda(), aux[0].cuda()
@@ -176,7 +177,7 @@ def test_device_wait_timeout_is_reported(cluster_n):
     """A k-block that is never loaded: the MMA warp's bounded wait runs out,
     the kernel records GE_ERR_TIMEOUT, drains and exits; the context stays
     usable and the next run is correct."""
-    w = small(W.CONFIGS[0], 1, 256, 256, 256)
+    w = small(W.MY_EPILOGUE_128, 1, 256, 256, 256)
     inputs = W.make_inputs(w)
     opt = B.ge_options(timeout_ms=50, debug_flags=B.GE_DEBUG_SKIP_FIRST_LOAD,
                        max_ctas=2 * cluster_n, cta_group=2, tile_n=256, cluster_n=cluster_n)
@@ -198,7 +199,7 @@ def test_device_wait_timeout_is_reported(cluster_n):
 # ------------------------------------------ catalog vs interpreter --
 
 def test_headline_workloads_use_builtin_epilogues():
-    for w in W.CONFIGS:
+    for w in W.WORKLOADS:
         plan = B.gemm_epi_plan_create(w.L, w.M, w.N, w.K, _gpu.dtypes_of(w), B.make_dag(w.dag))
         try:
             info = B.gemm_epi_plan_info(plan)
@@ -207,8 +208,8 @@ def test_headline_workloads_use_builtin_epilogues():
         assert info["epi_variant"] >= 0, w.name
 
 
-CATALOG_CASES = [small(W.CONFIGS[0], 2, 300, 392, 200), small(W.CONFIGS[2], 1, 264, 520, 136),
-                 small(W.CONFIGS[3], 1, 384, 264, 520), small(W.CONFIGS[4], 3, 200, 264, 200)] + \
+CATALOG_CASES = [small(W.MY_EPILOGUE_128, 2, 300, 392, 200), small(W.RELU_2400X3232X4096, 1, 264, 520, 136),
+                 small(W.ALPHA_BETA_X_8192, 1, 384, 264, 520), small(W.BIAS_RELU_SQUARE_L8, 3, 200, 264, 200)] + \
     [small(w, 2, 136, 264, 72) for w in W.page_examples()]
 
 
@@ -368,7 +369,7 @@ def test_leaky_relu_forms(w, variant):
 
 # ------------------------------------------------ eight epilogue warps --
 
-@pytest.mark.parametrize("w", CATALOG_CASES[:4] + [small(W.CONFIGS[4], 2, 264, 520, 136)] +
+@pytest.mark.parametrize("w", CATALOG_CASES[:4] + [small(W.BIAS_RELU_SQUARE_L8, 2, 264, 520, 136)] +
                          [x for x in CATALOG_CASES if x.name in ("complex_gelu_tanh",
                                                                   "row_col_bias_f16")],
                          ids=lambda w: w.name)
@@ -387,14 +388,14 @@ def test_eight_epilogue_warps_bitwise(w, variant):
 
 
 def test_eight_epilogue_warps_rules():
-    w = small(W.CONFIGS[0], 1, 256, 256, 256)
+    w = small(W.MY_EPILOGUE_128, 1, 256, 256, 256)
     dt, dag = _gpu.dtypes_of(w), B.make_dag(w.dag)
     with pytest.raises(B.GemmEpiError) as e:
         B.gemm_epi_plan_create(1, 256, 256, 256, dt, dag, B.ge_options(epi_warps=6))
     assert e.value.status == B.GE_ERR_INVALID
 
 
-@pytest.mark.parametrize("w", [small(W.CONFIGS[4], 2, 264, 520, 136)] +
+@pytest.mark.parametrize("w", [small(W.BIAS_RELU_SQUARE_L8, 2, 264, 520, 136)] +
                          [x for x in CATALOG_CASES if x.name in ("act_sigmoid", "clamp_f16",
                                                                   "aux_normalize_f16")],
                          ids=lambda w: w.name)
@@ -413,7 +414,7 @@ def test_interpreter_eight_warps_bitwise(w, variant):
 
 
 def test_eight_epilogue_warps_timeout_is_reported():
-    w = small(W.CONFIGS[0], 1, 256, 256, 256)
+    w = small(W.MY_EPILOGUE_128, 1, 256, 256, 256)
     inputs = W.make_inputs(w)
     A, Bm, aux, sc = inputs
     opt = B.ge_options(timeout_ms=50, debug_flags=B.GE_DEBUG_SKIP_FIRST_LOAD, max_ctas=2,
@@ -465,7 +466,7 @@ def test_run_captured_in_cuda_graph():
     """gemm_epi_run only launches once its tensor maps are encoded (first
     run), so it can be captured into a CUDA graph and replayed; replays give
     the plain run's bits, including after the inputs change in place."""
-    w = small(W.CONFIGS[4], 2, 264, 520, 136)
+    w = small(W.BIAS_RELU_SQUARE_L8, 2, 264, 520, 136)
     inputs = W.make_inputs(w)
     A, Bm, aux, sc = inputs
     dev = torch.device("cuda")
@@ -508,9 +509,9 @@ def test_epilogue_warps_follow_the_mainloop_length():
             return B.gemm_epi_plan_info(plan)["epi_warps"]
         finally:
             B.gemm_epi_plan_destroy(plan)
-    cfg4, cfg5 = W.CONFIGS[3], W.CONFIGS[4]
-    assert warps(cfg4) == 4                                   # K = 8192: 128 k-blocks a tile
-    assert warps(dataclasses.replace(cfg4, K=1024)) == 8      # 16 k-blocks a tile
-    assert warps(cfg5) == 8                                   # K = 2048, three epilogue tensors
-    assert warps(cfg4, epi_warps=8) == 8
-    assert warps(cfg4, debug_flags=B.GE_DEBUG_FORCE_INTERPRETER) == 8
+    ab, brs = W.ALPHA_BETA_X_8192, W.BIAS_RELU_SQUARE_L8
+    assert warps(ab) == 4                                     # K = 8192: 128 k-blocks a tile
+    assert warps(dataclasses.replace(ab, K=1024)) == 8        # 16 k-blocks a tile
+    assert warps(brs) == 8                                    # K = 2048, three epilogue tensors
+    assert warps(ab, epi_warps=8) == 8
+    assert warps(ab, debug_flags=B.GE_DEBUG_FORCE_INTERPRETER) == 8

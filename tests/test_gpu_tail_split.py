@@ -15,8 +15,8 @@ import test_gpu_majors as MJ  # noqa: E402
 from _gpu import B, W  # noqa: E402
 
 NO_SPLIT = B.GE_DEBUG_NO_TAIL_SPLIT
-CFG1 = W.CONFIGS[0]   # D = 0.5 * (acc + 2 C), Aux = acc + 2 C: integer inputs, exact
-CFG5 = W.CONFIGS[4]   # bf16, D = relu(0.5 acc + C + bias), E = D * D: N(0,1) inputs
+MYEPI = W.MY_EPILOGUE_128   # D = 0.5 * (acc + 2 C), Aux = acc + 2 C: integer inputs, exact
+BRS = W.BIAS_RELU_SQUARE_L8   # bf16, D = relu(0.5 acc + C + bias), E = D * D: N(0,1) inputs
 
 
 def both_schedules(w, unfused=False, **opt):
@@ -55,33 +55,33 @@ SHAPES = [
 @pytest.mark.parametrize("shape", SHAPES, ids=lambda s: "L%d_%dx%dx%d_cg%d_n%d" % s)
 def test_split_matches_unsplit_exact(shape):
     L, M, N, K, cg, bn = shape
-    w = dataclasses.replace(CFG1, L=L, M=M, N=N, K=K, sample_rows=None)
+    w = dataclasses.replace(MYEPI, L=L, M=M, N=N, K=K, sample_rows=None)
     info_s, _ = check(w, cta_group=cg, tile_n=bn)
     assert info_s["cta_group"] == cg and info_s["tile_n"] == bn
 
 
 def test_split_bf16_broadcast_two_outputs():
     """Row-vector bias read at the half tile's own columns, two outputs."""
-    w = dataclasses.replace(CFG5, L=2, M=512, N=640, K=128, sample_rows=None)
+    w = dataclasses.replace(BRS, L=2, M=512, N=640, K=128, sample_rows=None)
     check(w, cta_group=2, tile_n=256)
 
 
 def test_split_four_epilogue_warps_and_interpreter():
-    w = dataclasses.replace(CFG1, L=1, M=2048, N=1000, K=128, sample_rows=None)
+    w = dataclasses.replace(MYEPI, L=1, M=2048, N=1000, K=128, sample_rows=None)
     check(w, cta_group=2, tile_n=256, epi_warps=4)
     check(w, cta_group=2, tile_n=256, debug_flags=B.GE_DEBUG_FORCE_INTERPRETER)
 
 
 def test_split_unfused_path():
     """The unfused path's fp32-accumulator GEMM uses the same schedule."""
-    w = dataclasses.replace(CFG1, L=1, M=2048, N=1000, K=192, sample_rows=None)
+    w = dataclasses.replace(MYEPI, L=1, M=2048, N=1000, K=192, sample_rows=None)
     check(w, unfused=True, cta_group=2, tile_n=256)
 
 
 @pytest.mark.parametrize("majors", [(0, 1, 0), (1, 0, 0), (1, 1, 1)], ids=str)
 def test_split_with_majors(majors):
     """K-major B (half tiles load whole boxes), M-major A, M-major epilogue."""
-    w = dataclasses.replace(CFG1, L=1, M=2048, N=1024, K=128, sample_rows=None)
+    w = dataclasses.replace(MYEPI, L=1, M=2048, N=1024, K=128, sample_rows=None)
     inputs = W.make_inputs(w)
     split = MJ.run_majors(w, inputs, majors, cta_group=2, tile_n=256)
     plain = MJ.run_majors(w, inputs, majors, cta_group=2, tile_n=256, debug_flags=NO_SPLIT)
@@ -91,13 +91,13 @@ def test_split_with_majors(majors):
 
 def test_no_split_when_the_last_wave_is_more_than_half_full():
     """60 pair tiles (more than half of the 76 pairs) stay whole."""
-    w = dataclasses.replace(CFG1, L=1, M=2560, N=1536, K=64, sample_rows=None)  # 10 x 6
+    w = dataclasses.replace(MYEPI, L=1, M=2560, N=1536, K=64, sample_rows=None)  # 10 x 6
     _, _, _, info_s, info_p = both_schedules(w, cta_group=2, tile_n=256)
     assert info_s["num_tiles"] == info_p["num_tiles"] == 60
 
 
 def test_split_runs_in_a_cuda_graph():
-    w = dataclasses.replace(CFG1, L=1, M=2048, N=1000, K=128, sample_rows=None)
+    w = dataclasses.replace(MYEPI, L=1, M=2048, N=1000, K=128, sample_rows=None)
     inputs = W.make_inputs(w)
     ref, _ = _gpu.run_gpu(w, inputs, options=B.ge_options(cta_group=2, tile_n=256))
     A, Bm, aux, scalars = inputs

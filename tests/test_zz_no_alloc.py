@@ -27,7 +27,7 @@ def _outputs(w):
 def test_noalloc_matches_unfused_on_two_calls_in_a_row():
     # one plan, two calls with different inputs: the second must not see the
     # first call's workspace contents
-    w = dataclasses.replace(W.CONFIGS[4], L=2, M=256, N=520, K=264, sample_rows=None)
+    w = dataclasses.replace(W.BIAS_RELU_SQUARE_L8, L=2, M=256, N=520, K=264, sample_rows=None)
     assert B.gemm_epi_unfused_workspace_bytes  # exported
     plan = B.gemm_epi_plan_create(w.L, w.M, w.N, w.K, _gpu.dtypes_of(w), B.make_dag(w.dag))
     try:
@@ -53,7 +53,7 @@ def test_noalloc_matches_unfused_on_two_calls_in_a_row():
 
 
 def test_noalloc_rejects_problems_beyond_its_workspace():
-    w = W.CONFIGS[3]  # 8192^3: 256 MiB of fp32 workspace
+    w = W.ALPHA_BETA_X_8192  # 8192^3: 256 MiB of fp32 workspace
     plan = B.gemm_epi_plan_create(w.L, w.M, w.N, w.K, _gpu.dtypes_of(w), B.make_dag(w.dag))
     try:
         assert B.gemm_epi_unfused_workspace_bytes(plan) > B.GE_NOALLOC_SCRATCH_BYTES
