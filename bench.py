@@ -74,6 +74,31 @@ def peaks():
         return dict(FALLBACK_PEAKS), "fallback"
 
 
+def roofline(flops, alg_bytes, ms, traffic):
+    """The launch against the bound its arithmetic intensity sets: tensor
+    (flops / measured dense peak) or HBM (algorithmic bytes / measured copy
+    bandwidth), whichever takes longer; the other fraction rides along."""
+    pk, pk_src = peaks()
+    tflops = float(pk.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    tflops_sus = float(pk.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
+    gbs = float(pk.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+    sec = ms * 1e-3
+    t_frac = flops / sec / 1e12 / tflops
+    h_frac = alg_bytes / sec / 1e9 / gbs
+    extra = {"alg_bytes_per_launch": alg_bytes, "flops_per_launch": flops,
+             "frac_of_sustained": flops / sec / 1e12 / tflops_sus,
+             "frac_of_nominal_2250": flops / sec / 1e12 / 2250.0,
+             "tensor_frac": t_frac, "hbm_frac": h_frac}
+    if alg_bytes / (gbs * 1e9) > flops / (tflops * 1e12):
+        return dict({"bound": "hbm", "achieved": alg_bytes / sec / 1e9, "peak": gbs,
+                     "unit": "GB/s", "frac": h_frac, "traffic": traffic,
+                     "peak_source": "%s copy bandwidth" % pk_src}, **extra)
+    return dict({"bound": "tensor", "achieved": flops / sec / 1e12, "peak": tflops,
+                 "unit": "TFLOP/s", "frac": t_frac, "traffic": traffic,
+                 "peak_source": "%s bf16 dense burst (fp16 has the same nominal rate)" % pk_src},
+                **extra)
+
+
 def kernel_source_hash():
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "dense_gemm_elementwise_gb300", "csrc")
@@ -381,17 +406,7 @@ def run_ours(args, w):
         raise RuntimeError("device-side timeout during the timed region")
     value = world * flops / (ms_max * 1e-3) / 1e12
 
-    pk, pk_src = peaks()
-    peak = float(pk.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
-    peak_sus = float(pk.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
-    achieved = flops / (ms * 1e-3) / 1e12
-    roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                "frac": achieved / peak, "traffic": ncu_traffic(w.name),
-                "peak_source": "%s bf16 dense burst (fp16 has the same nominal rate)" % pk_src,
-                "frac_of_sustained": achieved / peak_sus,
-                "frac_of_nominal_2250": achieved / 2250.0,
-                "alg_bytes_per_launch": w.alg_bytes(),
-                "hbm_frac": w.alg_bytes() / (ms * 1e-3) / 1e9 / float(pk.get("hbm_gbs", 6800.0))}
+    roof = roofline(flops, w.alg_bytes(), ms, ncu_traffic(w.name))
 
     unfused = None
     if not args.no_unfused:
@@ -487,8 +502,8 @@ def run_ours(args, w):
                    "(inputs %d MiB)" % (in_bytes >> 20) if flush_l2 else
                    "no flush: inputs (%d MiB) larger than twice the L2" % (in_bytes >> 20)),
             "plan": info, "options": args.opt or "auto"}),
-        "pct_of_peak": 100.0 * achieved / peak,
-        "roofline": roofline, "gpu_launches": args.steps, "clocks": clk,
+        "pct_of_peak": 100.0 * roof["tensor_frac"],
+        "roofline": roof, "gpu_launches": args.steps, "clocks": clk,
         "unfused": unfused, "e2e": e2e, "cpu_baseline": cpu,
     }
     print(json.dumps(line), flush=True)
@@ -686,9 +701,7 @@ def run_grouped(args, w):
     B.gemm_epi_plan_destroy(plan)
     if rank != 0:
         return
-    pk, pk_src = peaks()
-    peak = float(pk.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
-    achieved = flops / (ms * 1e-3) / 1e12
+    roof = roofline(flops, w.alg_bytes(), ms, None)
     print(json.dumps({
         "metric": GROUPED_METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_max,
@@ -697,9 +710,7 @@ def run_grouped(args, w):
         "config": dict(grouped_config(w, world), **{
             "l2": "flushed before every timed step: 512 MiB write, then 256 MiB read",
             "plan": info, "options": args.opt or "auto"}),
-        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                     "frac": achieved / peak, "traffic": None,
-                     "peak_source": "%s bf16 dense burst" % pk_src},
+        "roofline": roof,
         "gpu_launches": args.steps, "clocks": clk, "one_launch_per_problem": separate,
         "e2e": e2e, "cpu_baseline": cpu}), flush=True)
 
