@@ -1,5 +1,12 @@
 // epilogue.cuh -- evaluation of the compiled epilogue program.
 //
+// Arithmetic as the pages fix it: every intermediate in fp32, one rounding
+// per store ("Custom Epilogue Example", "Running the Example":
+// --epi_dtype Float32); ReLU as where(d > 0, d, 0), so +0 for d <= 0
+// ("Activation Functions"); the activations of the legacy interface's
+// registry (the epilogue notebook of "CUTLASS Python 接口示例全解析"), with
+// GELU in its exact erf form, written through erfc.
+//
 // A program (program.cuh) is evaluated for CH consecutive columns of one
 // output row per thread.  Two executors evaluate the same instruction list:
 //

@@ -1,5 +1,13 @@
 // gemm_kernel.cuh -- persistent, warp-specialised GEMM + fused epilogue for sm_103a.
 //
+// The operation: "CUTLASS Operator API: Custom epilogue fusions for GEMMs"
+// (the GEMM result accum goes through a user epilogue before anything is
+// stored) and "Custom Epilogue Example", "Basic Example: Alpha-Beta Scaling"
+// (the epilogue reads C and X tiles and writes D and Y in the same kernel).
+// The pages' own kernel (128x128 MMA tile, 2x1 cluster, 2-CTA instructions,
+// "Running the Example") is prior art for other hardware; the tiling here is
+// this file's own.
+//
 // One CTA per SM (or one 2x1 cluster per SM pair with cta_group::2), looping
 // over output tiles in a static round-robin order.  Warp roles:
 //   warp 0      TMA producer: A and B k-blocks (K-major or MN-major) into an

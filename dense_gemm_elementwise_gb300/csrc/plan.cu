@@ -1,5 +1,11 @@
 // plan.cu -- host side of libgemm_epi.so: the C ABI declared in gemm_epi.h.
 //
+// The DAG rules follow "CUTLASS Operator API: Custom epilogue fusions for
+// GEMMs", "Failure examples" (cells [10]-[13]: the accumulator must be an
+// input, D must be produced, values are assigned once, every output must be
+// provided); the alignment rule follows "Custom Epilogue Example",
+// "Constraints" (16-byte aligned contiguous dimensions).
+//
 //   validate     DAG and type rules (host only, no device needed)
 //   compile      ge_dag -> two-address epilogue program (register allocation)
 //   configure    tile shape, CTA pairing, stage count, persistent grid

@@ -1,5 +1,11 @@
 // program.cuh -- the DAG -> epilogue-program compiler.
 //
+// The DAG is the one "CUTLASS Operator API: Custom epilogue fusions for
+// GEMMs" describes ("How the epilogue fusion API works", figure
+// "Intermediate DAG representation"): AccFetch, Load and compute nodes
+// ending in Stores, in single-assignment order ("Defining an epilogue via a
+// Python function").
+//
 // constexpr and __host__ __device__ so that the very same function compiles
 // user DAGs at plan time (host) and the built-in catalog of epilogues at
 // build time (template arguments of the specialised kernels).  A user DAG

@@ -1,4 +1,7 @@
-// unfused.cu -- the unfused comparison path's second kernel: a grid-stride
+// unfused.cu -- the unfused comparison path ("Custom Epilogue Example",
+// "Overview": a GEMM kernel followed by separate elementwise kernels, against
+// one fused kernel that saves the memory traffic and the extra launches).
+// Its second kernel: a grid-stride
 // elementwise pass that reads the fp32 accumulator the GEMM wrote to a
 // workspace, evaluates the same compiled epilogue program as the fused kernel
 // (interpreter or catalog executor), and writes the outputs.  One thread
