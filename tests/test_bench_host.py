@@ -72,3 +72,23 @@ def test_unparseable_timestamp_falls_back_to_arrival_time():
                           "Not Active, Not Active\n")]
     w = s.window(t0, t0 + 0.2)
     assert w["samples"] == 1 and w["sm_mhz"] == 1800 and w["reasons"] == []
+
+
+def test_roofline_takes_the_binding_bound(monkeypatch):
+    """A launch is measured against the tensor peak when its flops take longer
+    at peak than its algorithmic bytes at copy bandwidth, else against HBM."""
+    bench = load_bench()
+    monkeypatch.setattr(bench, "peaks", lambda: ({"bf16_tflops": 2000.0,
+                                                   "bf16_tflops_sustained": 1800.0,
+                                                   "hbm_gbs": 8000.0}, "measured"))
+    # 8192^3 with four 128 MiB inputs and two outputs: 550 us at peak vs 100 us of bytes
+    big = bench.roofline(2.0 * 8192 ** 3, 805306368, 0.70, 123)
+    assert big["bound"] == "tensor" and big["unit"] == "TFLOP/s" and big["traffic"] == 123
+    assert abs(big["achieved"] - 2.0 * 8192 ** 3 / 0.70e-3 / 1e12) < 1e-6
+    assert abs(big["frac"] - big["achieved"] / 2000.0) < 1e-12
+    assert abs(big["frac_of_sustained"] - big["achieved"] / 1800.0) < 1e-12
+    # 1024^3 with 10 MiB of operands: 1.07 us at peak vs 1.31 us of bytes
+    small = bench.roofline(2.0 * 1024 ** 3, 10485760, 0.0148, None)
+    assert small["bound"] == "hbm" and small["unit"] == "GB/s" and small["peak"] == 8000.0
+    assert abs(small["achieved"] - 10485760 / 0.0148e-3 / 1e9) < 1e-6
+    assert abs(small["frac"] - small["hbm_frac"]) < 1e-12 and small["tensor_frac"] < small["frac"]
