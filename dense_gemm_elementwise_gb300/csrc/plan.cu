@@ -502,7 +502,9 @@ int configure(gemm_epi_plan *pl) {
     const int64_t tiles = pl->L * Lo->num_m_blk * int64_t(Lo->num_n_blk);
     if (tiles > (int64_t(1) << 30)) return GE_ERR_SHAPE;
     Lo->num_tiles = static_cast<int>(tiles);
-    Lo->raster_group = o.raster_group ? o.raster_group : 8;
+    // 16 M tiles per raster group: with the k-snake order 0.3-1.6 % faster
+    // than 8 at 8192^3 in four interleaved repetitions
+    Lo->raster_group = o.raster_group ? o.raster_group : 16;
     int sms = pl->num_sms;
     if (o.max_ctas) sms = std::min(sms, o.max_ctas);
     int units = std::max(1, sms / (cg * mc));
