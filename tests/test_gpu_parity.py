@@ -112,6 +112,25 @@ def test_small_grid_many_tiles_per_cta(cluster_n):
     _gpu.compare(w, gpu, _gpu.oracle_rows(w, inputs))
 
 
+@pytest.mark.parametrize("variant", [(1, 128, 1), (2, 256, 1), (2, 256, 2)],
+                         ids=lambda v: "cg%d_n%d_mc%d" % v)
+def test_k_snake_with_ragged_k(variant):
+    """A few CTAs loop over many tiles, so half of their tiles walk K
+    backwards and start on the partial last k-block (K = 200 and 1000 are
+    not multiples of 64): bit-exact against the oracle, and the unfused
+    path (same schedule) bit-identical."""
+    cg, bn, mc = variant
+    for K in (200, 1000):
+        w = small(W.MY_EPILOGUE_128, 2, 520, 776, K)
+        inputs = W.make_inputs(w)
+        opts = B.ge_options(max_ctas=2 * cg * mc, cta_group=cg, tile_n=bn, cluster_n=mc)
+        gpu, info = _gpu.run_gpu(w, inputs, options=opts)
+        assert info["num_tiles"] >= 4 * info["grid"] // (cg * mc)
+        _gpu.compare(w, gpu, _gpu.oracle_rows(w, inputs))
+        unf, _ = _gpu.run_gpu(w, inputs, options=opts, unfused=True)
+        _gpu.bitwise_equal(gpu, unf)
+
+
 # ------------------------------------------------------------ unfused --
 
 @pytest.mark.parametrize("w", [W.MY_EPILOGUE_1024, small(W.BIAS_RELU_SQUARE_L8, 2, 256, 392, 520),
