@@ -39,6 +39,13 @@
  *    store rounds (round to nearest even) to its output type ("Custom
  *    Epilogue Example", "Running the Example": --acc_dtype Float32,
  *    --epi_dtype Float32).  ReLU returns +0 for inputs <= 0.
+ *  * Results are bit-for-bit repeatable for a given plan on a given device.
+ *    The order of the sum over K belongs to the plan (tile shape, grid,
+ *    and a tile's place in the schedule: a CTA walks K upwards on its even
+ *    tiles and downwards on its odd ones), so two plans that differ in those
+ *    may round non-integer results differently, within fp32 summation error;
+ *    the epilogue warp count, the last-wave split and the fused/unfused
+ *    choice never change the result.
  *  * Return values are GE_* status codes; gemm_epi_status_string names them.
  */
 #ifndef GEMM_EPI_H
