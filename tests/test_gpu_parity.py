@@ -131,6 +131,20 @@ def test_k_snake_with_ragged_k(variant):
         _gpu.bitwise_equal(gpu, unf)
 
 
+def test_fused_and_unfused_share_the_k_order():
+    """N(0,1) inputs, where the order of the sum over K shows in the last
+    bits, and many tiles per CTA, half of them walking K backwards: the
+    unfused path's GEMM must use the same schedule, bit for bit."""
+    w = small(W.ALPHA_BETA_X_8192, 1, 1040, 776, 1000)
+    inputs = W.make_inputs(w)
+    opts = B.ge_options(max_ctas=4, cta_group=2, tile_n=256)
+    fused, info = _gpu.run_gpu(w, inputs, options=opts)
+    assert info["num_tiles"] >= 4 * info["grid"] // 2
+    unf, _ = _gpu.run_gpu(w, inputs, options=opts, unfused=True)
+    _gpu.bitwise_equal(fused, unf)
+    _gpu.compare(w, fused, _gpu.oracle_rows(w, inputs))
+
+
 # ------------------------------------------------------------ unfused --
 
 @pytest.mark.parametrize("w", [W.MY_EPILOGUE_1024, small(W.BIAS_RELU_SQUARE_L8, 2, 256, 392, 520),
