@@ -17,8 +17,7 @@ CSRC = os.path.join(HERE, "csrc")
 OBJ = os.path.join(HERE, "_build")
 LIBDIR = os.path.join(HERE, "lib")
 LIB = os.path.join(LIBDIR, "libgemm_epi.so")
-UNITS = ["plan", "unfused", "jit", "k_cg1_n64", "k_cg1_n128", "k_cg1_n256", "k_cg2_n128", "k_cg2_n256",
-         "k_cg2_n256_mc2"]
+UNITS = ["plan", "unfused", "jit", "k_cg1_n64", "k_cg1_n128", "k_cg1_n256", "k_cg2_n128", "k_cg2_n256"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

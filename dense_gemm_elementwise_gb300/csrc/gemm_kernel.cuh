@@ -33,17 +33,13 @@
 // blocks), and each problem brings its own tensor maps and vector pointers
 // from a problem table in global memory.
 //
-// MC = 2: two CTA pairs of a 4-CTA cluster compute adjacent N tiles with the
-// same A rows; each CTA fetches half of its A rows and multicasts them to its
-// counterpart in the other pair (25% less L2->SM traffic).  A stage is free
-// only when both pairs' MMAs have read it, so empty barriers count one commit
-// per pair and the commits multicast to the whole cluster.
-//
 // cta_group::2: the CTA pair computes a (256 x BN) tile.  Each CTA loads its
 // 128 rows of A and its BN/2 columns of B into its own shared memory; the
 // leader's MMA thread issues the pair MMA, which reads both CTAs' halves and
 // writes each CTA's 128 accumulator rows into that CTA's TMEM.  Stage
-// completion is counted on the leader's barriers; commits multicast to both.
+// completion is counted on the leader's barriers; each commit arrives on the
+// same barrier in both CTAs.  Every TMA load lands in the issuing CTA's own
+// shared memory (no cluster multicast).
 //
 // Every wait is bounded (globaltimer): on expiry the kernel records
 // GE_ERR_TIMEOUT in the status word, stops issuing work, waits (bounded) for
@@ -56,14 +52,12 @@
 
 namespace ge {
 
-template <int CG, int BN, int MC>
+template <int CG, int BN>
 struct TileCfg {
-  static constexpr int kCluster = CG * MC;         // CTAs per cluster
+  static constexpr int kCluster = CG;              // CTAs per cluster
   static constexpr int kMmaM = BM * CG;            // rows of one MMA tile
   static constexpr int kBnLocal = BN / CG;         // B columns loaded per CTA
   static constexpr int kABytes = BM * BK * 2;      // one A stage
-  static constexpr int kALoadRows = BM / MC;       // A rows this CTA fetches per stage
-  static_assert(MC == 1 || CG == 2, "A multicast is built on CTA pairs");
   static constexpr int kBBytes = kBnLocal * BK * 2;
   static constexpr int kBAtoms = kBnLocal / 64;    // 64-column swizzle atoms of B
   static constexpr int kSteps = BN / EW;          // epilogue steps per tile
@@ -235,13 +229,13 @@ struct FusedMem {
   }
 };
 
-template <int CG, int BN, int MC, class Epi>
+template <int CG, int BN, class Epi>
 __global__ void __launch_bounds__(threads_for(Epi::kWarps), 1)
     gemm_epi_kernel(const __grid_constant__ KParams p) {
   constexpr int kEpiWarps = Epi::kWarps;
   constexpr int kSplit = kEpiWarps / 4;  // warps per TMEM lane quarter
   static_assert(kEpiWarps == 4 || kEpiWarps == 8, "4 or 8 epilogue warps");
-  using T = TileCfg<CG, BN, MC>;
+  using T = TileCfg<CG, BN>;
   extern __shared__ uint8_t smem_raw[];
   // 1024-byte alignment of the shared-window address (swizzle atoms)
   uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
@@ -249,14 +243,11 @@ __global__ void __launch_bounds__(threads_for(Epi::kWarps), 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const uint32_t crank = (T::kCluster > 1) ? cluster_ctarank() : 0u;
-  const uint32_t rank = crank % CG;          // rank within the CTA pair
-  const int pair = static_cast<int>(crank / CG);  // pair within the cluster (MC > 1)
-  const uint32_t leader = crank - rank;      // cluster rank of this pair's leader
+  const uint32_t rank = (CG > 1) ? cluster_ctarank() : 0u;  // rank within the CTA pair
+  constexpr uint32_t leader = 0;             // cluster rank of the pair's leader
   const int unit = blockIdx.x / T::kCluster;  // this CTA's cluster (or CTA) index
   const int n_units = gridDim.x / T::kCluster;
-  constexpr uint16_t kAllMask = static_cast<uint16_t>((1u << T::kCluster) - 1u);
-  const uint16_t pair_mask = static_cast<uint16_t>(0x3u << (CG * pair));
+  constexpr uint16_t kPairMask = 0x3u;  // a commit arrives in both CTAs of the pair
 
   const uint32_t bar = sb + p.off_bar;
   const uint32_t bar_aux = bar + kBarAux;
@@ -266,7 +257,7 @@ __global__ void __launch_bounds__(threads_for(Epi::kWarps), 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < p.stages; ++s) {
       mbar_init(bar + kBarFull + 8 * s, 1);
-      mbar_init(bar + kBarEmpty + 8 * s, MC);  // released by every pair sharing the stage
+      mbar_init(bar + kBarEmpty + 8 * s, 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(bar + kBarTmemFull + 8 * b, 1);
@@ -305,7 +296,7 @@ __global__ void __launch_bounds__(threads_for(Epi::kWarps), 1)
       const GroupDesc *ready_gd = nullptr;  // problem whose A/B maps are fenced and prefetched
       for (int i = 0; ok && i < my_tiles; ++i) {
         const TileRef tr = tc.next();
-        const int l = tr.l, mb = tr.mb, nb = tr.nb * MC + pair;
+        const int l = tr.l, mb = tr.mb, nb = tr.nb;
         const CUtensorMap *mA = tr.gd ? &tr.gd->tmA : &p.tmA;
         const CUtensorMap *mB = tr.gd ? &tr.gd->tmB : &p.tmB;
         if (tr.gd && tr.gd != ready_gd) {
@@ -342,21 +333,11 @@ __global__ void __launch_bounds__(threads_for(Epi::kWarps), 1)
             if constexpr (CG == 2) {
               const uint32_t fb = mapa_shared(fb_local, leader);
               if (rank == 0) mbar_arrive_expect_tx(fb_local, tx);
-              if constexpr (MC == 1) {
-                if (p.a_mn) {  // two 64-row atoms of the M-major A tile
-                  tma_load_3d_pair(sa, mA, fb, m0, kx, l);
-                  tma_load_3d_pair(sa + 8192, mA, fb, m0 + 64, kx, l);
-                } else {
-                  tma_load_3d_pair(sa, mA, fb, kx, m0, l);
-                }
+              if (p.a_mn) {  // two 64-row atoms of the M-major A tile
+                tma_load_3d_pair(sa, mA, fb, m0, kx, l);
+                tma_load_3d_pair(sa + 8192, mA, fb, m0 + 64, kx, l);
               } else {
-                // this pair fetches its share of the A rows and multicasts it to
-                // the CTA with the same rank in every pair of the cluster
-                uint16_t mask = 0;
-#pragma unroll
-                for (int pp = 0; pp < MC; ++pp) mask |= static_cast<uint16_t>(1u << (pp * CG + rank));
-                tma_load_3d_pair_mc(sa + pair * T::kALoadRows * 128, mA, fb, kx,
-                                    m0 + pair * T::kALoadRows, l, mask);
+                tma_load_3d_pair(sa, mA, fb, kx, m0, l);
               }
               if (p.b_k) {
                 tma_load_3d_pair(sbb, mB, fb, kx, n0, l);
@@ -465,14 +446,14 @@ __global__ void __launch_bounds__(threads_for(Epi::kWarps), 1)
 #pragma unroll
           for (int k = 0; k < BK / UMMA_K; ++k)
             umma_f16<CG>(d, ad + a_k16 * k, bd + b_k16 * k, idt, (kb | k) != 0 ? 1u : 0u);
-          umma_commit<CG>(bar + kBarEmpty + 8 * stage, kAllMask);
+          umma_commit<CG>(bar + kBarEmpty + 8 * stage, kPairMask);
           if (++stage == p.stages) {
             stage = 0;
             phase ^= 1u;
           }
         }
         if (!ok) break;
-        umma_commit<CG>(bar + kBarTmemFull + 8 * abuf, pair_mask);
+        umma_commit<CG>(bar + kBarTmemFull + 8 * abuf, kPairMask);
         abuf ^= 1;
         if (abuf == 0) aphase ^= 1u;
       }
@@ -486,7 +467,7 @@ __global__ void __launch_bounds__(threads_for(Epi::kWarps), 1)
         }
       } else {
         // abort: let the MMAs already issued finish before TMEM is freed
-        umma_commit<CG>(bar + kBarDrain, pair_mask);
+        umma_commit<CG>(bar + kBarDrain, kPairMask);
         wt.drain(bar + kBarDrain, 0u);
       }
     }
@@ -528,7 +509,7 @@ __global__ void __launch_bounds__(threads_for(Epi::kWarps), 1)
         const TileRef tr = pf_tc.next();  // tiles are entered in order, one at a time
         pf_l = tr.l;
         pf_tile = ii;
-        pf_x0 = (tr.nb * MC + pair) * BN + (tr.half > 0 ? BN / 2 : 0);
+        pf_x0 = tr.nb * BN + (tr.half > 0 ? BN / 2 : 0);
         pf_y = tr.mb * T::kMmaM + static_cast<int>(rank) * BM + q * 32;
         if (tr.gd && pf_maps != tr.gd->tmAux)
           for (int a = 0; a < p.prog.n_tma_aux; ++a) {
@@ -550,7 +531,7 @@ __global__ void __launch_bounds__(threads_for(Epi::kWarps), 1)
 
     for (int i = 0; ok && i < my_tiles; ++i) {
       const TileRef tr = tc.next();
-      const int l = tr.l, mb = tr.mb, nb = tr.nb * MC + pair;
+      const int l = tr.l, mb = tr.mb, nb = tr.nb;
       const int m0 = mb * T::kMmaM + static_cast<int>(rank) * BM + q * 32;
       const int n0 = nb * BN + (tr.half > 0 ? BN / 2 : 0);
       const int steps = tr.half < 0 ? T::kSteps : T::kSteps / 2;  // 32-column steps of this tile

@@ -125,10 +125,9 @@ std::string program_literal(const EpiProgram &P) {
   return o;
 }
 
-std::string cache_key(const EpiProgram &P, int cg, int bn, int mc, int warps) {
+std::string cache_key(const EpiProgram &P, int cg, int bn, int warps) {
   std::string k = program_literal(P);
-  k += "|" + std::to_string(cg) + "," + std::to_string(bn) + "," + std::to_string(mc) + "," +
-       std::to_string(warps);
+  k += "|" + std::to_string(cg) + "," + std::to_string(bn) + "," + std::to_string(warps);
   return k;
 }
 
@@ -139,14 +138,13 @@ std::map<std::string, const void *> g_jit_cache;
 
 bool jit_available() { return nvrtc().ok; }
 
-const void *jit_gemm_kernel(const EpiProgram &P, int cg, int bn, int mc, int warps,
-                            std::string *log) {
+const void *jit_gemm_kernel(const EpiProgram &P, int cg, int bn, int warps, std::string *log) {
   const Nvrtc &n = nvrtc();
   if (!n.ok) {
     if (log) *log = "runtime compiler (libnvrtc) not found";
     return nullptr;
   }
-  const std::string key = cache_key(P, cg, bn, mc, warps);
+  const std::string key = cache_key(P, cg, bn, warps);
   std::lock_guard<std::mutex> lock(g_jit_mutex);
   auto it = g_jit_cache.find(key);
   if (it != g_jit_cache.end()) return it->second;
@@ -163,8 +161,7 @@ const void *jit_gemm_kernel(const EpiProgram &P, int cg, int bn, int mc, int war
                           "};\n"
                           "}  // namespace ge\n";
   const std::string name = "ge::gemm_epi_kernel<" + std::to_string(cg) + ", " +
-                           std::to_string(bn) + ", " + std::to_string(mc) +
-                           ", ge::EpiStatic<ge::JitProg, " + std::to_string(warps) + "> >";
+                           std::to_string(bn) + ", ge::EpiStatic<ge::JitProg, " + std::to_string(warps) + "> >";
   const std::string o_csrc = "-I" + csrc, o_inc = "-I" + inc,
                     o_cuda = "-I" + cuda_home() + "/include";
   // -default-device: the C ABI's host declarations in gemm_epi.h are never

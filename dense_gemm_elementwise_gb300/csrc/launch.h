@@ -20,12 +20,10 @@ const void *gemm_kernel_cg1_n128(int epi, int warps);
 const void *gemm_kernel_cg1_n256(int epi, int warps);
 const void *gemm_kernel_cg2_n128(int epi, int warps);
 const void *gemm_kernel_cg2_n256(int epi, int warps);
-const void *gemm_kernel_cg2_n256_mc2(int epi, int warps);  // 4-CTA cluster, A multicast
 
 // a fused kernel compiled at run time for program P (nullptr, with the
 // compiler's log in *log, if the runtime compiler is missing or fails)
-const void *jit_gemm_kernel(const EpiProgram &P, int cg, int bn, int mc, int warps,
-                            std::string *log);
+const void *jit_gemm_kernel(const EpiProgram &P, int cg, int bn, int warps, std::string *log);
 bool jit_available();
 
 // unfused comparison path: elementwise epilogue over an fp32 accumulator

@@ -184,7 +184,6 @@ bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 // ------------------------------------------------------------ configuration --
 struct Layout {
   int cg = 0, bn = 0, stages = 0, aux_stages = 0, grid = 0, num_tiles = 0;
-  int mc = 1;         // CTA pairs per cluster sharing A (multicast)
   int warps = 4;      // epilogue warps (4 or 8)
   const void *fn = nullptr;  // the kernel (chosen by configure)
   int smem = 0;       // dynamic smem requested at launch
@@ -324,8 +323,7 @@ constexpr int kEpiSpecialized = -3;
 // interpreter); never returned through the ABI
 constexpr int GE_ERR_JIT = -100;
 
-const void *gemm_kernel(int cg, int bn, int mc, int epi, int warps) {
-  if (mc == 2) return (cg == 2 && bn == 256) ? gemm_kernel_cg2_n256_mc2(epi, warps) : nullptr;
+const void *gemm_kernel(int cg, int bn, int epi, int warps) {
   if (cg == 1 && bn == 64) return gemm_kernel_cg1_n64(epi, warps);
   if (cg == 1 && bn == 128) return gemm_kernel_cg1_n128(epi, warps);
   if (cg == 1 && bn == 256) return gemm_kernel_cg1_n256(epi, warps);
@@ -334,12 +332,12 @@ const void *gemm_kernel(int cg, int bn, int mc, int epi, int warps) {
   return nullptr;
 }
 
-const void *resolve_kernel(gemm_epi_plan *pl, int cg, int bn, int mc, int epi, int warps,
+const void *resolve_kernel(gemm_epi_plan *pl, int cg, int bn, int epi, int warps,
                            const EpiProgram *P) {
   (void)pl;
-  if (epi != kEpiSpecialized) return gemm_kernel(cg, bn, mc, epi, warps);
+  if (epi != kEpiSpecialized) return gemm_kernel(cg, bn, epi, warps);
   std::string log;
-  const void *fn = jit_gemm_kernel(*P, cg, bn, mc, warps, &log);
+  const void *fn = jit_gemm_kernel(*P, cg, bn, warps, &log);
   if (!fn && log_enabled())
     std::fprintf(stderr, "[gemm_epi] run-time compilation failed, using the interpreter: %s\n",
                  log.c_str());
@@ -354,9 +352,9 @@ cudaLaunchConfig_t launch_config(const Layout &Lo, cudaStream_t s, cudaLaunchAtt
   cfg.stream = s;
   cfg.attrs = nullptr;
   cfg.numAttrs = 0;
-  if (Lo.cg * Lo.mc > 1) {
+  if (Lo.cg > 1) {
     attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = static_cast<unsigned>(Lo.cg * Lo.mc);
+    attr[0].val.clusterDim.x = static_cast<unsigned>(Lo.cg);
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
@@ -379,12 +377,11 @@ cudaError_t launch_gemm(const Layout &Lo, int epi, const KParams &kp, cudaStream
 // into half-width tiles: when it would leave at least half of them idle, its
 // r tiles become 2r halves (one per CTA at most), so the wave takes about
 // half as long.  Needs whole 32-column epilogue steps per warp in a half
-// (BN >= 128), whole 64-column B atoms per CTA in a half (BN / cg >= 128, or
-// K-major B, which loads whole boxes), and no A multicast (whose cluster
-// shares a tile's A rows between pairs).
-bool split_tail(int64_t tiles, int64_t units, int cg, int bn, int mc, bool b_k) {
+// (BN >= 128) and whole 64-column B atoms per CTA in a half (BN / cg >= 128,
+// or K-major B, which loads whole boxes).
+bool split_tail(int64_t tiles, int64_t units, int cg, int bn, bool b_k) {
   const int64_t r = tiles % units;
-  return r > 0 && 2 * r <= units && mc == 1 && bn >= 128 && (b_k || bn / cg >= 128);
+  return r > 0 && 2 * r <= units && bn >= 128 && (b_k || bn / cg >= 128);
 }
 
 // Rough cost model in SM clocks: waves x per-tile mainloop, where a k-block
@@ -393,22 +390,21 @@ bool split_tail(int64_t tiles, int64_t units, int cg, int bn, int mc, bool b_k) 
 // its operand fill time at
 // ~48 B/clk/SM of L2 bandwidth when every SM is busy (measured: per-SM
 // throughput drops by a third from 38 to 152 active SMs with 32 KiB per
-// k-block).  With A multicast (mc = 2)
-// a CTA fetches only half of its A rows.
-double est_kblock_cycles(int cg, int bn, int mc) {
+// k-block).
+double est_kblock_cycles(int cg, int bn) {
   const double mma = 2.0 * bn;
-  const double fill = double((BM / mc + bn / cg) * BK * 2) / 48.0;
+  const double fill = double((BM + bn / cg) * BK * 2) / 48.0;
   return std::max(mma, fill);
 }
 
-double est_cycles(const gemm_epi_plan *pl, int cg, int bn, int mc, int units) {
+double est_cycles(const gemm_epi_plan *pl, int cg, int bn, int units) {
   const int64_t mt = (pl->M + BM * cg - 1) / (BM * cg);
-  const int64_t nt = (pl->N + int64_t(bn) * mc - 1) / (int64_t(bn) * mc);
+  const int64_t nt = (pl->N + bn - 1) / bn;
   const int64_t tiles = pl->L * mt * nt;
   const int64_t kb = (pl->K + BK - 1) / BK;
-  const double per_tile = kb * est_kblock_cycles(cg, bn, mc);
+  const double per_tile = kb * est_kblock_cycles(cg, bn);
   const bool split = (pl->opt.debug_flags & GE_DEBUG_NO_TAIL_SPLIT) == 0u &&
-                     split_tail(tiles, units, cg, bn, mc, pl->b_k != 0);
+                     split_tail(tiles, units, cg, bn, pl->b_k != 0);
   const double waves = split ? double(tiles / units) + 0.5 : double((tiles + units - 1) / units);
   return waves * per_tile + (bn / CH) * 300.0;
 }
@@ -459,32 +455,31 @@ int configure(gemm_epi_plan *pl) {
   if (o.cta_group != 0 && o.cta_group != 1 && o.cta_group != 2) return GE_ERR_INVALID;
   if (o.tile_n != 0 && o.tile_n != 64 && o.tile_n != 128 && o.tile_n != 256) return GE_ERR_INVALID;
   if (o.stages < 0 || o.stages > kMaxStages || o.max_ctas < 0 || o.raster_group < 0 ||
-      o.timeout_ms < 0 || (o.cluster_n != 0 && o.cluster_n != 1 && o.cluster_n != 2))
+      o.timeout_ms < 0)
     return GE_ERR_INVALID;
-  const int cand[6][3] = {{2, 256, 2}, {2, 256, 1}, {2, 128, 1}, {1, 256, 1}, {1, 128, 1}, {1, 64, 1}};
+  const int cand[5][2] = {{2, 256}, {2, 128}, {1, 256}, {1, 128}, {1, 64}};
   int best = -1;
   double best_c = 0;
-  for (int c = 0; c < 6; ++c) {
-    const int cg = cand[c][0], bn = cand[c][1], mc = cand[c][2];
+  for (int c = 0; c < 5; ++c) {
+    const int cg = cand[c][0], bn = cand[c][1];
     if (o.cta_group && o.cta_group != cg) continue;
     if (o.tile_n && o.tile_n != bn) continue;
-    if (o.cluster_n ? o.cluster_n != mc : mc != 1) continue;  // multicast: opt-in
     int sms = pl->num_sms;
     if (o.max_ctas) sms = std::min(sms, o.max_ctas);
-    if (sms < cg * mc) continue;
-    const int units = sms / (cg * mc);
-    const double cost = est_cycles(pl, cg, bn, mc, units);
+    if (sms < cg) continue;
+    const int units = sms / cg;
+    const double cost = est_cycles(pl, cg, bn, units);
     if (best < 0 || cost < best_c * 0.98) {
       best = c;
       best_c = cost;
     }
   }
   if (best < 0) return GE_ERR_INVALID;  // e.g. cta_group 2 with tile_n 64
-  const int cg = cand[best][0], bn = cand[best][1], mc = cand[best][2];
+  const int cg = cand[best][0], bn = cand[best][1];
 
   int warps = 0;
   const int64_t kb = (pl->K + BK - 1) / BK;
-  int st = pick_epi_warps(pl, &warps, bn, double(kb) * est_kblock_cycles(cg, bn, mc));
+  int st = pick_epi_warps(pl, &warps, bn, double(kb) * est_kblock_cycles(cg, bn));
   if (st != GE_OK) return st;
   st = make_layout(&pl->lay, cg, bn, o.stages, pl->prog, pl->max_smem, 4, 5, warps);
   if (st != GE_OK) return st;
@@ -494,10 +489,8 @@ int configure(gemm_epi_plan *pl) {
   if (st != GE_OK) return st;
 
   for (Layout *Lo : {&pl->lay, &pl->lay_acc}) {
-    Lo->mc = mc;
     Lo->num_m_blk = static_cast<int>((pl->M + BM * cg - 1) / (BM * cg));
-    // with A multicast a tile index covers mc adjacent N tiles (one per pair)
-    Lo->num_n_blk = static_cast<int>((pl->N + int64_t(bn) * mc - 1) / (int64_t(bn) * mc));
+    Lo->num_n_blk = static_cast<int>((pl->N + bn - 1) / bn);
     Lo->num_kb = static_cast<int>((pl->K + BK - 1) / BK);
     const int64_t tiles = pl->L * Lo->num_m_blk * int64_t(Lo->num_n_blk);
     if (tiles > (int64_t(1) << 30)) return GE_ERR_SHAPE;
@@ -507,31 +500,31 @@ int configure(gemm_epi_plan *pl) {
     Lo->raster_group = o.raster_group ? o.raster_group : 16;
     int sms = pl->num_sms;
     if (o.max_ctas) sms = std::min(sms, o.max_ctas);
-    int units = std::max(1, sms / (cg * mc));
-    const void *fn = resolve_kernel(pl, cg, bn, mc, Lo == &pl->lay ? pl->epi : pl->epi_acc,
+    int units = std::max(1, sms / cg);
+    const void *fn = resolve_kernel(pl, cg, bn, Lo == &pl->lay ? pl->epi : pl->epi_acc,
                                     Lo->warps, Lo == &pl->lay ? &pl->prog : &pl->prog_acc);
     if (!fn) return pl->epi == kEpiSpecialized && Lo == &pl->lay ? GE_ERR_JIT : GE_ERR_INVALID;
     Lo->fn = fn;
     if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, Lo->smem) != cudaSuccess)
       return GE_ERR_CUDA;
-    if (cg * mc > 1) {
+    if (cg > 1) {
       int clusters = 0;
       cudaLaunchAttribute attr[1];
       cudaLaunchConfig_t cfg = launch_config(*Lo, nullptr, attr);
-      cfg.gridDim = dim3(static_cast<unsigned>(cg * mc));
+      cfg.gridDim = dim3(static_cast<unsigned>(cg));
       if (cudaOccupancyMaxActiveClusters(&clusters, fn, &cfg) == cudaSuccess && clusters > 0)
         units = std::min(units, clusters);
       cudaGetLastError();
     }
     Lo->num_full = Lo->num_tiles;
     if ((o.debug_flags & GE_DEBUG_NO_TAIL_SPLIT) == 0u &&
-        split_tail(tiles, units, cg, bn, mc, pl->b_k != 0)) {
+        split_tail(tiles, units, cg, bn, pl->b_k != 0)) {
       const int64_t r = tiles % units;
       Lo->num_full = static_cast<int>(tiles - r);
       Lo->num_tiles = static_cast<int>(tiles + r);
     }
     units = static_cast<int>(std::min<int64_t>(units, Lo->num_tiles));
-    Lo->grid = units * cg * mc;
+    Lo->grid = units * cg;
   }
   return GE_OK;
 }
@@ -580,7 +573,6 @@ void fill_params(const gemm_epi_plan *pl, const Layout &Lo, const EpiProgram &P,
   kp->cd_m = pl->cd_m;
 }
 
-// A box: the rows one CTA fetches per stage (all 128, or its share under multicast)
 // A and B tensor maps of one (L, M, N, K) problem.  K-major A: (K, M, L), box
 // 64 x the rows one CTA fetches; M-major A: (M, K, L), box 64 x 64 (one of
 // the tile's two 64-row atoms); N-major B: (N, K, L), box 64 x 64 (one 64-column
@@ -591,8 +583,7 @@ bool encode_ab_maps(const gemm_epi_plan *pl, CUtensorMap *tA, CUtensorMap *tB, c
   const auto sw = CU_TENSOR_MAP_SWIZZLE_128B;
   const auto l2 = CU_TENSOR_MAP_L2_PROMOTION_L2_256B;
   const bool okA = pl->a_mn ? encode3d(tA, ab, A, M, K, L, 64, BK, sw, l2)
-                            : encode3d(tA, ab, A, K, M, L, BK,
-                                       static_cast<uint32_t>(BM / pl->lay.mc), sw, l2);
+                            : encode3d(tA, ab, A, K, M, L, BK, BM, sw, l2);
   const bool okB = pl->b_k ? encode3d(tB, ab, B, K, N, L, BK,
                                       static_cast<uint32_t>(pl->lay.bn / pl->lay.cg), sw, l2)
                            : encode3d(tB, ab, B, N, K, L, 64, BK, sw, l2);
@@ -605,18 +596,17 @@ bool encode_operands(const gemm_epi_plan *pl, KParams *kp, const void *A, const 
 
 // An epilogue tensor's map: N-major (N, M, L) with 32 x 32 swizzled boxes, or
 // M-major (M, N, L) with 32 x 32 plain boxes.  The unfused path's fp32
-// workspace is always N-major (row_major).
+// workspace follows the epilogue tensors' order.
 bool encode_epi_map(const gemm_epi_plan *pl, CUtensorMap *m, int dt, const void *ptr, uint64_t L,
-                    uint64_t M, uint64_t N, bool row_major = false) {
-  if (pl->cd_m && !row_major)
+                    uint64_t M, uint64_t N) {
+  if (pl->cd_m)
     return encode3d(m, dt, ptr, M, N, L, 32, EW, CU_TENSOR_MAP_SWIZZLE_NONE,
                     CU_TENSOR_MAP_L2_PROMOTION_L2_128B);
   return encode3d(m, dt, ptr, N, M, L, EW, 32, epi_swizzle(dt), CU_TENSOR_MAP_L2_PROMOTION_L2_128B);
 }
 
-bool encode_epilogue_map(const gemm_epi_plan *pl, CUtensorMap *m, int dt, const void *ptr,
-                         bool row_major = false) {
-  return encode_epi_map(pl, m, dt, ptr, pl->L, pl->M, pl->N, row_major);
+bool encode_epilogue_map(const gemm_epi_plan *pl, CUtensorMap *m, int dt, const void *ptr) {
+  return encode_epi_map(pl, m, dt, ptr, pl->L, pl->M, pl->N);
 }
 
 // Operand and epilogue majors from the options (all row-major without options).
@@ -627,8 +617,8 @@ int read_majors(gemm_epi_plan *pl, const ge_options *o) {
   pl->a_mn = o->a_major == GE_COL_MAJOR;
   pl->b_k = o->b_major == GE_COL_MAJOR;
   pl->cd_m = o->cd_major == GE_COL_MAJOR;
-  // A multicast splits the A tile by rows of a K-major tile
-  if (o->cluster_n == 2 && pl->a_mn) return GE_ERR_UNSUPPORTED;
+  // one CTA pair per cluster: no cluster multicast of operand tiles
+  if (o->cluster_n != 0 && o->cluster_n != 1) return GE_ERR_UNSUPPORTED;
   return GE_OK;
 }
 
@@ -698,9 +688,9 @@ int check_run_args(const gemm_epi_plan *pl, const void *A, const void *B, const 
 void log_plan(const gemm_epi_plan *pl) {
   const Layout &Lo = pl->lay;
   std::fprintf(stderr,
-               "[gemm_epi] L=%lld M=%lld N=%lld K=%lld: cta_group=%d x%d tile=%dx%dx%d stages=%d "
+               "[gemm_epi] L=%lld M=%lld N=%lld K=%lld: cta_group=%d tile=%dx%dx%d stages=%d "
                "aux_stages=%d grid=%d tiles=%d smem=%d program=%d ins/%d regs epilogue=%s\n",
-               (long long)pl->L, (long long)pl->M, (long long)pl->N, (long long)pl->K, Lo.cg, Lo.mc,
+               (long long)pl->L, (long long)pl->M, (long long)pl->N, (long long)pl->K, Lo.cg,
                BM * Lo.cg, Lo.bn, BK, Lo.stages, Lo.aux_stages, Lo.grid, Lo.num_tiles, Lo.smem_used,
                pl->prog.n_ins, pl->prog.n_regs,
                pl->epi >= 0                 ? catalog::kEntries[pl->epi].name
@@ -777,7 +767,6 @@ int gemm_epi_plan_create_ex(gemm_epi_plan **plan, int64_t L, int64_t M, int64_t 
   }
   fill_params(pl, pl->lay, pl->prog, &pl->kp);
   fill_params(pl, pl->lay_acc, pl->prog_acc, &pl->kp_acc);
-  pl->kp_acc.cd_m = 0;  // the unfused path's fp32 workspace is N-major
   if (log_enabled()) log_plan(pl);
   *plan = pl;
   return GE_OK;
@@ -806,7 +795,7 @@ int gemm_epi_plan_info(const gemm_epi_plan *pl, ge_plan_info *info) {
   info->n_regs = pl->prog.n_regs;
   info->num_sms = pl->num_sms;
   info->epi_variant = pl->epi;
-  info->cluster_n = pl->lay.mc;
+  info->cluster_n = 1;
   info->epi_warps = pl->lay.warps;
   return GE_OK;
 }
@@ -862,7 +851,7 @@ int gemm_epi_run_unfused(gemm_epi_plan *pl, const void *A, const void *B, const 
   if (!(pl->acc_maps_ok && pl->aA == A && pl->aB == B && pl->aWs == workspace)) {
     pl->acc_maps_ok = false;
     if (!encode_operands(pl, &ka, A, B)) return GE_ERR_CUDA;
-    if (!encode_epilogue_map(pl, &ka.tmOut[0], GE_F32, workspace, true)) return GE_ERR_CUDA;
+    if (!encode_epilogue_map(pl, &ka.tmOut[0], GE_F32, workspace)) return GE_ERR_CUDA;
     pl->aA = A;
     pl->aB = B;
     pl->aWs = workspace;
@@ -882,10 +871,12 @@ int gemm_epi_run_unfused(gemm_epi_plan *pl, const void *A, const void *B, const 
   for (int o = 0; o < pl->dt.n_out; ++o) ep.out_ptr[o] = outs[o];
   ep.prog = P;
   for (int i = 0; i < pl->dt.n_scalar; ++i) ep.prog.scalars[i] = scalars[i];
-  ep.rows = pl->L * pl->M;
   ep.N = static_cast<int32_t>(pl->N);
-  ep.chunks_per_row = static_cast<int32_t>((pl->N + kEwCols - 1) / kEwCols);
   ep.cd_m = pl->cd_m;
+  // units of 8 elements along the contiguous dimension: 8 columns of one of
+  // the L*M rows, or (M-major) 8 rows of one of the L*N columns
+  ep.rows = pl->cd_m ? pl->L * pl->N : pl->L * pl->M;
+  ep.chunks_per_row = static_cast<int32_t>(((pl->cd_m ? pl->M : pl->N) + kEwCols - 1) / kEwCols);
   const int64_t units = ep.rows * ep.chunks_per_row;
   const int64_t blocks = (units + kEwThreads - 1) / kEwThreads;
   const int grid = static_cast<int>(std::min<int64_t>(blocks, int64_t(pl->num_sms) * 16));
@@ -941,9 +932,8 @@ int configure_grouped(gemm_epi_plan *pl) {
   if (o.cta_group != 0 && o.cta_group != 1 && o.cta_group != 2) return GE_ERR_INVALID;
   if (o.tile_n != 0 && o.tile_n != 64 && o.tile_n != 128 && o.tile_n != 256) return GE_ERR_INVALID;
   if (o.stages < 0 || o.stages > kMaxStages || o.max_ctas < 0 || o.raster_group < 0 ||
-      o.timeout_ms < 0 || (o.cluster_n != 0 && o.cluster_n != 1 && o.cluster_n != 2))
+      o.timeout_ms < 0)
     return GE_ERR_INVALID;
-  if (o.cluster_n == 2) return GE_ERR_UNSUPPORTED;
   const int cand[5][2] = {{2, 256}, {2, 128}, {1, 256}, {1, 128}, {1, 64}};
   int sms = pl->num_sms;
   if (o.max_ctas) sms = std::min(sms, o.max_ctas);
@@ -980,7 +970,6 @@ int configure_grouped(gemm_epi_plan *pl) {
                    std::min(kMaxAuxStages, 2 * bn / EW), 4, warps);
   if (st != GE_OK) return st;
   Layout &Lo = pl->lay;
-  Lo.mc = 1;
   Lo.raster_group = o.raster_group ? o.raster_group : 8;
   int64_t tiles = 0;
   for (int j = 0; j < n; ++j) {
@@ -990,7 +979,7 @@ int configure_grouped(gemm_epi_plan *pl) {
   if (tiles > (int64_t(1) << 24)) return GE_ERR_SHAPE;  // the tile table: 16 bytes a tile
   Lo.num_tiles = static_cast<int>(tiles);
   Lo.num_full = Lo.num_tiles;  // grouped tiles are never split
-  const void *fn = resolve_kernel(pl, cg, bn, 1, pl->epi, Lo.warps, &pl->prog);
+  const void *fn = resolve_kernel(pl, cg, bn, pl->epi, Lo.warps, &pl->prog);
   if (!fn) return pl->epi == kEpiSpecialized ? GE_ERR_JIT : GE_ERR_INVALID;
   Lo.fn = fn;
   if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, Lo.smem) != cudaSuccess)

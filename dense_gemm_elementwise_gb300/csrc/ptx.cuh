@@ -136,18 +136,6 @@ __device__ __forceinline__ void tma_load_3d_pair(uint32_t dst, const CUtensorMap
       : "memory");
 }
 
-// CTA-pair form with cluster multicast: the same box lands at offset `dst` in
-// every CTA of `mask`; each destination's completion is counted on the
-// barrier at `bar`'s offset in the leader CTA of that destination's pair.
-__device__ __forceinline__ void tma_load_3d_pair_mc(uint32_t dst, const CUtensorMap *m, uint32_t bar,
-                                                    int32_t x, int32_t y, int32_t z, uint16_t mask) {
-  asm volatile(
-      "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
-      ".multicast::cluster [%0], [%1, {%3, %4, %5}], [%2], %6;" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(m)), "r"(bar), "r"(x), "r"(y), "r"(z), "h"(mask)
-      : "memory");
-}
-
 __device__ __forceinline__ void tma_store_3d(const CUtensorMap *m, uint32_t src, int32_t x,
                                              int32_t y, int32_t z) {
   asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%2, %3, %4}], [%1];" ::
@@ -234,8 +222,8 @@ __device__ __forceinline__ void umma_f16(uint32_t d_tmem, uint64_t a_desc, uint6
 }
 
 // arrive once on `bar` when every tcgen05 operation this thread issued so far
-// has completed; the pair form arrives on the same barrier offset in both CTAs
-// (pair form: on the same barrier offset in every CTA of `mask`)
+// has completed; the pair form arrives on the same barrier offset in every
+// CTA of `mask` (both CTAs of the pair)
 template <int CG>
 __device__ __forceinline__ void umma_commit(uint32_t bar, uint16_t mask = 0x3) {
   if constexpr (CG == 1) {

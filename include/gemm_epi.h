@@ -144,10 +144,9 @@ typedef struct {
   int32_t raster_group; /* 0 auto, else M tiles per raster group (L2 reuse of B)        */
   int32_t timeout_ms;   /* 0 = 1000; bound on every device-side wait                    */
   uint32_t debug_flags; /* 0; GE_DEBUG_* below, for tests only                          */
-  int32_t cluster_n;    /* 0 or 1: no multicast; 2 = two CTA pairs per 4-CTA cluster
-                           computing adjacent N tiles and sharing A by TMA multicast
-                           (cta_group 2, tile_n 256).  Opt-in: on GB300 only 36 such
-                           clusters fit (144 SMs), which offsets the traffic saved.     */
+  int32_t cluster_n;    /* 0 or 1 (one CTA, or one CTA pair, per cluster); any other
+                           value is GE_ERR_UNSUPPORTED.  Every TMA load lands in the
+                           issuing CTA's own shared memory: no cluster multicast.     */
   /* Storage order, packed in every case (GE_ERR_INVALID for other values):
    *   a_major   GE_ROW_MAJOR: A is (L,M,K), K contiguous ("K-major");
    *             GE_COL_MAJOR: stored (L,K,M), M contiguous ("M-major")
@@ -158,7 +157,7 @@ typedef struct {
    *             N contiguous; GE_COL_MAJOR stored (L,N,M), M contiguous.
    *             Row and column vectors are unaffected.
    * The contiguous dimension of each tensor must be whole 16-byte units
-   * (GE_ERR_MISALIGNED).  cluster_n 2 needs a K-major A (GE_ERR_UNSUPPORTED). */
+   * (GE_ERR_MISALIGNED). */
   int32_t a_major;
   int32_t b_major;
   int32_t cd_major;
@@ -208,7 +207,7 @@ typedef struct {
   int32_t epi_variant;                        /* built-in epilogue used; -1, -2: interpreter
                                                  (4 / 8 program registers); -3: compiled for
                                                  this program when the plan was made        */
-  int32_t cluster_n;                          /* CTA pairs sharing A per cluster         */
+  int32_t cluster_n;                          /* always 1: no operand sharing between pairs */
   int32_t epi_warps;                          /* epilogue warps per CTA (4 or 8)         */
 } ge_plan_info;
 
@@ -282,7 +281,9 @@ size_t gemm_epi_unfused_workspace_bytes(const gemm_epi_plan *plan);
  * `workspace`; launch 2: a vectorised elementwise kernel reads it back with
  * the aux operands and evaluates the same epilogue program, so results are
  * bit-identical to gemm_epi_run.
- *   workspace        caller-owned device buffer of >= gemm_epi_unfused_workspace_bytes
+ *   workspace        caller-owned device buffer of >= gemm_epi_unfused_workspace_bytes;
+ *                    it receives accum in the epilogue tensors' storage order
+ *                    ((L,M,N), or (L,N,M) with cd_major GE_COL_MAJOR)
  * Errors: as gemm_epi_run, plus GE_ERR_WORKSPACE.
  */
 int gemm_epi_run_unfused(gemm_epi_plan *plan, const void *A, const void *B,
@@ -308,7 +309,10 @@ int gemm_epi_run_unfused(gemm_epi_plan *plan, const void *A, const void *B,
  *    (L*M*N*4 bytes) are rejected with GE_ERR_WORKSPACE before any launch.
  *  * The first call on a device looks up that device's address of the array
  *    (cudaGetSymbolAddress, with that device current); make the first call on
- *    each device before any stream capture.
+ *    each device before any stream capture.  The address is kept for the
+ *    life of the process: after a cudaDeviceReset it, like every plan made
+ *    before the reset, is no longer valid, so do not use this library on
+ *    that device again in the same process.
  *  * All calls share the one array and it keeps whatever the last call left
  *    in it.  Nothing in it needs to start at zero: the GEMM overwrites every
  *    element it later reads.  Calls whose work overlaps on the GPU (different
@@ -342,8 +346,7 @@ typedef struct {
 
 /*
  * Build a grouped plan.  Validation as gemm_epi_plan_create_ex, per problem;
- * opts may be NULL (cluster_n 2 is not available for grouped plans:
- * GE_ERR_UNSUPPORTED).  The plan allocates its tables: four problem tables
+ * opts may be NULL.  The plan allocates its tables: four problem tables
  * in device memory and their pinned host staging (1.5 KiB per problem each)
  * and the launch's tile order (16 bytes per output tile), which it uploads
  * once with a synchronous copy (GE_ERR_CUDA if any of that fails).  Errors:

@@ -231,7 +231,8 @@ def test_grouped_run_rejects_null_plan():
 
 def test_majors_checked_before_device():
     """Storage orders: bad values, the contiguous dimension of each tensor
-    (per its major) in whole 16-byte units, multicast needing a K-major A."""
+    (per its major) in whole 16-byte units; no cluster of more than one
+    CTA pair (cluster_n 2 was an A-multicast option, since removed)."""
     dt, dag = _base()
     cases = [(dict(a_major=1), (1, 100, 128, 128), B.GE_ERR_MISALIGNED),
              (dict(b_major=1), (1, 128, 128, 100), B.GE_ERR_MISALIGNED),
@@ -239,7 +240,8 @@ def test_majors_checked_before_device():
              (dict(cd_major=1), (1, 100, 128, 128), B.GE_ERR_MISALIGNED),
              (dict(cd_major=-1), (1, 128, 128, 128), B.GE_ERR_INVALID),
              (dict(b_major=3), (1, 128, 128, 128), B.GE_ERR_INVALID),
-             (dict(a_major=1, cluster_n=2), (1, 128, 128, 128), B.GE_ERR_UNSUPPORTED)]
+             (dict(cluster_n=2), (1, 128, 128, 128), B.GE_ERR_UNSUPPORTED),
+             (dict(cluster_n=-1), (1, 128, 128, 128), B.GE_ERR_UNSUPPORTED)]
     for kw, (L, M, N, K), want in cases:
         with pytest.raises(B.GemmEpiError) as e:
             B.gemm_epi_plan_create(L, M, N, K, dt, B.make_dag(dag), B.ge_options(**kw))

@@ -205,10 +205,6 @@ def test_grouped_argument_errors():
         assert st == B.GE_ERR_INVALID
     finally:
         B.gemm_epi_plan_destroy(plan)
-    with pytest.raises(B.GemmEpiError) as e:
-        B.gemm_epi_grouped_plan_create(w.problems, dtypes_of(w), B.make_dag(w.dag),
-                                       B.ge_options(cluster_n=2))
-    assert e.value.status == B.GE_ERR_UNSUPPORTED
 
 
 def test_grouped_device_wait_timeout_is_reported():

@@ -102,9 +102,7 @@ def test_majors_alignment_and_option_errors():
              (dict(a_major=0), (1, 100, 128, 128), B.GE_OK),
              (dict(b_major=1), (1, 128, 128, 100), B.GE_ERR_MISALIGNED),   # K*2 bytes
              (dict(cd_major=1), (1, 100, 128, 128), B.GE_ERR_MISALIGNED),  # M*2 bytes (C, D)
-             (dict(a_major=2), (1, 128, 128, 128), B.GE_ERR_INVALID),
-             (dict(a_major=1, cluster_n=2, cta_group=2, tile_n=256), (1, 512, 512, 128),
-              B.GE_ERR_UNSUPPORTED)]
+             (dict(a_major=2), (1, 128, 128, 128), B.GE_ERR_INVALID)]
     for kw, (L, M, N, K), want in cases:
         try:
             plan = B.gemm_epi_plan_create(L, M, N, K, dt, dag, B.ge_options(**kw))

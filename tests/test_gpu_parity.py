@@ -55,28 +55,27 @@ def test_page_examples(w):
 
 SHAPES = [(1, 1, 8, 8), (1, 8, 8, 8), (1, 129, 136, 72), (3, 200, 264, 200),
           (2, 257, 520, 1000), (1, 300, 24, 64), (1, 64, 1032, 136), (2, 513, 392, 8)]
-# (cta_group, tile N, CTA pairs per cluster sharing A by multicast)
-VARIANTS = [(1, 64, 1), (1, 128, 1), (1, 256, 1), (2, 128, 1), (2, 256, 1), (2, 256, 2)]
+# (cta_group, tile N)
+VARIANTS = [(1, 64), (1, 128), (1, 256), (2, 128), (2, 256)]
 
 
 def opts(variant, **kw):
-    return B.ge_options(cta_group=variant[0], tile_n=variant[1], cluster_n=variant[2], **kw)
+    return B.ge_options(cta_group=variant[0], tile_n=variant[1], **kw)
 
 
 def vid(v):
-    return "cg%d_n%d_x%d" % v
+    return "cg%d_n%d" % v
 
 
 @pytest.mark.parametrize("shape", SHAPES, ids=lambda s: "x".join(map(str, s)))
 @pytest.mark.parametrize("variant", VARIANTS, ids=vid)
 def test_ragged_shapes_exact(shape, variant):
     """Integer inputs: every kernel variant must be bit-exact on ragged M, N,
-    K (TMA zero-fills loads and clips stores at the edges; with multicast an
-    odd number of N tiles leaves the second pair's tile out of range)."""
+    K (TMA zero-fills loads and clips stores at the edges)."""
     w = small(W.MY_EPILOGUE_128, *shape)
     inputs = W.make_inputs(w)
     gpu, info = _gpu.run_gpu(w, inputs, options=opts(variant))
-    assert (info["cta_group"], info["tile_n"], info["cluster_n"]) == variant
+    assert (info["cta_group"], info["tile_n"]) == variant
     _gpu.compare(w, gpu, _gpu.oracle_rows(w, inputs))
 
 
@@ -89,43 +88,40 @@ def test_bf16_bias_relu_square_variants(variant):
 
 
 @pytest.mark.parametrize("stages", [2, 3, 4])
-@pytest.mark.parametrize("cluster_n", [1, 2])
-def test_few_stages(stages, cluster_n):
+def test_few_stages(stages):
     """Short rings wrap the stage/phase bookkeeping many times per tile."""
     w = small(W.ALPHA_BETA_X_8192, 1, 512, 1024, 1024)
     inputs = W.make_inputs(w)
     gpu, info = _gpu.run_gpu(w, inputs, options=B.ge_options(
-        stages=stages, cta_group=2, tile_n=256, cluster_n=cluster_n))
+        stages=stages, cta_group=2, tile_n=256))
     assert info["stages"] == stages
     _gpu.compare(w, gpu, _gpu.oracle_rows(w, inputs))
 
 
-@pytest.mark.parametrize("cluster_n", [1, 2])
-def test_small_grid_many_tiles_per_cta(cluster_n):
+def test_small_grid_many_tiles_per_cta():
     """Four CTAs loop over many tiles: both TMEM accumulators, the aux
     prefetch across tile boundaries and the raster order all wrap."""
     w = small(W.ALPHA_BETA_X_8192, 2, 1024, 768, 256)
     inputs = W.make_inputs(w)
     gpu, info = _gpu.run_gpu(w, inputs, options=B.ge_options(
-        max_ctas=4, raster_group=3, cta_group=2, tile_n=256, cluster_n=cluster_n))
-    assert info["grid"] <= 4 and info["cluster_n"] == cluster_n
+        max_ctas=4, raster_group=3, cta_group=2, tile_n=256))
+    assert info["grid"] <= 4 and info["cluster_n"] == 1
     _gpu.compare(w, gpu, _gpu.oracle_rows(w, inputs))
 
 
-@pytest.mark.parametrize("variant", [(1, 128, 1), (2, 256, 1), (2, 256, 2)],
-                         ids=lambda v: "cg%d_n%d_mc%d" % v)
+@pytest.mark.parametrize("variant", [(1, 128), (2, 256)], ids=lambda v: "cg%d_n%d" % v)
 def test_k_snake_with_ragged_k(variant):
     """A few CTAs loop over many tiles, so half of their tiles walk K
     backwards and start on the partial last k-block (K = 200 and 1000 are
     not multiples of 64): bit-exact against the oracle, and the unfused
     path (same schedule) bit-identical."""
-    cg, bn, mc = variant
+    cg, bn = variant
     for K in (200, 1000):
         w = small(W.MY_EPILOGUE_128, 2, 520, 776, K)
         inputs = W.make_inputs(w)
-        opts = B.ge_options(max_ctas=2 * cg * mc, cta_group=cg, tile_n=bn, cluster_n=mc)
+        opts = B.ge_options(max_ctas=2 * cg, cta_group=cg, tile_n=bn)
         gpu, info = _gpu.run_gpu(w, inputs, options=opts)
-        assert info["num_tiles"] >= 4 * info["grid"] // (cg * mc)
+        assert info["num_tiles"] >= 4 * info["grid"] // cg
         _gpu.compare(w, gpu, _gpu.oracle_rows(w, inputs))
         unf, _ = _gpu.run_gpu(w, inputs, options=opts, unfused=True)
         _gpu.bitwise_equal(gpu, unf)
@@ -162,7 +158,7 @@ def test_variants_agree_on_normal_inputs():
     w = small(W.ALPHA_BETA_X_8192, 1, 512, 512, 2048)
     inputs = W.make_inputs(w)
     base, _ = _gpu.run_gpu(w, inputs, options=opts(VARIANTS[4]))
-    for v in VARIANTS[:4] + VARIANTS[5:]:
+    for v in VARIANTS[:4]:
         other, _ = _gpu.run_gpu(w, inputs, options=opts(v))
         for a, b in zip(base, other):
             assert torch.allclose(a.float(), b.float(), rtol=1e-3, atol=1e-2)
@@ -205,15 +201,14 @@ def test_run_argument_errors():
         B.gemm_epi_plan_destroy(plan)
 
 
-@pytest.mark.parametrize("cluster_n", [1, 2])
-def test_device_wait_timeout_is_reported(cluster_n):
+def test_device_wait_timeout_is_reported():
     """A k-block that is never loaded: the MMA warp's bounded wait runs out,
     the kernel records GE_ERR_TIMEOUT, drains and exits; the context stays
     usable and the next run is correct."""
     w = small(W.MY_EPILOGUE_128, 1, 256, 256, 256)
     inputs = W.make_inputs(w)
     opt = B.ge_options(timeout_ms=50, debug_flags=B.GE_DEBUG_SKIP_FIRST_LOAD,
-                       max_ctas=2 * cluster_n, cta_group=2, tile_n=256, cluster_n=cluster_n)
+                       max_ctas=2, cta_group=2, tile_n=256)
     A, Bm, aux, sc = inputs
     dev = torch.device("cuda")
     outs = [torch.empty(1, 256, 256, dtype=torch.float16, device=dev) for _ in range(2)]
@@ -247,12 +242,12 @@ CATALOG_CASES = [small(W.MY_EPILOGUE_128, 2, 300, 392, 200), small(W.RELU_2400X3
 
 
 @pytest.mark.parametrize("w", CATALOG_CASES, ids=lambda w: w.name)
-@pytest.mark.parametrize("variant", [(1, 64, 1), (2, 256, 2)], ids=vid)
+@pytest.mark.parametrize("variant", [(1, 64), (2, 256)], ids=vid)
 def test_builtin_and_interpreter_agree_bitwise(w, variant):
     """The straight-line kernels and the interpreter evaluate the same
     compiled program in the same order: identical bits, fused and unfused."""
     inputs = W.make_inputs(w)
-    base = dict(cta_group=variant[0], tile_n=variant[1], cluster_n=variant[2])
+    base = dict(cta_group=variant[0], tile_n=variant[1])
     fast, info = _gpu.run_gpu(w, inputs, options=B.ge_options(**base))
     slow, info2 = _gpu.run_gpu(w, inputs, options=B.ge_options(
         debug_flags=B.GE_DEBUG_FORCE_INTERPRETER, **base))
@@ -285,7 +280,7 @@ def _reverse_ops_workload():
                       exact=True)
 
 
-@pytest.mark.parametrize("variant", [(1, 128, 1), (2, 256, 1)], ids=vid)
+@pytest.mark.parametrize("variant", [(1, 128), (2, 256)], ids=vid)
 def test_reversed_sub_div_and_min(variant):
     w = _reverse_ops_workload()
     inputs = W.make_inputs(w)
@@ -318,7 +313,7 @@ def _ulp(v, dt):
 
 
 @pytest.mark.parametrize("w", ACT_CASES, ids=lambda w: w.name)
-@pytest.mark.parametrize("variant", [(1, 128, 1), (2, 256, 1)], ids=vid)
+@pytest.mark.parametrize("variant", [(1, 128), (2, 256)], ids=vid)
 def test_activations_within_one_ulp(w, variant):
     """The fp32 activations (CUDA math library) against the fp64 oracle.
     The activation's argument differs between the two sides by at most the
@@ -391,7 +386,7 @@ def _leaky_workloads():
 
 
 @pytest.mark.parametrize("w", _leaky_workloads(), ids=lambda w: w.name)
-@pytest.mark.parametrize("variant", [(1, 128, 1), (2, 256, 1)], ids=vid)
+@pytest.mark.parametrize("variant", [(1, 128), (2, 256)], ids=vid)
 def test_leaky_relu_forms(w, variant):
     inputs = W.make_inputs(w)
     gpu, info = _gpu.run_gpu(w, inputs, options=opts(variant))
@@ -406,13 +401,12 @@ def test_leaky_relu_forms(w, variant):
                          [x for x in CATALOG_CASES if x.name in ("complex_gelu_tanh",
                                                                   "row_col_bias_f16")],
                          ids=lambda w: w.name)
-@pytest.mark.parametrize("variant", [(1, 64, 1), (1, 256, 1), (2, 128, 1), (2, 256, 1),
-                                     (2, 256, 2)], ids=vid)
+@pytest.mark.parametrize("variant", [(1, 64), (1, 256), (2, 128), (2, 256)], ids=vid)
 def test_eight_epilogue_warps_bitwise(w, variant):
     """Two warps per accumulator lane quarter, each taking every other
     32-column step: the same bits as four warps, and the oracle's values."""
     inputs = W.make_inputs(w)
-    base = dict(cta_group=variant[0], tile_n=variant[1], cluster_n=variant[2])
+    base = dict(cta_group=variant[0], tile_n=variant[1])
     four, i4 = _gpu.run_gpu(w, inputs, options=B.ge_options(epi_warps=4, **base))
     eight, i8 = _gpu.run_gpu(w, inputs, options=B.ge_options(epi_warps=8, **base))
     assert i8["epi_variant"] >= 0
@@ -432,12 +426,12 @@ def test_eight_epilogue_warps_rules():
                          [x for x in CATALOG_CASES if x.name in ("act_sigmoid", "clamp_f16",
                                                                   "aux_normalize_f16")],
                          ids=lambda w: w.name)
-@pytest.mark.parametrize("variant", [(1, 128, 1), (2, 256, 1)], ids=vid)
+@pytest.mark.parametrize("variant", [(1, 128), (2, 256)], ids=vid)
 def test_interpreter_eight_warps_bitwise(w, variant):
     """The interpreter on 8 warps: the same bits as on 4 and as the
     built-in kernels."""
     inputs = W.make_inputs(w)
-    base = dict(cta_group=variant[0], tile_n=variant[1], cluster_n=variant[2],
+    base = dict(cta_group=variant[0], tile_n=variant[1],
                 debug_flags=B.GE_DEBUG_FORCE_INTERPRETER)
     four, i4 = _gpu.run_gpu(w, inputs, options=B.ge_options(epi_warps=4, **base))
     eight, i8 = _gpu.run_gpu(w, inputs, options=B.ge_options(epi_warps=8, **base))
