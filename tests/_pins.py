@@ -330,6 +330,25 @@ def pin_integer_closed_form(L_):
     assert np.array_equal(np_decode(D, "f16"), ref.astype(np.float64))
 
 
+def pin_gemm_accum_closed_form(L_):
+    """The accumulator alone, before any epilogue ("CUTLASS Operator API:
+    Custom epilogue fusions for GEMMs": accum is the GEMM result the
+    epilogue receives), on integer inputs: the exact int64 product, per
+    batch, for every row and for an unordered row subset spread over the
+    batches, fp16 and bf16 operands, one thread and several."""
+    for w in (small(W.MY_EPILOGUE_128, L=3, M=20, N=24, K=72),
+              small(W.BIAS_RELU_SQUARE_L8, L=2, M=12, N=40, K=56, dist="randint")):
+        (A, B, _, _), Ai, Bi, _ = _int_inputs(w)
+        want = np.einsum("lik,lkj->lij", Ai, Bi).reshape(w.L * w.M, w.N).astype(np.float64)
+        full = oracle.gemm_accum(w.L, w.M, w.N, w.K, w.ab, W.to_codes(A), W.to_codes(B),
+                                 threads=1, lib_handle=L_)
+        assert np.array_equal(full, want), w.name
+        rows = np.array([w.L * w.M - 1, 0, w.M + 3, 7, w.M, 2 * w.M - 1], dtype=np.int64)
+        part = oracle.gemm_accum(w.L, w.M, w.N, w.K, w.ab, W.to_codes(A), W.to_codes(B),
+                                 rows=rows, threads=3, lib_handle=L_)
+        assert np.array_equal(part, want[rows]), w.name
+
+
 def pin_new_ops_closed_form(L_):
     """Integer inputs through subtraction, division by powers of two, min,
     max and row + column broadcasts: the exact results, computed in numpy."""
@@ -575,6 +594,7 @@ def pin_rows_and_threads(L_):
 
 ALL_PINS = [pin_decode_exhaustive, pin_encode_roundtrip, pin_encode_midpoints,
             pin_encode_random_vs_table, pin_golden, pin_integer_closed_form,
+            pin_gemm_accum_closed_form,
             pin_broadcast_closed_form, pin_new_ops_closed_form, pin_activation_identities,
             pin_grouped_closed_form,
             pin_fraction_brute_force,

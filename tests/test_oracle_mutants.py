@@ -65,6 +65,10 @@ MUTANTS = [
      "case ORC_SILU: v[n] = v[nd->a] / (1.0 + exp(v[nd->a]));"),
     ("hardswish_clamp_3", "c = c < 0.0 ? 0.0 : (c > 6.0 ? 6.0 : c);",
      "c = c < 0.0 ? 0.0 : (c > 3.0 ? 3.0 : c);"),
+    ("accum_drops_last_column", "memcpy(jb->acc_rows + out_row * N, acc, sizeof(double) * (size_t)N);",
+     "memcpy(jb->acc_rows + out_row * N, acc, sizeof(double) * (size_t)(N - 1));"),
+    ("accum_row_by_job_index", "memcpy(jb->acc_rows + out_row * N, acc,",
+     "memcpy(jb->acc_rows + t * N, acc,"),
     ("leaky_side", "case ORC_LEAKY_RELU: v[n] = v[nd->a] > 0.0 ? v[nd->a] : v[nd->b] * v[nd->a];",
      "case ORC_LEAKY_RELU: v[n] = v[nd->a] < 0.0 ? v[nd->a] : v[nd->b] * v[nd->a];"),
 ]
