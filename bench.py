@@ -61,6 +61,8 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-unfused", action="store_true")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip the other workloads' figures (the configs object)")
     return ap.parse_args()
 
 
@@ -203,6 +205,7 @@ class ClockSampler:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
         samples = self._samples()
         inside = [x for x in samples if t0 <= x[0] <= t1]
+        n_inside = len(inside)
         where = "timed region"
         if not inside:
             inside = [x for x in samples if t0 - 0.25 <= x[0] <= t1 + 0.25]
@@ -213,13 +216,81 @@ class ClockSampler:
         return {"sm_mhz": statistics.median(x[1] for x in inside),
                 "sm_max_mhz": max(x[2] for x in inside),
                 "reasons": sorted({r for x in inside for r in x[4]}),
-                "samples": len(inside), "window": where,
+                "samples": len(inside), "samples_inside_region": n_inside, "window": where,
                 "window_s": round(t1 - t0, 3),
                 "power_w_median": statistics.median(x[3] for x in inside),
                 "power_w_max": max(x[3] for x in inside)}
 
 
 # ------------------------------------------------------------ helpers ---
+
+def _numa_nodes_of(addr_lo, addr_hi):
+    """NUMA nodes holding the pages of [addr_lo, addr_hi) of this process
+    (from /proc/self/numa_maps: per mapping, pages resident on each node)."""
+    nodes = {}
+    try:
+        with open("/proc/self/numa_maps") as f:
+            lines = f.readlines()
+        with open("/proc/self/maps") as f:
+            spans = {}
+            for ln in f:
+                lo, hi = (int(x, 16) for x in ln.split()[0].split("-"))
+                spans[lo] = hi
+    except OSError:
+        return None
+    for ln in lines:
+        parts = ln.split()
+        lo = int(parts[0], 16)
+        hi = spans.get(lo, lo)
+        if hi <= addr_lo or lo >= addr_hi:
+            continue
+        for p in parts[1:]:
+            if p.startswith("N") and "=" in p:
+                k, v = p[1:].split("=", 1)
+                if k.isdigit():
+                    nodes[int(k)] = nodes.get(int(k), 0) + int(v)
+    return nodes
+
+
+def host_numa_note(local, tensors=()):
+    """Where the end-to-end leg's pinned host buffers sit relative to the
+    GPU: the GPU's NUMA node (sysfs), the nodes of this process's CPUs, and
+    the nodes holding the buffers' pages."""
+    import torch
+    out = {}
+    try:
+        p = torch.cuda.get_device_properties(local)
+        bus = "%04x:%02x:%02x.0" % (p.pci_domain_id, p.pci_bus_id, p.pci_device_id)
+    except (AttributeError, RuntimeError):
+        bus = None
+    if bus:
+        try:
+            with open("/sys/bus/pci/devices/%s/numa_node" % bus.lower()) as f:
+                out["gpu_numa_node"] = int(f.read().strip())
+        except (OSError, ValueError):
+            out["gpu_numa_node"] = None
+        out["gpu_pci"] = bus.lower()
+    try:
+        cpus = sorted(os.sched_getaffinity(0))
+        cnodes = set()
+        for c in cpus:
+            d = "/sys/devices/system/cpu/cpu%d" % c
+            for name in os.listdir(d):
+                if name.startswith("node") and name[4:].isdigit():
+                    cnodes.add(int(name[4:]))
+        out["cpu_numa_nodes"] = sorted(cnodes)
+    except OSError:
+        pass
+    pages = {}
+    for t in tensors:
+        lo = t.data_ptr()
+        got = _numa_nodes_of(lo, lo + t.numel() * t.element_size())
+        for k, v in (got or {}).items():
+            pages[k] = pages.get(k, 0) + v
+    if tensors:
+        out["buffer_pages_by_node"] = {str(k): v for k, v in sorted(pages.items())}
+    return out
+
 
 def dist_setup(n):
     rank = int(os.environ.get("RANK", "0"))
@@ -334,6 +405,126 @@ def run_reference(args, w):
 
 # ------------------------------------------------------------ our arm ---
 
+def parse_opts(B, text):
+    if not text:
+        return None
+    return B.ge_options(**{k: int(v) for k, v in (kv.split("=") for kv in text.split(","))})
+
+
+def l2_note(flush, in_bytes):
+    if flush:
+        return ("flushed before every timed step: 512 MiB write, then 256 MiB read "
+                "(inputs %d MiB)" % (in_bytes >> 20))
+    return "no flush: inputs (%d MiB) larger than twice the L2" % (in_bytes >> 20)
+
+
+class Measured:
+    """One workload planned, resident in device memory and timed under the
+    benchmark's protocol: W warm-up launches, then K timed ones, each between
+    CUDA events on the launch stream, the L2 flushed before every timed
+    launch when the inputs are smaller than twice the L2."""
+
+    def __init__(self, w, dev_, stream, world, opts, host_inputs=None):
+        import torch
+
+        from dense_gemm_elementwise_gb300 import binding as B
+        from dense_gemm_elementwise_gb300 import workloads as W
+        self.w, self.dev, self.stream, self.world, self.opts = w, dev_, stream, world, opts
+        self.B = B
+        self.inputs = host_inputs if host_inputs is not None else W.make_inputs(w)
+        A, Bm, aux, self.scalars = self.inputs
+        self.Ad, self.Bd = A.to(dev_), Bm.to(dev_)
+        self.auxd = [a.to(dev_) for a in aux]
+        self.outs = [torch.empty(w.L, w.M, w.N, dtype=W.TORCH_DTYPE[dt], device=dev_)
+                     for _, dt in w.outs]
+        self.dtypes = B.make_dtypes(w.ab, [s[2] for s in w.aux], len(w.scalars),
+                                    [dt for _, dt in w.outs])
+        self.plan = B.gemm_epi_plan_create(w.L, w.M, w.N, w.K, self.dtypes, B.make_dag(w.dag),
+                                           opts)
+        self.info = B.gemm_epi_plan_info(self.plan)
+        self.flops = w.flops()
+        self.in_bytes = w.alg_bytes() - sum(w.L * w.M * w.N * W.ESIZE[dt] for _, dt in w.outs)
+        # inputs smaller than twice the L2: flush it before every timed step by
+        # writing 512 MiB and reading 256 MiB (the read pays the write-back of
+        # the dirty lines before the step starts)
+        self.flush_l2 = self.in_bytes < 2 * L2_BYTES
+        if self.flush_l2:
+            self.fbuf = torch.empty(512 << 20, dtype=torch.uint8, device=dev_)
+            self.cbuf = torch.ones(64 << 20, dtype=torch.float32, device=dev_)
+
+    def timed(self, fn, steps):
+        """CUDA events around every step on the launch stream; returns ms/step."""
+        import torch
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(steps)]
+        torch.cuda.synchronize()
+        barrier(self.world)
+        torch.cuda.synchronize()
+        with torch.cuda.stream(self.stream):
+            for s, e in evs:
+                if self.flush_l2:
+                    self.fbuf.zero_()
+                    self.cbuf.sum()
+                s.record(self.stream)
+                fn()
+                e.record(self.stream)
+        torch.cuda.synchronize()
+        barrier(self.world)
+        torch.cuda.synchronize()
+        return sum(s.elapsed_time(e) for s, e in evs) / steps
+
+    def fused(self):
+        self.B.gemm_epi_run(self.plan, self.Ad, self.Bd, self.auxd, self.scalars, self.outs,
+                            stream=self.stream)
+
+    def run_fused(self, steps, warmup):
+        import torch
+        for _ in range(warmup):
+            self.fused()
+        torch.cuda.synchronize()
+        if self.B.gemm_epi_last_error(self.plan) != self.B.GE_OK:
+            raise RuntimeError("device-side timeout during warm-up (%s)" % self.w.name)
+        ms = self.timed(self.fused, steps)
+        if self.B.gemm_epi_last_error(self.plan) != self.B.GE_OK:
+            raise RuntimeError("device-side timeout during the timed region (%s)" % self.w.name)
+        return ms
+
+    def run_unfused(self, steps, warmup, ms_fused):
+        import torch
+        B, w = self.B, self.w
+        ws = torch.empty(B.gemm_epi_unfused_workspace_bytes(self.plan) // 4,
+                         dtype=torch.float32, device=self.dev)
+
+        def unf():
+            B.gemm_epi_run_unfused(self.plan, self.Ad, self.Bd, self.auxd, self.scalars,
+                                   self.outs, ws, stream=self.stream)
+
+        for _ in range(warmup):
+            unf()
+        ums = self.timed(unf, steps)
+        del ws
+        return {"ms_per_step": ums, "value": self.flops / (ums * 1e-3) / 1e12,
+                "fused_speedup": ums / ms_fused, "launches_per_step": 2,
+                "extra_bytes_per_step": 8 * w.L * w.M * w.N}
+
+    def close(self):
+        if self.plan is not None:
+            self.B.gemm_epi_plan_destroy(self.plan)
+            self.plan = None
+
+
+def config_entry(m, ms, unfused):
+    """One workload's figures for the bench line's ``configs`` object."""
+    w = m.w
+    roof = roofline(m.flops, w.alg_bytes(), ms, ncu_traffic(w.name))
+    return {"workload": w.name, "L": w.L, "M": w.M, "N": w.N, "K": w.K, "ab_dtype": w.ab,
+            "outs": [n + ":" + dt for n, dt in w.outs],
+            "ms_per_step": ms, "value": m.flops / (ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+            "roofline": {k: roof[k] for k in ("bound", "achieved", "peak", "unit", "frac",
+                                              "traffic", "tensor_frac", "hbm_frac")},
+            "unfused": unfused, "l2": l2_note(m.flush_l2, m.in_bytes), "plan": m.info}
+
+
 def run_ours(args, w):
     import torch
 
@@ -345,64 +536,22 @@ def run_ours(args, w):
     dev_ = torch.device("cuda", local)
     stream = torch.cuda.Stream(device=dev_)
     clocks = ClockSampler(local).start()
-    inputs = W.make_inputs(w)
+    opts = parse_opts(B, args.opt)
+    m = Measured(w, dev_, stream, world, opts)
+    inputs = m.inputs
     A, Bm, aux, scalars = inputs
-    Ad, Bd = A.to(dev_), Bm.to(dev_)
-    auxd = [a.to(dev_) for a in aux]
-    outs = [torch.empty(w.L, w.M, w.N, dtype=W.TORCH_DTYPE[dt], device=dev_) for _, dt in w.outs]
-    dtypes = B.make_dtypes(w.ab, [s[2] for s in w.aux], len(w.scalars),
-                           [dt for _, dt in w.outs])
-    opts = None
-    if args.opt:
-        opts = B.ge_options(**{k: int(v) for k, v in (kv.split("=") for kv in args.opt.split(","))})
-    plan = B.gemm_epi_plan_create(w.L, w.M, w.N, w.K, dtypes, B.make_dag(w.dag), opts)
-    info = B.gemm_epi_plan_info(plan)
-    flops = w.flops()
-    in_bytes = w.alg_bytes() - sum(w.L * w.M * w.N * W.ESIZE[dt] for _, dt in w.outs)
-    # inputs smaller than twice the L2: flush it before every timed step by
-    # writing 512 MiB and reading 256 MiB (the read pays the write-back of
-    # the dirty lines before the step starts)
-    flush_l2 = in_bytes < 2 * L2_BYTES
-    if flush_l2:
-        fbuf = torch.empty(512 << 20, dtype=torch.uint8, device=dev_)
-        cbuf = torch.ones(64 << 20, dtype=torch.float32, device=dev_)
-
-    def timed(fn, steps):
-        """CUDA events around every step on the launch stream; returns ms/step."""
-        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-               for _ in range(steps)]
-        torch.cuda.synchronize()
-        barrier(world)
-        torch.cuda.synchronize()
-        with torch.cuda.stream(stream):
-            for s, e in evs:
-                if flush_l2:
-                    fbuf.zero_()
-                    cbuf.sum()
-                s.record(stream)
-                fn()
-                e.record(stream)
-        torch.cuda.synchronize()
-        barrier(world)
-        torch.cuda.synchronize()
-        return sum(s.elapsed_time(e) for s, e in evs) / steps
-
-    def fused():
-        B.gemm_epi_run(plan, Ad, Bd, auxd, scalars, outs, stream=stream)
+    info, flops, dtypes = m.info, m.flops, m.dtypes
 
     for _ in range(args.warmup):
-        fused()
+        m.fused()
     torch.cuda.synchronize()
-    if B.gemm_epi_last_error(plan) != B.GE_OK:
+    if B.gemm_epi_last_error(m.plan) != B.GE_OK:
         raise RuntimeError("device-side timeout during warm-up")
     t_begin = time.time()
-    ms = timed(fused, args.steps)
+    ms = m.timed(m.fused, args.steps)
     t_end = time.time()
-    time.sleep(0.1)  # the first sample after the region is in
-    clocks.stop()
-    clk = clocks.window(t_begin, t_end)
     ms_max = max_over_ranks(ms, world)
-    if B.gemm_epi_last_error(plan) != B.GE_OK:
+    if B.gemm_epi_last_error(m.plan) != B.GE_OK:
         raise RuntimeError("device-side timeout during the timed region")
     value = world * flops / (ms_max * 1e-3) / 1e12
 
@@ -410,19 +559,7 @@ def run_ours(args, w):
 
     unfused = None
     if not args.no_unfused:
-        ws = torch.empty(B.gemm_epi_unfused_workspace_bytes(plan) // 4, dtype=torch.float32,
-                         device=dev_)
-
-        def unf():
-            B.gemm_epi_run_unfused(plan, Ad, Bd, auxd, scalars, outs, ws, stream=stream)
-
-        for _ in range(max(3, args.warmup // 4)):
-            unf()
-        ums = timed(unf, max(3, args.steps // 4))
-        unfused = {"ms_per_step": ums, "value": flops / (ums * 1e-3) / 1e12,
-                   "fused_speedup": ums / ms, "launches_per_step": 2,
-                   "extra_bytes_per_step": 8 * w.L * w.M * w.N}
-        del ws
+        unfused = m.run_unfused(max(3, args.steps // 4), max(3, args.warmup // 4), ms)
 
     e2e = None
     if not args.no_e2e:
@@ -430,6 +567,7 @@ def run_ours(args, w):
         # inputs from pinned host memory and its outputs back.  Steps are
         # pipelined over three streams (H2D of step i+1, compute of step i,
         # D2H of step i-1) with two device buffer sets, ordered by events.
+        Ad, Bd, auxd, outs = m.Ad, m.Bd, m.auxd, m.outs
         hA, hB = A.pin_memory(), Bm.pin_memory()
         haux = [a.pin_memory() for a in aux]
         houts = [[torch.empty(o.shape, dtype=o.dtype).pin_memory() for o in outs] for _ in range(2)]
@@ -438,7 +576,8 @@ def run_ours(args, w):
         dev = [(Ad, Bd, auxd, outs),
                (torch.empty_like(Ad), torch.empty_like(Bd), [torch.empty_like(a) for a in auxd],
                 [torch.empty_like(o) for o in outs])]
-        plans = [plan, B.gemm_epi_plan_create(w.L, w.M, w.N, w.K, dtypes, B.make_dag(w.dag), opts)]
+        plans = [m.plan, B.gemm_epi_plan_create(w.L, w.M, w.N, w.K, dtypes, B.make_dag(w.dag),
+                                                opts)]
         s_in, s_out = torch.cuda.Stream(device=dev_), torch.cuda.Stream(device=dev_)
         ev_in = [torch.cuda.Event() for _ in range(2)]
         ev_done = [torch.cuda.Event() for _ in range(2)]
@@ -481,15 +620,41 @@ def run_ours(args, w):
         barrier(world)
         ems = max_over_ranks(t0.elapsed_time(t1) / e_steps, world)
         B.gemm_epi_plan_destroy(plans[1])
+        del dev, houts
         e2e = {"value": world * flops / (ems * 1e-3) / 1e12, "unit": "TFLOP/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e_steps,
-               "ms_per_step": ems, "pipelined_streams": 3}
+               "ms_per_step": ems, "pipelined_streams": 3,
+               "host_memory": host_numa_note(local, [hA, hB] + haux)}
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(w, inputs)
 
-    B.gemm_epi_plan_destroy(plan)
+    # every workload of the task's table under the same protocol (the headline
+    # figures above are its entry), with the fused kernel's roofline and the
+    # unfused comparison; default-sized workloads only (not under --mnk)
+    configs = None
+    if not args.no_configs and not args.mnk:
+        configs = {}
+        for cw in W.WORKLOADS:
+            if cw.name == w.name:
+                configs[cw.name] = config_entry(m, ms, unfused)
+                continue
+            cm = Measured(cw, dev_, stream, world, None)
+            try:
+                cms = cm.run_fused(args.steps, args.warmup)
+                cun = None if args.no_unfused else cm.run_unfused(
+                    max(3, args.steps // 4), max(3, args.warmup // 4), cms)
+                configs[cw.name] = config_entry(cm, cms, cun)
+            finally:
+                cm.close()
+            del cm
+            torch.cuda.empty_cache()
+
+    time.sleep(0.1)  # the first sample after the region is in
+    clocks.stop()
+    clk = clocks.window(t_begin, t_end)
+    m.close()
     if rank != 0:
         return
     line = {
@@ -497,14 +662,11 @@ def run_ours(args, w):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_max,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": w.ab, "data": "synthetic",
-        "config": dict(workload_config(w, world), **{
-            "l2": ("flushed before every timed step: 512 MiB write, then 256 MiB read "
-                   "(inputs %d MiB)" % (in_bytes >> 20) if flush_l2 else
-                   "no flush: inputs (%d MiB) larger than twice the L2" % (in_bytes >> 20)),
-            "plan": info, "options": args.opt or "auto"}),
+        "config": workload_config(w, world),
+        "l2": l2_note(m.flush_l2, m.in_bytes), "plan": info, "options": args.opt or "auto",
         "pct_of_peak": 100.0 * roof["tensor_frac"],
         "roofline": roof, "gpu_launches": args.steps, "clocks": clk,
-        "unfused": unfused, "e2e": e2e, "cpu_baseline": cpu,
+        "unfused": unfused, "e2e": e2e, "cpu_baseline": cpu, "configs": configs,
     }
     print(json.dumps(line), flush=True)
 

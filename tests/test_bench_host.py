@@ -92,3 +92,15 @@ def test_roofline_takes_the_binding_bound(monkeypatch):
     assert small["bound"] == "hbm" and small["unit"] == "GB/s" and small["peak"] == 8000.0
     assert abs(small["achieved"] - 10485760 / 0.0148e-3 / 1e9) < 1e-6
     assert abs(small["frac"] - small["hbm_frac"]) < 1e-12 and small["tensor_frac"] < small["frac"]
+
+
+def test_numa_pages_of_a_host_buffer_are_found():
+    """The end-to-end leg reports which NUMA nodes hold its pinned buffers;
+    on any Linux host a touched buffer's pages are found on some node."""
+    import numpy as np
+    bench = load_bench()
+    if not os.path.exists("/proc/self/numa_maps"):
+        return
+    a = np.ones(1 << 20)
+    nodes = bench._numa_nodes_of(a.ctypes.data, a.ctypes.data + a.nbytes)
+    assert nodes and sum(nodes.values()) >= a.nbytes // (1 << 21)
