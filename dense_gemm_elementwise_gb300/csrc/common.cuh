@@ -95,14 +95,19 @@ struct EpiProgram {
 constexpr int BM = 128;      // accumulator rows per CTA (TMEM lanes)
 constexpr int BK = 64;       // 16-bit elements per k-block: one 128-byte swizzle row
 constexpr int UMMA_K = 16;   // K of one tcgen05.mma.kind::f16
-// Epilogue warps: 4 (one per TMEM lane quarter) or 8 (two per quarter, each
-// taking every other 32-column step of the tile).  A CTA has a producer warp,
-// an MMA warp and the epilogue warps.
+// Epilogue warps: one group of 4 (one warp per TMEM lane quarter) or two
+// groups (8 warps, the groups taking alternate 32-column steps of the tile).
+// A CTA has a producer warp, an MMA warp and an epilogue TMA warp ahead of
+// the epilogue warps.
 constexpr int kMaxEpiWarps = 8;
-__host__ __device__ constexpr int threads_for(int epi_warps) { return 64 + 32 * epi_warps; }
-// Output staging buffers per epilogue warp: two (a step's outputs are written
-// while the previous step's TMA store still reads its buffer) with 4 warps;
-// one with 8, where the quarter's other warp keeps the stores flowing.
+constexpr int kMaxEpiGroups = kMaxEpiWarps / 4;
+constexpr int kEpiWarp0 = 3;   // first epilogue warp
+constexpr int kEpiRows = 128;  // rows of a staged epilogue box: all of a CTA's accumulator rows
+__host__ __device__ constexpr int threads_for(int epi_warps) { return 32 * kEpiWarp0 + 32 * epi_warps; }
+// Output staging boxes per epilogue group: two (a step's outputs are written
+// while the previous step's box is still being stored) with one group; one
+// per group with two, where the other group keeps the stores flowing.
+constexpr int kMaxOutBufs = 2;
 __host__ __device__ constexpr int out_bufs_for(int epi_warps) { return epi_warps == 8 ? 1 : 2; }
 constexpr int kMaxStages = 8;
 constexpr int kMaxAuxStages = 8;
@@ -125,8 +130,8 @@ struct alignas(128) GroupDesc {
 struct KParams {
   CUtensorMap tmA;                    // (K, M, L) box (64, 128, 1), 128B swizzle
   CUtensorMap tmB;                    // (N, K, L) box (64, 64, 1), 128B swizzle
-  CUtensorMap tmAux[GE_MAX_TMA_AUX];  // (N, M, L) box (EW, 32, 1)
-  CUtensorMap tmOut[GE_MAX_OUT];      // (N, M, L) box (EW, 32, 1)
+  CUtensorMap tmAux[GE_MAX_TMA_AUX];  // (N, M, L) box (EW, kEpiRows, 1)
+  CUtensorMap tmOut[GE_MAX_OUT];      // (N, M, L) box (EW, kEpiRows, 1)
   const void *bcast_ptr[GE_MAX_AUX];
   const void *cbcast_ptr[GE_MAX_AUX];
   uint32_t *status;                   // device status word (timeouts)
@@ -139,11 +144,12 @@ struct KParams {
   int32_t raster_group;
   int32_t stages, aux_stages;
   uint32_t off_A, off_B, off_aux, off_out, off_bar;  // byte offsets in dynamic smem
-  uint32_t aux_stage_bytes, out_stage_bytes;          // one epilogue warp, one stage
+  uint32_t aux_stage_bytes, out_stage_bytes;          // one staging slot: a kEpiRows x EW box
+                                                      // per aux tensor / per output
   uint32_t aux_off[GE_MAX_TMA_AUX], out_off[GE_MAX_OUT];
   uint32_t tx_bytes;      // bytes one k-block stage receives (both CTAs of a pair)
   uint32_t tx_bytes_half; // the same for a half-width tile
-  uint32_t aux_tx_bytes;  // bytes one epilogue warp's aux stage receives
+  uint32_t aux_tx_bytes;  // bytes one aux staging slot receives
   uint32_t b_lbo, b_sbo;  // B smem descriptor strides (bytes)
   uint64_t timeout_ns;
   uint32_t debug_flags;
@@ -178,6 +184,8 @@ enum WaitSite : uint32_t {
   SITE_EPI_TMEM_FULL = 4,
   SITE_EPI_AUX_FULL = 5,
   SITE_DRAIN = 6,
+  SITE_EPI_TMA = 7,        // the epilogue TMA thread saw no progress
+  SITE_EPI_OUT_EMPTY = 8,  // an epilogue warp waited for an output box
 };
 
 }  // namespace ge

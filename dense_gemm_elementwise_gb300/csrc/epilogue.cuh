@@ -83,7 +83,8 @@ __device__ __forceinline__ uint4 pack8(const float *t) {
 }
 
 // ----------------------------------------------------- swizzled staging box --
-// One TMA box: 32 rows x EW (32) columns, row = lane.  16-bit rows are 64 bytes
+// One TMA box: kEpiRows (128) rows x EW (32) columns; a warp touches the 32
+// rows of its lane quarter (row = 32 * quarter + lane).  16-bit rows are 64 bytes
 // (64-byte swizzle: 16-byte chunk j of row r at r*64 + ((j ^ ((r>>1)&3))*16));
 // fp32 rows are 128 bytes (128-byte swizzle: chunk j at r*128 + ((j ^ (r&7))*16)).
 // Either way the 8 lanes of a 16-byte access phase hit 8 different bank
@@ -131,9 +132,9 @@ __device__ __forceinline__ void box_store(uint8_t *box, int row, int half, const
 }
 
 // Epilogue tensors stored M-major (each batch column-major): the staged box
-// is 32 columns of 32 rows, a column's 32 rows contiguous ([n][m], no
+// is 32 columns of kEpiRows rows, a column's rows contiguous ([n][m], no
 // swizzle).  Lane = row touches one element per column, so every warp access
-// covers one contiguous 64- or 128-byte column without bank conflicts.
+// covers a contiguous 64- or 128-byte run of a column without bank conflicts.
 __device__ __forceinline__ float widen16(uint16_t u, bool bf16) {
   return bf16 ? __uint_as_float(static_cast<uint32_t>(u) << 16)
               : __half2float(__ushort_as_half(static_cast<unsigned short>(u)));
@@ -145,9 +146,9 @@ __device__ __forceinline__ void col_box_load(const uint8_t *box, int row, int ha
   for (int e = 0; e < 16; ++e) {
     const int n = 16 * half + e;
     if constexpr (DT == GE_F32)
-      t[e] = reinterpret_cast<const float *>(box)[n * 32 + row];
+      t[e] = reinterpret_cast<const float *>(box)[n * kEpiRows + row];
     else
-      t[e] = widen16(reinterpret_cast<const uint16_t *>(box)[n * 32 + row], DT == GE_BF16);
+      t[e] = widen16(reinterpret_cast<const uint16_t *>(box)[n * kEpiRows + row], DT == GE_BF16);
   }
 }
 
@@ -157,11 +158,11 @@ __device__ __forceinline__ void col_box_store(uint8_t *box, int row, int half, c
   for (int e = 0; e < 16; ++e) {
     const int n = 16 * half + e;
     if constexpr (DT == GE_F32) {
-      reinterpret_cast<float *>(box)[n * 32 + row] = t[e];
+      reinterpret_cast<float *>(box)[n * kEpiRows + row] = t[e];
     } else if constexpr (DT == GE_BF16) {
-      reinterpret_cast<__nv_bfloat16 *>(box)[n * 32 + row] = __float2bfloat16_rn(t[e]);
+      reinterpret_cast<__nv_bfloat16 *>(box)[n * kEpiRows + row] = __float2bfloat16_rn(t[e]);
     } else {
-      reinterpret_cast<__half *>(box)[n * 32 + row] = __float2half_rn(t[e]);
+      reinterpret_cast<__half *>(box)[n * kEpiRows + row] = __float2half_rn(t[e]);
     }
   }
 }

@@ -16,12 +16,21 @@
 //               tcgen05.mma (fp16/bf16 -> fp32) into one of two TMEM
 //               accumulators; tcgen05.commit frees ring stages and publishes
 //               finished accumulators.
-//   warps 2..   epilogue, 4 or 8 warps (Epi::kWarps; with 8, the two warps of
-//               a TMEM lane quarter take alternate 32-column steps):
-//               tcgen05.ld of 32-column steps, aux tensors staged per warp by
-//               TMA (prefetched ahead, across tiles), the epilogue program in
-//               fp32 (interpreted, or straight-line for catalog entries),
-//               rounding, TMA stores from staging boxes.
+//   warp 2      epilogue TMA thread: for every 32-column step of every tile
+//               it loads each aux tensor's 128-row x 32-column box (all of
+//               this CTA's accumulator rows) into a staging slot ahead of
+//               time, and stores each output's box once the epilogue warps
+//               have written it.  One thread issues every epilogue copy, a
+//               quarter as many as 32-row boxes would take, and the
+//               epilogue warps never wait on a copy being issued.
+//   warps 3..   epilogue, one or two groups of 4 warps (Epi::kWarps 4 or 8;
+//               a group's warps cover the four TMEM lane quarters, and two
+//               groups take alternate 32-column steps): tcgen05.ld of the
+//               step, the epilogue program in fp32 (interpreted, or
+//               straight-line for catalog entries) on the staged aux boxes,
+//               rounding into the output staging box.  Slots and boxes are
+//               handed over through mbarriers (aux full / empty, out full /
+//               empty).
 // The two TMEM accumulators let the epilogue of tile i overlap the mainloop of
 // tile i+1.  Ragged M/N/K edges are handled by TMA: out-of-range loads read
 // zeros, out-of-range stores are dropped.  When the host splits the last wave
@@ -71,10 +80,14 @@ constexpr uint32_t kBarFull = 0;                       // kMaxStages x 8
 constexpr uint32_t kBarEmpty = 64;                     // kMaxStages x 8
 constexpr uint32_t kBarTmemFull = 128;                 // 2 x 8
 constexpr uint32_t kBarTmemEmpty = 144;                // 2 x 8
-constexpr uint32_t kBarAux = 160;                      // kMaxEpiWarps x kMaxAuxStages x 8
-constexpr uint32_t kBarDrain = kBarAux + 8 * kMaxEpiWarps * kMaxAuxStages;  // 672
-constexpr uint32_t kTmemSlot = kBarDrain + 8;          // 680
-constexpr uint32_t kAbortFlag = kTmemSlot + 4;         // 684
+// epilogue staging, per warp group and slot (group-major)
+constexpr uint32_t kBarAuxFull = 160;                  // kMaxEpiGroups x kMaxAuxStages x 8
+constexpr uint32_t kBarAuxEmpty = kBarAuxFull + 8 * kMaxEpiGroups * kMaxAuxStages;  // 288
+constexpr uint32_t kBarOutFull = kBarAuxEmpty + 8 * kMaxEpiGroups * kMaxAuxStages;  // 416
+constexpr uint32_t kBarOutEmpty = kBarOutFull + 8 * kMaxEpiGroups * kMaxOutBufs;    // 448
+constexpr uint32_t kBarDrain = kBarOutEmpty + 8 * kMaxEpiGroups * kMaxOutBufs;      // 480
+constexpr uint32_t kTmemSlot = kBarDrain + 8;          // 488
+constexpr uint32_t kAbortFlag = kTmemSlot + 4;         // 492
 constexpr uint32_t kBarBlockBytes = 1024;
 static_assert(kAbortFlag + 4 <= kBarBlockBytes, "barrier block overflow");
 
@@ -194,9 +207,10 @@ struct Waiter {
 };
 
 // Epilogue leaves and stores for the fused kernel: aux tensors and outputs
-// live in this warp's swizzled TMA staging boxes (row = lane, `half` picks the
-// 16-column half of the 32-column box), broadcast vectors are read from
-// global memory (the same addresses for every lane).
+// live in the warp group's swizzled 128-row TMA staging boxes (row = the
+// lane's accumulator row, 32 * quarter + lane; `half` picks the 16-column
+// half of the 32-column box), broadcast vectors are read from global memory
+// (the same addresses for every lane).
 struct FusedMem {
   const KParams *p;
   const void *const *bptr;  // row-broadcast vectors of this tile's problem
@@ -233,7 +247,6 @@ template <int CG, int BN, class Epi>
 __global__ void __launch_bounds__(threads_for(Epi::kWarps), 1)
     gemm_epi_kernel(const __grid_constant__ KParams p) {
   constexpr int kEpiWarps = Epi::kWarps;
-  constexpr int kSplit = kEpiWarps / 4;  // warps per TMEM lane quarter
   static_assert(kEpiWarps == 4 || kEpiWarps == 8, "4 or 8 epilogue warps");
   using T = TileCfg<CG, BN>;
   extern __shared__ uint8_t smem_raw[];
@@ -250,23 +263,35 @@ __global__ void __launch_bounds__(threads_for(Epi::kWarps), 1)
   constexpr uint16_t kPairMask = 0x3u;  // a commit arrives in both CTAs of the pair
 
   const uint32_t bar = sb + p.off_bar;
-  const uint32_t bar_aux = bar + kBarAux;
+  constexpr int kGroups = kEpiWarps / 4;      // epilogue warp groups
+  constexpr int kOutBufs = out_bufs_for(kEpiWarps);
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + p.off_bar + kTmemSlot);
   volatile uint32_t *abort_flag = reinterpret_cast<volatile uint32_t *>(smem + p.off_bar + kAbortFlag);
 
-  if (threadIdx.x == 0) {
-    for (int s = 0; s < p.stages; ++s) {
-      mbar_init(bar + kBarFull + 8 * s, 1);
-      mbar_init(bar + kBarEmpty + 8 * s, 1);
+  if (warp == 0) {
+    // the lanes of warp 0 initialise the barriers in parallel
+    if (lane < p.stages) {
+      mbar_init(bar + kBarFull + 8 * lane, 1);
+      mbar_init(bar + kBarEmpty + 8 * lane, 1);
     }
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(bar + kBarTmemFull + 8 * b, 1);
-      mbar_init(bar + kBarTmemEmpty + 8 * b, kEpiWarps * CG);
+    if (lane < 2) {
+      mbar_init(bar + kBarTmemFull + 8 * lane, 1);
+      mbar_init(bar + kBarTmemEmpty + 8 * lane, kEpiWarps * CG);
     }
-    for (int i = 0; i < kEpiWarps * kMaxAuxStages; ++i) mbar_init(bar_aux + 8 * i, 1);
-    mbar_init(bar + kBarDrain, 1);
-    *abort_flag = 0u;
+    if (lane < kGroups * kMaxAuxStages) {  // slot (lane % kMaxAuxStages) of group (lane / ...)
+      mbar_init(bar + kBarAuxFull + 8 * lane, 1);
+      mbar_init(bar + kBarAuxEmpty + 8 * lane, 4);  // the group's 4 warps release a slot
+    }
+    if (lane < kGroups * kMaxOutBufs) {
+      mbar_init(bar + kBarOutFull + 8 * lane, 4);   // the group's 4 warps fill a box
+      mbar_init(bar + kBarOutEmpty + 8 * lane, 1);  // the TMA thread frees it
+    }
+    if (lane == 0) {
+      mbar_init(bar + kBarDrain, 1);
+      *abort_flag = 0u;
+    }
     fence_mbarrier_init();
+    __syncwarp();
   }
   if (warp == 0 && lane == 0 && p.groups == nullptr) {
     prefetch_tensormap(&p.tmA);
@@ -471,111 +496,182 @@ __global__ void __launch_bounds__(threads_for(Epi::kWarps), 1)
         wt.drain(bar + kBarDrain, 0u);
       }
     }
+  } else if (warp == 2) {
+    // ------------------------------------------------- epilogue TMA thread --
+    // Walks this CTA's tiles and their 32-column steps twice, as two
+    // sequences: the aux loads (step g of a group into slot g % SA, once the
+    // group has released it) run ahead of the output stores (step g's boxes,
+    // once the group's four warps have filled them).  One polling loop
+    // serves both, so neither blocks the other.
+    if (lane == 0) {
+      const bool has_aux = p.prog.n_tma_aux > 0;
+      const int SA = p.aux_stages;
+      TileCursor ltc(p, unit, n_units, my_tiles), stc(p, unit, n_units, my_tiles);
+      int l_i = 0, l_s = 0, l_steps = 0, l_x0 = 0, l_y0 = 0, l_l = 0;
+      int s_i = 0, s_s = 0, s_steps = 0, s_x0 = 0, s_y0 = 0, s_l = 0;
+      int l_g[kMaxEpiGroups] = {0, 0}, s_g[kMaxEpiGroups] = {0, 0};
+      const CUtensorMap *l_maps = p.tmAux, *s_maps = p.tmOut;
+      const GroupDesc *l_gd = nullptr, *s_gd = nullptr;  // problems whose maps are fenced
+      bool l_more = has_aux && my_tiles > 0, s_more = my_tiles > 0;
+      // a tile's column origin, this CTA's first accumulator row, batch, steps
+      auto enter = [&](const TileRef &tr, int &x0, int &y0, int &ll, int &steps) {
+        x0 = tr.nb * BN + (tr.half > 0 ? BN / 2 : 0);
+        y0 = tr.mb * T::kMmaM + static_cast<int>(rank) * BM;
+        ll = tr.l;
+        steps = tr.half < 0 ? T::kSteps : T::kSteps / 2;
+      };
+      if (l_more) {
+        const TileRef tr = ltc.next();
+        enter(tr, l_x0, l_y0, l_l, l_steps);
+        if (tr.gd) {
+          l_gd = tr.gd;
+          l_maps = tr.gd->tmAux;
+          for (int a = 0; a < p.prog.n_tma_aux; ++a) fence_tensormap_acquire(&l_maps[a]);
+        }
+      }
+      if (s_more) {
+        const TileRef tr = stc.next();
+        enter(tr, s_x0, s_y0, s_l, s_steps);
+        if (tr.gd) {
+          s_gd = tr.gd;
+          s_maps = tr.gd->tmOut;
+          for (int o = 0; o < p.prog.n_out; ++o) fence_tensormap_acquire(&s_maps[o]);
+        }
+      }
+      uint64_t t_idle = globaltimer_ns();
+      uint32_t polls = 0;
+      bool ok = true;
+      while (ok && (l_more || s_more)) {
+        bool progress = false;
+        if (s_more) {
+          const int grp = s_s % kGroups;
+          const int buf = s_g[grp] % kOutBufs;
+          const uint32_t fb = bar + kBarOutFull + 8u * (grp * kMaxOutBufs + buf);
+          if (mbar_test_wait(fb, static_cast<uint32_t>(s_g[grp] / kOutBufs) & 1u)) {
+            const uint8_t *box = smem + p.off_out + (grp * kOutBufs + buf) * p.out_stage_bytes;
+            const int x = s_x0 + s_s * EW;
+            for (int o = 0; o < p.prog.n_out; ++o)
+              tma_store_3d(&s_maps[o], smem_u32(box + p.out_off[o]), p.cd_m ? s_y0 : x,
+                           p.cd_m ? x : s_y0, s_l);
+            bulk_commit_group();
+            // the box is free once the copy has read it
+            bulk_wait_group_read<0>();
+            mbar_arrive(bar + kBarOutEmpty + 8u * (grp * kMaxOutBufs + buf));
+            ++s_g[grp];
+            if (++s_s == s_steps) {
+              s_s = 0;
+              if (++s_i < my_tiles) {
+                const TileRef tr = stc.next();
+                enter(tr, s_x0, s_y0, s_l, s_steps);
+                if (tr.gd) {
+                  s_maps = tr.gd->tmOut;
+                  if (tr.gd != s_gd) {
+                    s_gd = tr.gd;
+                    for (int o = 0; o < p.prog.n_out; ++o) fence_tensormap_acquire(&s_maps[o]);
+                  }
+                }
+              } else {
+                s_more = false;
+              }
+            }
+            progress = true;
+          }
+        }
+        if (l_more) {
+          const int grp = l_s % kGroups;
+          const int slot = l_g[grp] % SA;
+          const uint32_t eb = bar + kBarAuxEmpty + 8u * (grp * kMaxAuxStages + slot);
+          if (mbar_test_wait(eb, (static_cast<uint32_t>(l_g[grp] / SA) & 1u) ^ 1u)) {
+            const uint32_t fb = bar + kBarAuxFull + 8u * (grp * kMaxAuxStages + slot);
+            const uint8_t *box = smem + p.off_aux + (grp * SA + slot) * p.aux_stage_bytes;
+            const int x = l_x0 + l_s * EW;
+            mbar_arrive_expect_tx(fb, p.aux_tx_bytes);
+            for (int a = 0; a < p.prog.n_tma_aux; ++a)
+              tma_load_3d(smem_u32(box + p.aux_off[a]), &l_maps[a], fb, p.cd_m ? l_y0 : x,
+                          p.cd_m ? x : l_y0, l_l);
+            ++l_g[grp];
+            if (++l_s == l_steps) {
+              l_s = 0;
+              if (++l_i < my_tiles) {
+                const TileRef tr = ltc.next();
+                enter(tr, l_x0, l_y0, l_l, l_steps);
+                if (tr.gd) {
+                  l_maps = tr.gd->tmAux;
+                  if (tr.gd != l_gd) {
+                    l_gd = tr.gd;
+                    for (int a = 0; a < p.prog.n_tma_aux; ++a) {
+                      fence_tensormap_acquire(&l_maps[a]);
+                      prefetch_tensormap(&l_maps[a]);
+                    }
+                  }
+                }
+              } else {
+                l_more = false;
+              }
+            }
+            progress = true;
+          }
+        }
+        if (progress) {
+          t_idle = globaltimer_ns();
+          polls = 0;
+        } else if ((++polls & 15u) == 0u) {
+          if (*abort_flag) {
+            ok = false;
+          } else if (globaltimer_ns() - t_idle > p.timeout_ns) {
+            wt.fail(SITE_EPI_TMA);
+            ok = false;
+          } else {
+            __nanosleep(64);
+          }
+        }
+      }
+      if (!ok) {
+        // abort: wait (bounded) for the aux loads still in flight, the last
+        // one issued into each slot
+        for (int grp = 0; grp < kGroups; ++grp)
+          for (int j = max(l_g[grp] - SA, 0); j < l_g[grp]; ++j)
+            wt.drain(bar + kBarAuxFull + 8u * (grp * kMaxAuxStages + j % SA),
+                     static_cast<uint32_t>(j / SA) & 1u);
+      }
+      bulk_wait_group<0>();
+    }
   } else {
     // --------------------------------------------------------- epilogue --
-    const int e = warp - 2;  // staging slot
-    const int q = warp & 3;  // TMEM lane quarter this warp may access
-    const int ch = e / 4;    // which of the quarter's warps: takes steps ch, ch + kSplit, ...
-    constexpr int kStepsW = T::kSteps / kSplit;  // this warp's steps per tile
-    static_assert(T::kSteps % kSplit == 0, "steps split evenly between a quarter's warps");
-    // a half tile has half the steps (the host splits tiles only where that
-    // is a whole, nonzero number per warp)
-    constexpr int kHalfW = kStepsW / 2 > 0 ? kStepsW / 2 : 1;
+    const int e = warp - kEpiWarp0;  // epilogue warp index
+    const int q = warp & 3;          // TMEM lane quarter this warp may access
+    const int grp = e / 4;           // group: takes steps grp, grp + kGroups, ...
     const uint32_t tq = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
-    uint8_t *aux_w = smem + p.off_aux + e * p.aux_stages * p.aux_stage_bytes;
-    constexpr int kOutBufs = out_bufs_for(kEpiWarps);
-    uint8_t *out_w = smem + p.off_out + e * kOutBufs * p.out_stage_bytes;
-    const uint32_t auxbar_w = bar_aux + 8u * e * kMaxAuxStages;
     const bool has_aux = p.prog.n_tma_aux > 0;
     const int SA = p.aux_stages;
-    // this CTA's full tiles come first, then its half tiles
-    const int q_full = unit < p.num_full ? min((p.num_full - 1 - unit) / n_units + 1, my_tiles) : 0;
-    const int full_steps = q_full * kStepsW;
-    const int total = full_steps + (my_tiles - q_full) * kHalfW;
-    int issued = 0, g = 0, abuf = 0, obuf = 0;
+    const int row = q * 32 + lane;   // this lane's row of the CTA's 128 accumulator rows
+    int g = 0, abuf = 0;             // this group's steps so far
     uint32_t aphase = 0;
     bool ok = true;
-    int pf_tile = -1, pf_x0 = 0, pf_y = 0, pf_l = 0;  // prefetch: coordinates of tile pf_tile
-    TileCursor pf_tc(p, unit, n_units, my_tiles);        // tiles of the aux prefetch
-    TileCursor tc(p, unit, n_units, my_tiles);           // tiles of the epilogue proper
-    const CUtensorMap *pf_maps = p.tmAux;               // aux maps of tile pf_tile
-    const GroupDesc *out_gd = nullptr;                  // problem whose output maps are fenced
-
-    // TMA loads of every Load tensor for this warp's 32 rows of step gi
-    auto issue_aux = [&](int gi) {
-      const int ii = gi < full_steps ? gi / kStepsW : q_full + (gi - full_steps) / kHalfW;
-      const int first = ii <= q_full ? ii * kStepsW : full_steps + (ii - q_full) * kHalfW;
-      if (ii != pf_tile) {
-        const TileRef tr = pf_tc.next();  // tiles are entered in order, one at a time
-        pf_l = tr.l;
-        pf_tile = ii;
-        pf_x0 = tr.nb * BN + (tr.half > 0 ? BN / 2 : 0);
-        pf_y = tr.mb * T::kMmaM + static_cast<int>(rank) * BM + q * 32;
-        if (tr.gd && pf_maps != tr.gd->tmAux)
-          for (int a = 0; a < p.prog.n_tma_aux; ++a) {
-            fence_tensormap_acquire(&tr.gd->tmAux[a]);
-            prefetch_tensormap(&tr.gd->tmAux[a]);
-          }
-        pf_maps = tr.gd ? tr.gd->tmAux : p.tmAux;
-      }
-      const int as = gi % SA;
-      const uint32_t ab = auxbar_w + 8u * as;
-      uint8_t *dst = aux_w + as * p.aux_stage_bytes;
-      fence_proxy_async_smem();
-      mbar_arrive_expect_tx(ab, p.aux_tx_bytes);
-      const int x = pf_x0 + ((gi - first) * kSplit + ch) * EW;
-      for (int a = 0; a < p.prog.n_tma_aux; ++a)
-        tma_load_3d(smem_u32(dst + p.aux_off[a]), &pf_maps[a], ab, p.cd_m ? pf_y : x,
-                    p.cd_m ? x : pf_y, pf_l);
-    };
+    TileCursor tc(p, unit, n_units, my_tiles);
 
     for (int i = 0; ok && i < my_tiles; ++i) {
       const TileRef tr = tc.next();
-      const int l = tr.l, mb = tr.mb, nb = tr.nb;
-      const int m0 = mb * T::kMmaM + static_cast<int>(rank) * BM + q * 32;
-      const int n0 = nb * BN + (tr.half > 0 ? BN / 2 : 0);
+      const int m0 = tr.mb * T::kMmaM + static_cast<int>(rank) * BM + q * 32;
+      const int n0 = tr.nb * BN + (tr.half > 0 ? BN / 2 : 0);
       const int steps = tr.half < 0 ? T::kSteps : T::kSteps / 2;  // 32-column steps of this tile
-      const CUtensorMap *out_maps = tr.gd ? tr.gd->tmOut : p.tmOut;
       const void *const *bptr = tr.gd ? tr.gd->bcast_ptr : p.bcast_ptr;
       const void *const *cptr = tr.gd ? tr.gd->cbcast_ptr : p.cbcast_ptr;
       const int pM = tr.gd ? __ldg(&tr.gd->M) : p.M;
       const int pN = tr.gd ? __ldg(&tr.gd->N) : p.N;
-      // output maps of this problem, unless made ready during the last tile
-      if (lane == 0 && tr.gd && tr.gd != out_gd) {
-        for (int o = 0; o < p.prog.n_out; ++o) fence_tensormap_acquire(&out_maps[o]);
-        out_gd = tr.gd;
-      }
-      // start this tile's aux loads before its accumulator is ready
-      if (has_aux && lane == 0) {
-        while (issued < total && issued < g + SA) issue_aux(issued++);
-      }
-      __syncwarp();
       const bool got = wt.wait(bar + kBarTmemFull + 8 * abuf, aphase, SITE_EPI_TMEM_FULL);
       if (!__all_sync(0xffffffffu, got)) {
         ok = false;
         break;
       }
-      // the next tile's problem: make its output maps ready while this tile's
-      // epilogue runs (its table entry was loaded with this tile's)
-      if (lane == 0 && tc.has_more() && tc.nxt.gd && tc.nxt.gd != out_gd) {
-        out_gd = tc.nxt.gd;
-        for (int o = 0; o < p.prog.n_out; ++o) {
-          fence_tensormap_acquire(&out_gd->tmOut[o]);
-          prefetch_tensormap(&out_gd->tmOut[o]);
-        }
-      }
       tc_fence_after();
-      for (int s = ch; s < steps; s += kSplit, ++g) {
-        if (has_aux && lane == 0) {
-          while (issued < total && issued < g + SA) issue_aux(issued++);
-        }
-        __syncwarp();
+      for (int s = grp; s < steps; s += kGroups, ++g) {
         float acc0[CH], acc1[CH];
         const uint32_t col = static_cast<uint32_t>(abuf * BN + s * EW);
         tmem_ld16(tq + col, acc0);
         tmem_ld16(tq + col + CH, acc1);
         tmem_wait_ld();
-        if (s + kSplit >= steps) {
+        if (s + kGroups >= steps) {
           // accumulator fully read: hand it back to the MMA warp
           tc_fence_before();
           __syncwarp();
@@ -585,42 +681,41 @@ __global__ void __launch_bounds__(threads_for(Epi::kWarps), 1)
             else mbar_arrive(tb);
           }
         }
+        const int slot = g % SA, buf = g % kOutBufs;
         if (has_aux) {
-          const bool a_ok = wt.wait(auxbar_w + 8u * (g % SA), static_cast<uint32_t>(g / SA) & 1u,
-                                    SITE_EPI_AUX_FULL);
+          const bool a_ok = wt.wait(bar + kBarAuxFull + 8u * (grp * kMaxAuxStages + slot),
+                                    static_cast<uint32_t>(g / SA) & 1u, SITE_EPI_AUX_FULL);
           if (!__all_sync(0xffffffffu, a_ok)) {
             ok = false;
             break;
           }
         }
-        // the staging buffer about to be written has been read by its last store
-        if (lane == 0) bulk_wait_group_read<kOutBufs - 1>();
-        __syncwarp();
-        uint8_t *ostage = out_w + obuf * p.out_stage_bytes;
-        const uint8_t *astage = aux_w + (g % SA) * p.aux_stage_bytes;
+        // the output box about to be written has been read by its last store
+        const bool o_ok = wt.wait(bar + kBarOutEmpty + 8u * (grp * kMaxOutBufs + buf),
+                                  (static_cast<uint32_t>(g / kOutBufs) & 1u) ^ 1u,
+                                  SITE_EPI_OUT_EMPTY);
+        if (!__all_sync(0xffffffffu, o_ok)) {
+          ok = false;
+          break;
+        }
+        uint8_t *ostage = smem + p.off_out + (grp * kOutBufs + buf) * p.out_stage_bytes;
+        const uint8_t *astage = smem + p.off_aux + (grp * SA + slot) * p.aux_stage_bytes;
         const int c0 = n0 + s * EW;
-        Epi::template run<CH>(p.prog, acc0, FusedMem{&p, bptr, cptr, pM, pN, astage, ostage, lane,
+        Epi::template run<CH>(p.prog, acc0, FusedMem{&p, bptr, cptr, pM, pN, astage, ostage, row,
                                                      0, c0, m0 + lane, p.cd_m != 0});
-        Epi::template run<CH>(p.prog, acc1, FusedMem{&p, bptr, cptr, pM, pN, astage, ostage, lane,
+        Epi::template run<CH>(p.prog, acc1, FusedMem{&p, bptr, cptr, pM, pN, astage, ostage, row,
                                                      1, c0 + CH, m0 + lane, p.cd_m != 0});
+        // the aux slot has been read; the output box is written (visible to
+        // the TMA engine after the proxy fence)
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) {
-          for (int o = 0; o < p.prog.n_out; ++o)
-            tma_store_3d(&out_maps[o], smem_u32(ostage + p.out_off[o]), p.cd_m ? m0 : c0,
-                         p.cd_m ? c0 : m0, l);
-          bulk_commit_group();
+          if (has_aux) mbar_arrive(bar + kBarAuxEmpty + 8u * (grp * kMaxAuxStages + slot));
+          mbar_arrive(bar + kBarOutFull + 8u * (grp * kMaxOutBufs + buf));
         }
-        if constexpr (kOutBufs == 2) obuf ^= 1;
       }
       abuf ^= 1;
       if (abuf == 0) aphase ^= 1u;
-    }
-    if (lane == 0) {
-      if (!ok)
-        for (int gi = g; gi < issued; ++gi)
-          wt.drain(auxbar_w + 8u * (gi % SA), static_cast<uint32_t>(gi / SA) & 1u);
-      bulk_wait_group<0>();
     }
     __syncwarp();
   }

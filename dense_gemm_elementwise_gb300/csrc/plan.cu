@@ -200,9 +200,11 @@ constexpr int kBarBlock = 1024;
 constexpr int kAlignSlack = 1024;
 
 // Shared-memory layout for (cg, bn) and a program; stages = 0 picks the most
-// that fit.  The aux prefetch gets the deepest ring (up to max_aux) that still
-// leaves min_main mainloop stages.  Returns GE_ERR_SMEM if fewer than 2 (or the
-// requested count) fit.
+// that fit.  Epilogue staging is per group of 4 epilogue warps: aux slots
+// (one kEpiRows x EW box per aux tensor) and output boxes (one per output).
+// The aux prefetch gets the deepest ring (up to max_aux slots per group) that
+// still leaves min_main mainloop stages.  Returns GE_ERR_SMEM if fewer than 2
+// (or the requested count) fit.
 int make_layout(Layout *Lo, int cg, int bn, int want_stages, const EpiProgram &P, int max_smem,
                 int max_aux = 4, int min_main = 5, int warps = 4) {
   const uint32_t a_bytes = BM * BK * 2;
@@ -210,14 +212,15 @@ int make_layout(Layout *Lo, int cg, int bn, int want_stages, const EpiProgram &P
   uint32_t aux_stage = 0, out_stage = 0;
   for (int t = 0; t < P.n_tma_aux; ++t) {
     Lo->aux_off[t] = aux_stage;
-    aux_stage += 32u * EW * esize(P.tma_aux_dtype[t]);
+    aux_stage += uint32_t(kEpiRows) * EW * esize(P.tma_aux_dtype[t]);
   }
   for (int o = 0; o < P.n_out; ++o) {
     Lo->out_off[o] = out_stage;
-    out_stage += 32u * EW * esize(P.out_dtype[o]);
+    out_stage += uint32_t(kEpiRows) * EW * esize(P.out_dtype[o]);
   }
+  const int groups = warps / 4;
   auto stages_with = [&](int sa) {
-    const int64_t epi = int64_t(warps) * sa * aux_stage + int64_t(warps) * out_bufs_for(warps) * out_stage;
+    const int64_t epi = int64_t(groups) * sa * aux_stage + int64_t(groups) * out_bufs_for(warps) * out_stage;
     const int64_t room = int64_t(max_smem) - kAlignSlack - kBarBlock - epi;
     const int s = room > 0 ? static_cast<int>(room / (a_bytes + b_bytes)) : 0;
     return std::min(s, kMaxStages);
@@ -250,8 +253,8 @@ int make_layout(Layout *Lo, int cg, int bn, int want_stages, const EpiProgram &P
   Lo->off_A = 0;
   Lo->off_B = stages * a_bytes;
   Lo->off_aux = Lo->off_B + stages * b_bytes;
-  Lo->off_out = Lo->off_aux + warps * sa * aux_stage;
-  Lo->off_bar = Lo->off_out + warps * out_bufs_for(warps) * out_stage;
+  Lo->off_out = Lo->off_aux + groups * sa * aux_stage;
+  Lo->off_bar = Lo->off_out + groups * out_bufs_for(warps) * out_stage;
   Lo->warps = warps;
   Lo->smem_used = static_cast<int>(Lo->off_bar + kBarBlock + kAlignSlack);
   // Always request the whole opt-in shared memory: exactly one CTA per SM, so
@@ -594,15 +597,17 @@ bool encode_operands(const gemm_epi_plan *pl, KParams *kp, const void *A, const 
   return encode_ab_maps(pl, &kp->tmA, &kp->tmB, A, B, pl->L, pl->M, pl->N, pl->K);
 }
 
-// An epilogue tensor's map: N-major (N, M, L) with 32 x 32 swizzled boxes, or
-// M-major (M, N, L) with 32 x 32 plain boxes.  The unfused path's fp32
+// An epilogue tensor's map: N-major (N, M, L) with EW x kEpiRows swizzled
+// boxes, or M-major (M, N, L) with kEpiRows x EW plain boxes: one box holds a
+// 32-column step of all of a CTA's accumulator rows.  The unfused path's fp32
 // workspace follows the epilogue tensors' order.
 bool encode_epi_map(const gemm_epi_plan *pl, CUtensorMap *m, int dt, const void *ptr, uint64_t L,
                     uint64_t M, uint64_t N) {
   if (pl->cd_m)
-    return encode3d(m, dt, ptr, M, N, L, 32, EW, CU_TENSOR_MAP_SWIZZLE_NONE,
+    return encode3d(m, dt, ptr, M, N, L, kEpiRows, EW, CU_TENSOR_MAP_SWIZZLE_NONE,
                     CU_TENSOR_MAP_L2_PROMOTION_L2_128B);
-  return encode3d(m, dt, ptr, N, M, L, EW, 32, epi_swizzle(dt), CU_TENSOR_MAP_L2_PROMOTION_L2_128B);
+  return encode3d(m, dt, ptr, N, M, L, EW, kEpiRows, epi_swizzle(dt),
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_128B);
 }
 
 bool encode_epilogue_map(const gemm_epi_plan *pl, CUtensorMap *m, int dt, const void *ptr) {
