@@ -869,9 +869,9 @@ def run_grouped(args, w):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_max,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": w.ab, "data": "synthetic",
-        "config": dict(grouped_config(w, world), **{
-            "l2": "flushed before every timed step: 512 MiB write, then 256 MiB read",
-            "plan": info, "options": args.opt or "auto"}),
+        "config": grouped_config(w, world),
+        "l2": "flushed before every timed step: 512 MiB write, then 256 MiB read",
+        "plan": info, "options": args.opt or "auto",
         "roofline": roof,
         "gpu_launches": args.steps, "clocks": clk, "one_launch_per_problem": separate,
         "e2e": e2e, "cpu_baseline": cpu}), flush=True)
