@@ -228,12 +228,15 @@ int make_layout(Layout *Lo, int cg, int bn, int want_stages, const EpiProgram &P
   // 4 warps: at least 2 aux stages; 8 warps (each warp's steps twice as far
   // apart in time) may go down to 1
   const int min_sa = warps == 8 ? 1 : 2;
+  // a requested stage count takes the place of min_main: the aux ring is the
+  // deepest that still leaves room for it
+  const int need_main = want_stages > 0 ? want_stages : min_main;
   int sa = 1, stages = stages_with(1);
   if (P.n_tma_aux > 0) {
     sa = min_sa;
     stages = stages_with(min_sa);
     for (int cand = std::min(max_aux, kMaxAuxStages); cand > min_sa; --cand)
-      if (stages_with(cand) >= min_main) {
+      if (stages_with(cand) >= need_main) {
         sa = cand;
         stages = stages_with(cand);
         break;

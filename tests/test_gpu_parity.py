@@ -98,6 +98,18 @@ def test_few_stages(stages):
     _gpu.compare(w, gpu, _gpu.oracle_rows(w, inputs))
 
 
+@pytest.mark.parametrize("stages", [6, 7])
+def test_more_stages_than_default(stages):
+    """A requested stage count above the default takes its room from the aux
+    prefetch ring (128 x 64 tiles: 24 KiB a stage), bit-exact."""
+    w = small(W.MY_EPILOGUE_128, 2, 520, 776, 1000)
+    inputs = W.make_inputs(w)
+    gpu, info = _gpu.run_gpu(w, inputs, options=B.ge_options(
+        stages=stages, cta_group=1, tile_n=64))
+    assert info["stages"] == stages and info["aux_stages"] >= 1
+    _gpu.compare(w, gpu, _gpu.oracle_rows(w, inputs))
+
+
 def test_small_grid_many_tiles_per_cta():
     """Four CTAs loop over many tiles: both TMEM accumulators, the aux
     prefetch across tile boundaries and the raster order all wrap."""
