@@ -611,6 +611,7 @@ def run_ours(args, w):
     unfused = None
     if not args.no_unfused:
         unfused = m.run_unfused(max(3, args.steps // 4), max(3, args.warmup // 4), ms)
+    back_to_back = m.run_stream(max(3, args.steps // 4)) if m.flush_l2 else None
 
     e2e = None
     if not args.no_e2e:
@@ -689,7 +690,7 @@ def run_ours(args, w):
         configs = {}
         for cw in W.WORKLOADS:
             if cw.name == w.name:
-                configs[cw.name] = config_entry(m, ms, unfused)
+                configs[cw.name] = config_entry(m, ms, unfused, back_to_back)
                 continue
             cm = Measured(cw, dev_, stream, world, None)
             try:
@@ -718,7 +719,8 @@ def run_ours(args, w):
         "l2": l2_note(m.flush_l2, m.in_bytes), "plan": info, "options": args.opt or "auto",
         "pct_of_peak": 100.0 * roof["tensor_frac"],
         "roofline": roof, "gpu_launches": args.steps, "clocks": clk,
-        "unfused": unfused, "e2e": e2e, "cpu_baseline": cpu, "configs": configs,
+        "unfused": unfused, "back_to_back": back_to_back, "e2e": e2e, "cpu_baseline": cpu,
+        "configs": configs,
     }
     print(json.dumps(line), flush=True)
 

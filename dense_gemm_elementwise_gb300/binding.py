@@ -65,7 +65,7 @@ class ge_options(ctypes.Structure):
                 ("debug_flags", ctypes.c_uint32), ("cluster_n", ctypes.c_int32),
                 ("a_major", ctypes.c_int32), ("b_major", ctypes.c_int32),
                 ("cd_major", ctypes.c_int32), ("epi_warps", ctypes.c_int32),
-                ("specialize", ctypes.c_int32)]
+                ("specialize", ctypes.c_int32), ("no_pdl", ctypes.c_int32)]
 
 
 class ge_problem(ctypes.Structure):

@@ -306,6 +306,11 @@ __global__ void __launch_bounds__(threads_for(Epi::kWarps), 1)
   if constexpr (T::kCluster > 1) cluster_sync_all(); else __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t *>(tmem_slot);
+  // Launched with programmatic stream serialization, this grid may start
+  // while the previous kernel on the stream is still running: the set-up
+  // above touches no global memory; every role waits here before its first
+  // read of an input or write of an output.
+  griddep_wait();
   const Waiter wt{abort_flag, p.status, p.timeout_ns};
   const int my_tiles = unit < p.num_tiles ? (p.num_tiles - 1 - unit) / n_units + 1 : 0;
 
@@ -403,6 +408,9 @@ __global__ void __launch_bounds__(threads_for(Epi::kWarps), 1)
           prefetch_tensormap(&ready_gd->tmB);
         }
       }
+      // every operand copy is issued: the next launch on the stream may be
+      // scheduled (its CTAs start as SMs free up and wait for this grid)
+      griddep_launch_dependents();
       if (ok) {
         // tail: every stage released by the MMA, so all commit arrivals landed
         for (int i = 0; i < p.stages; ++i) {

@@ -350,31 +350,41 @@ const void *resolve_kernel(gemm_epi_plan *pl, int cg, int bn, int epi, int warps
   return fn;
 }
 
-cudaLaunchConfig_t launch_config(const Layout &Lo, cudaStream_t s, cudaLaunchAttribute *attr) {
+// `attr` has room for two attributes: the cluster shape and, with `pdl`,
+// programmatic stream serialization (the kernel may start while the
+// previous kernel on the stream finishes; it waits in griddepcontrol.wait
+// before touching global memory).
+cudaLaunchConfig_t launch_config(const Layout &Lo, cudaStream_t s, cudaLaunchAttribute *attr,
+                                 bool pdl = false) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(Lo.grid));
   cfg.blockDim = dim3(static_cast<unsigned>(threads_for(Lo.warps)));
   cfg.dynamicSmemBytes = static_cast<size_t>(Lo.smem);
   cfg.stream = s;
-  cfg.attrs = nullptr;
+  cfg.attrs = attr;
   cfg.numAttrs = 0;
   if (Lo.cg > 1) {
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = static_cast<unsigned>(Lo.cg);
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    attr[cfg.numAttrs].id = cudaLaunchAttributeClusterDimension;
+    attr[cfg.numAttrs].val.clusterDim.x = static_cast<unsigned>(Lo.cg);
+    attr[cfg.numAttrs].val.clusterDim.y = 1;
+    attr[cfg.numAttrs].val.clusterDim.z = 1;
+    ++cfg.numAttrs;
   }
+  if (pdl) {
+    attr[cfg.numAttrs].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[cfg.numAttrs].val.programmaticStreamSerializationAllowed = 1;
+    ++cfg.numAttrs;
+  }
+  if (cfg.numAttrs == 0) cfg.attrs = nullptr;
   return cfg;
 }
 
-cudaError_t launch_gemm(const Layout &Lo, int epi, const KParams &kp, cudaStream_t s) {
+cudaError_t launch_gemm(const Layout &Lo, int epi, const KParams &kp, cudaStream_t s, bool pdl) {
   (void)epi;
   const void *fn = Lo.fn;
   if (!fn) return cudaErrorInvalidDeviceFunction;
-  cudaLaunchAttribute attr[1];
-  cudaLaunchConfig_t cfg = launch_config(Lo, s, attr);
+  cudaLaunchAttribute attr[2];
+  cudaLaunchConfig_t cfg = launch_config(Lo, s, attr, pdl);
   void *args[] = {const_cast<KParams *>(&kp)};
   return cudaLaunchKernelExC(&cfg, fn, args);
 }
@@ -515,7 +525,7 @@ int configure(gemm_epi_plan *pl) {
       return GE_ERR_CUDA;
     if (cg > 1) {
       int clusters = 0;
-      cudaLaunchAttribute attr[1];
+      cudaLaunchAttribute attr[2];
       cudaLaunchConfig_t cfg = launch_config(*Lo, nullptr, attr);
       cfg.gridDim = dim3(static_cast<unsigned>(cg));
       if (cudaOccupancyMaxActiveClusters(&clusters, fn, &cfg) == cudaSuccess && clusters > 0)
@@ -836,7 +846,8 @@ int gemm_epi_run(gemm_epi_plan *pl, const void *A, const void *B, const void *co
   for (int b = 0; b < P.n_bcast; ++b) kp.bcast_ptr[b] = aux[P.bcast_slot[b]];
   for (int b = 0; b < P.n_cbcast; ++b) kp.cbcast_ptr[b] = aux[P.cbcast_slot[b]];
   for (int s = 0; s < pl->dt.n_scalar; ++s) kp.prog.scalars[s] = scalars[s];
-  const cudaError_t e = launch_gemm(pl->lay, pl->epi, kp, static_cast<cudaStream_t>(stream));
+  const cudaError_t e = launch_gemm(pl->lay, pl->epi, kp, static_cast<cudaStream_t>(stream),
+                                    pl->opt.no_pdl == 0);
   return e == cudaSuccess ? GE_OK : GE_ERR_CUDA;
 }
 
@@ -865,7 +876,7 @@ int gemm_epi_run_unfused(gemm_epi_plan *pl, const void *A, const void *B, const 
     pl->aWs = workspace;
     pl->acc_maps_ok = true;
   }
-  cudaError_t e = launch_gemm(pl->lay_acc, pl->epi_acc, ka, s);
+  cudaError_t e = launch_gemm(pl->lay_acc, pl->epi_acc, ka, s, pl->opt.no_pdl == 0);
   if (e != cudaSuccess) return GE_ERR_CUDA;
   // launch 2: the epilogue program, elementwise
   EwParams ep;
@@ -995,7 +1006,7 @@ int configure_grouped(gemm_epi_plan *pl) {
   int units = std::max(1, sms / cg);
   if (cg > 1) {
     int clusters = 0;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     cudaLaunchConfig_t cfg = launch_config(Lo, nullptr, attr);
     cfg.gridDim = dim3(static_cast<unsigned>(cg));
     if (cudaOccupancyMaxActiveClusters(&clusters, fn, &cfg) == cudaSuccess && clusters > 0)
@@ -1234,7 +1245,9 @@ int gemm_epi_grouped_run(gemm_epi_plan *pl, const void *const *A, const void *co
   KParams &kp = pl->kp;
   kp.groups = pl->d_desc + size_t(pl->slot) * n;
   for (int i = 0; i < pl->dt.n_scalar; ++i) kp.prog.scalars[i] = scalars[i];
-  if (launch_gemm(pl->lay, pl->epi, kp, s) != cudaSuccess) return GE_ERR_CUDA;
+  // not overlapped with the previous launch: the problem table was copied
+  // in just before it
+  if (launch_gemm(pl->lay, pl->epi, kp, s, false) != cudaSuccess) return GE_ERR_CUDA;
   if (cudaEventRecord(pl->ev[pl->slot], s) != cudaSuccess) return GE_ERR_CUDA;
   pl->ev_used[pl->slot] = true;
   pl->ev_stream[pl->slot] = s;

@@ -113,6 +113,16 @@ __device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t par
   return ok != 0;
 }
 
+// ---------------------------------------------- programmatic dependent launch --
+// Wait until the grids this launch depends on have completed and their
+// memory is visible (returns at once when the launch was not overlapped).
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// Let the next launch on the stream be scheduled before this grid ends.
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // --------------------------------------------------------------------- TMA --
 // Order this thread's later uses of a tensor map in global memory after the
 // writes that produced it (the table a grouped launch reads is copied in just

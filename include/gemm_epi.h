@@ -178,6 +178,15 @@ typedef struct {
    * about half a second.  -1: always the interpreter.  The unfused path
    * always interprets.                                                    */
   int32_t specialize;
+  /* 0 (default): batched runs are launched with programmatic stream
+   * serialization, so a run may start while the previous kernel on its
+   * stream is finishing: its set-up (barriers, TMEM allocation) overlaps
+   * that kernel's tail, and it reads no input and writes no output before
+   * that kernel has completed and its memory is visible.  A run also lets
+   * the next launch on the stream be scheduled once it has issued its last
+   * operand copy.  Nonzero: plain launches.  Grouped runs are always plain
+   * (their problem table is copied in just before the launch).             */
+  int32_t no_pdl;
 } ge_options;
 
 /* Test hook: the producer never loads the first k-block, so the MMA warp's

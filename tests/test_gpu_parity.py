@@ -554,3 +554,44 @@ def test_epilogue_warps_follow_the_mainloop_length():
     assert warps(brs) == 8                                    # K = 2048, three epilogue tensors
     assert warps(ab, epi_warps=8) == 8
     assert warps(ab, debug_flags=B.GE_DEBUG_FORCE_INTERPRETER) == 8
+
+
+@pytest.mark.parametrize("no_pdl", [0, 1])
+def test_back_to_back_runs_read_and_write_each_others_buffers(no_pdl):
+    """Batched runs are launched with programmatic stream serialization: a
+    run's set-up may overlap the previous kernel's tail, but its reads of
+    inputs and writes of outputs wait for that kernel.  Run 1 (Aux/D of
+    my_epilogue, a few CTAs) writes D1; run 2 reads D1 as its A (read after
+    write) and stores its fp32 product over the memory run 1 read its A
+    from (write after read).  Twenty pairs in a row on one stream, then
+    both results against the oracle, with the overlap and without it."""
+    w1 = small(W.MY_EPILOGUE_128, 1, 256, 256, 136)
+    A1, B1, aux1, sc1 = W.make_inputs(w1)
+    w2 = [x for x in W.page_examples(L=1, M=256, N=136, K=256) if x.name == "identity_f32_out"][0]
+    _, B2, _, _ = W.make_inputs(w2)
+    dev = torch.device("cuda")
+    s = torch.cuda.Stream()
+    nbytes = max(A1.numel() * 2, w2.M * w2.N * 4)
+    X = torch.empty(nbytes // 2, dtype=torch.int16, device=dev)
+    A1d = X[:A1.numel()].view(torch.float16).view(A1.shape)
+    out2 = X.view(torch.float32)[:w2.M * w2.N].view(1, w2.M, w2.N)
+    B1d, C1d, B2d = B1.to(dev), aux1[0].to(dev), B2.to(dev)
+    D1 = torch.empty(1, 256, 256, dtype=torch.float16, device=dev)
+    Aux1 = torch.empty_like(D1)
+    opt = B.ge_options(no_pdl=no_pdl)
+    p1 = B.gemm_epi_plan_create(1, 256, 256, 136, _gpu.dtypes_of(w1), B.make_dag(w1.dag), opt)
+    p2 = B.gemm_epi_plan_create(1, 256, 136, 256, _gpu.dtypes_of(w2), B.make_dag(w2.dag), opt)
+    try:
+        for _ in range(20):
+            with torch.cuda.stream(s):
+                A1d.copy_(A1.to(dev))  # run 2 of the previous pair overwrote it
+            B.gemm_epi_run(p1, A1d, B1d, [C1d], sc1, [D1, Aux1], stream=s)
+            B.gemm_epi_run(p2, D1, B2d, [], [], [out2], stream=s)
+        torch.cuda.synchronize()
+        assert B.gemm_epi_last_error(None) == B.GE_OK
+        d1, aux1_out, o2 = D1.cpu(), Aux1.cpu(), out2.cpu().clone()
+    finally:
+        B.gemm_epi_plan_destroy(p1)
+        B.gemm_epi_plan_destroy(p2)
+    _gpu.compare(w1, [d1, aux1_out], _gpu.oracle_rows(w1, (A1, B1, aux1, sc1)))
+    _gpu.compare(w2, [o2], _gpu.oracle_rows(w2, (d1, B2, [], [])))
