@@ -1223,7 +1223,11 @@ int gemm_epi_grouped_run(gemm_epi_plan *pl, const void *const *A, const void *co
     for (int a = 0; a < na; ++a) ptrs.push_back(aux ? aux[g * na + a] : nullptr);
     for (int o = 0; o < no; ++o) ptrs.push_back(outs[g * no + o]);
   }
+  // the launch may overlap the previous kernel on the stream only when
+  // nothing else precedes it: no table copy and no wait on another stream
+  bool overlap = pl->opt.no_pdl == 0;
   if (pl->slot < 0 || pl->slot_ptrs[pl->slot] != ptrs) {
+    overlap = false;
     const int next = (pl->slot + 1) % kGroupSlots;
     // the staging and device table of `next` are free once the run that used
     // them last has finished
@@ -1240,14 +1244,13 @@ int gemm_epi_grouped_run(gemm_epi_plan *pl, const void *const *A, const void *co
     // a table reused from another stream: order this run after the last run
     // that read it (which follows the table's copy), so every earlier reader
     // of the table is finished when its event next completes
+    overlap = false;
     if (cudaStreamWaitEvent(s, pl->ev[pl->slot], 0) != cudaSuccess) return GE_ERR_CUDA;
   }
   KParams &kp = pl->kp;
   kp.groups = pl->d_desc + size_t(pl->slot) * n;
   for (int i = 0; i < pl->dt.n_scalar; ++i) kp.prog.scalars[i] = scalars[i];
-  // not overlapped with the previous launch: the problem table was copied
-  // in just before it
-  if (launch_gemm(pl->lay, pl->epi, kp, s, false) != cudaSuccess) return GE_ERR_CUDA;
+  if (launch_gemm(pl->lay, pl->epi, kp, s, overlap) != cudaSuccess) return GE_ERR_CUDA;
   if (cudaEventRecord(pl->ev[pl->slot], s) != cudaSuccess) return GE_ERR_CUDA;
   pl->ev_used[pl->slot] = true;
   pl->ev_stream[pl->slot] = s;

@@ -184,8 +184,9 @@ typedef struct {
    * that kernel's tail, and it reads no input and writes no output before
    * that kernel has completed and its memory is visible.  A run also lets
    * the next launch on the stream be scheduled once it has issued its last
-   * operand copy.  Nonzero: plain launches.  Grouped runs are always plain
-   * (their problem table is copied in just before the launch).             */
+   * operand copy.  Nonzero: plain launches.  A grouped run overlaps only
+   * when it reuses its problem table from a run on the same stream (no
+   * table copy and no cross-stream wait precede it).                        */
   int32_t no_pdl;
 } ge_options;
 

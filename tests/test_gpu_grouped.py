@@ -230,3 +230,27 @@ def test_grouped_eight_epilogue_warps():
     for cg, bn in [(1, 128), (2, 256), (1, 64)]:
         info = run_and_check(w, B.ge_options(epi_warps=8, cta_group=cg, tile_n=bn))
         assert (info["cta_group"], info["tile_n"]) == (cg, bn) and info["epi_variant"] >= 0
+
+
+def test_grouped_reused_table_waits_for_the_previous_kernel():
+    """A run that reuses its problem table may overlap the previous kernel on
+    the stream (programmatic dependent launch) but must read its inputs only
+    after that kernel: each run follows an in-place negation of every A
+    (stream-ordered), five times; the result matches the oracle on the
+    final inputs."""
+    w = W.GROUPED_BY_NAME["grouped_bias_relu_ragged"]
+    inputs = W.make_grouped_inputs(w)
+    G = Grouped(w, inputs)
+    s = torch.cuda.Stream(device=DEV)
+    try:
+        G.run(stream=s)  # builds the table
+        for _ in range(5):
+            with torch.cuda.stream(s):
+                for a in G.As:
+                    a.neg_()
+            G.run(stream=s)
+        gpu = G.finish()
+    finally:
+        G.close()
+    As, Bs, auxs, sc = inputs
+    compare_grouped(w, gpu, oracle_grouped(w, ([a.neg() for a in As], Bs, auxs, sc)))
