@@ -918,13 +918,16 @@ namespace {
 // model of est_cycles) or the epilogue, whichever is slower, since the two
 // overlap across consecutive tiles, plus a fixed cost per tile.  The epilogue
 // and fixed terms are fitted to measured launches of many short problems,
-// whose tiles are short: 900 clocks per 16-column chunk with 4 epilogue
-// warps (half that with 8), 4000 per tile.
+// whose tiles are short: 3000 clocks per 16-column chunk with 4 epilogue
+// warps (half that with 8), 4000 per tile.  (Measured: the grouped
+// notebook's 50 problems run in 32.2 us on 128 x 128 single-CTA tiles
+// against 37.1 on 256 x 256 pair tiles; 12 ragged problems 18.6 against
+// 20.0 on 256 x 128 pairs.)
 double grouped_tile_cycles(int64_t K, int cg, int bn, int warps) {
   const int64_t kb = (K + BK - 1) / BK;
   const double fill = double((BM + bn / cg) * BK * 2) / 48.0;
   const double main = kb * std::max(2.0 * bn, fill);
-  return std::max(main, (bn / CH) * 900.0 * 4.0 / warps) + 4000.0;
+  return std::max(main, (bn / CH) * 3000.0 * 4.0 / warps) + 4000.0;
 }
 
 // The launch deals the tiles (problems with the most k-blocks first) round
