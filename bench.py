@@ -1,7 +1,10 @@
 """Benchmark: fused GEMM + elementwise epilogue on GB300, one JSON line.
 
-    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference|vendor]
                     [--workload NAME]
+
+(--impl vendor times torch.matmul, i.e. cuBLAS, on the workload's A and B
+alone, for context: it is not one of the two arms.)
 
 A step is one pass of the whole hot path over one batch of synthetic input:
 one fused GEMM + epilogue launch (plan creation is outside the timed region).
@@ -22,7 +25,8 @@ Reported next to the device-timed value:
   unfused       the same GEMM storing fp32 accum + a separate elementwise
                 kernel (the bytes fusion saves)
   cpu_baseline  the fp64 CPU oracle on a bounded sample of rows
-  clocks        nvidia-smi samples taken during the timed region
+  clocks        clock, power and throttle-reason samples taken during the
+                timed region (NVML every 2 ms, else nvidia-smi every 50 ms)
 
 Under torchrun (N > 1) every rank runs an independent replica on its own GPU
 (the problem has no exchange step); value = all ranks' FLOPs / max time.
@@ -52,7 +56,8 @@ def parse():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=20)
-    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference", "vendor"],
+                    help="vendor: torch.matmul (cuBLAS) on A and B alone, for context")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--mnk", default=None,
                     help="M,N,K override of the workload's sizes (profiling on a smaller case)")
@@ -101,18 +106,28 @@ def roofline(flops, alg_bytes, ms, traffic):
                 **extra)
 
 
+# host-only sources: they choose a launch's configuration, which a traffic
+# record matches separately (its "plan"), but hold no device code
+HOST_ONLY_SOURCES = ("plan.cu", "jit.cu")
+
+
 def kernel_source_hash():
+    """Hash of the device code: every source under csrc/ but the host-only
+    ones."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "dense_gemm_elementwise_gb300", "csrc")
     for name in sorted(os.listdir(csrc)):
+        if name in HOST_ONLY_SOURCES:
+            continue
         with open(os.path.join(csrc, name), "rb") as f:
             h.update(name.encode() + f.read())
     return h.hexdigest()[:16]
 
 
-def ncu_traffic(workload):
+def ncu_traffic(workload, plan=None):
     """DRAM bytes per launch from the committed ncu summary, if it was taken
-    on the current kernel sources."""
+    on the current device code and, where the record names the launch
+    configuration it was taken with, on the same configuration as `plan`."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(path) as f:
@@ -122,45 +137,114 @@ def ncu_traffic(workload):
     ent = d.get(workload)
     if not ent or ent.get("kernel_hash") != kernel_source_hash():
         return None
+    want = ent.get("plan")
+    if want is not None and (plan is None or any(plan.get(k) != v for k, v in want.items())):
+        return None
     return ent.get("dram_bytes_per_launch")
 
 
 # ------------------------------------------------------------ clocks ---
 
+# NVML clock-event reason bits (nvml.h, nvmlClocksEventReason*)
+NVML_REASON_BITS = (("sw_power_cap", 0x4), ("hw_slowdown", 0x8),
+                    ("sw_thermal_slowdown", 0x20), ("hw_thermal_slowdown", 0x40))
+
+
+def nvml_sampler_main(bus, period_ms):
+    """Body of ClockSampler's child process: read-only NVML queries of the GPU
+    at PCI address `bus` every `period_ms`, one line per sample (wall time,
+    SM clock and its maximum in MHz, power in W, clock-event reason bits).
+    Exits 3 when NVML or the device cannot be opened."""
+    import ctypes
+    try:
+        lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if lib.nvmlInit_v2() != 0:
+            sys.exit(3)
+        try:
+            reasons_fn = lib.nvmlDeviceGetCurrentClocksEventReasons
+        except AttributeError:
+            reasons_fn = lib.nvmlDeviceGetCurrentClocksThrottleReasons
+    except OSError:
+        sys.exit(3)
+    h = ctypes.c_void_p()
+    if lib.nvmlDeviceGetHandleByPciBusId_v2(bus.encode(), ctypes.byref(h)) != 0:
+        sys.exit(3)
+    clk, smax, mw, bits = ctypes.c_uint(), ctypes.c_uint(), ctypes.c_uint(), ctypes.c_ulonglong()
+    sm_clock = 1  # NVML_CLOCK_SM
+    lib.nvmlDeviceGetMaxClockInfo(h, sm_clock, ctypes.byref(smax))
+    period = max(period_ms, 1) / 1000.0
+    out = sys.stdout
+    while True:
+        ok = lib.nvmlDeviceGetClockInfo(h, sm_clock, ctypes.byref(clk)) == 0
+        if lib.nvmlDeviceGetPowerUsage(h, ctypes.byref(mw)) != 0:
+            mw.value = 0
+        if reasons_fn(h, ctypes.byref(bits)) != 0:
+            bits.value = 0
+        if ok:
+            try:
+                out.write("%.6f,%d,%d,%.3f,%d\n" % (time.time(), clk.value, smax.value,
+                                                     mw.value / 1000.0, bits.value))
+                out.flush()
+            except (BrokenPipeError, OSError):
+                return
+        time.sleep(period)
+
+
 class ClockSampler:
-    """nvidia-smi samples every 50 ms, each stamped with the tool's own
-    timestamp.  The sampler starts before the inputs are made, so the tool's
-    start-up (up to a second or two) is over well before the timed region;
-    window(t0, t1) keeps the samples taken between two time.time() marks.
-    Lines are read by a thread as they come (line-buffered through stdbuf
-    where it exists), so none are lost when the tool is stopped."""
+    """Clock, power and throttle-reason samples of the GPU, each stamped with
+    the wall time it was taken at; window(t0, t1) keeps the samples between
+    two time.time() marks.  Preferred source: a child process that polls
+    NVML (read-only queries) every 2 ms, so even a timed region of ~10 ms
+    holds samples; else nvidia-smi every 50 ms.  The sampler starts before
+    the inputs are made, so its start-up is over well before the timed
+    region.  Lines are read by a thread as they come, so none are lost when
+    the child is stopped."""
     FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
     REASONS = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+    NVML_PERIOD_MS = 2
 
-    def __init__(self, gpu_index):
+    def __init__(self, gpu_index, bus=None):
         self.proc = None
         self.gpu = gpu_index
+        self.bus = bus
+        self.source = None
         self.lines = []
         self.thread = None
 
-    def start(self):
-        import shutil
+    def _spawn(self, cmd):
         import threading
-        cmd = ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.FIELDS,
-               "--format=csv,noheader,nounits", "-lms", "50"]
-        if shutil.which("stdbuf"):
-            cmd = ["stdbuf", "-oL"] + cmd
         try:
             self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
                                          text=True)
         except OSError:
             self.proc = None
-            return self
+            return False
+        self.lines = []
         self.thread = threading.Thread(target=self._read, daemon=True)
         self.thread.start()
-        atexit.register(self.stop)  # never leave the tool running
+        return True
+
+    def start(self):
+        import shutil
+        atexit.register(self.stop)  # never leave the child running
+        if self.bus and self._spawn([sys.executable, os.path.abspath(__file__), "--nvml-sampler",
+                                     self.bus, str(self.NVML_PERIOD_MS)]):
+            t_end = time.time() + 5.0
+            while not self.lines and self.proc.poll() is None and time.time() < t_end:
+                time.sleep(0.01)
+            if self.lines:
+                self.source = "nvml every %d ms" % self.NVML_PERIOD_MS
+                return self
+            self.stop()
+            self.proc = None
+        cmd = ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.FIELDS,
+               "--format=csv,noheader,nounits", "-lms", "50"]
+        if shutil.which("stdbuf"):
+            cmd = ["stdbuf", "-oL"] + cmd
+        if self._spawn(cmd):
+            self.source = "nvidia-smi every 50 ms"
         return self
 
     def _read(self):
@@ -183,6 +267,14 @@ class ClockSampler:
         out = []
         for received, line in list(self.lines):
             parts = [p.strip() for p in line.split(",")]
+            if len(parts) == 5:  # NVML child: time, sm, max, power, reason bits
+                try:
+                    t, sm, smax, pw, bits = (float(parts[0]), float(parts[1]), float(parts[2]),
+                                             float(parts[3]), int(parts[4]))
+                except ValueError:
+                    continue
+                out.append((t, sm, smax, pw, [n for n, b in NVML_REASON_BITS if bits & b]))
+                continue
             if len(parts) < 9:
                 continue
             try:
@@ -202,7 +294,8 @@ class ClockSampler:
         shorter than the sampling period may hold none: then the nearest
         samples within 0.25 s of it are used, and "window" says so."""
         if self.proc is None:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+            return {"sm_mhz": None, "sm_max_mhz": None,
+                    "reasons": ["neither NVML nor nvidia-smi available"]}
         samples = self._samples()
         inside = [x for x in samples if t0 <= x[0] <= t1]
         n_inside = len(inside)
@@ -211,12 +304,13 @@ class ClockSampler:
             inside = [x for x in samples if t0 - 0.25 <= x[0] <= t1 + 0.25]
             where = "timed region +- 0.25 s (no sample inside it)"
         if not inside:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no nvidia-smi sample"],
-                    "samples": 0, "samples_total": len(samples)}
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no clock sample"],
+                    "samples": 0, "samples_total": len(samples), "source": self.source}
         return {"sm_mhz": statistics.median(x[1] for x in inside),
                 "sm_max_mhz": max(x[2] for x in inside),
                 "reasons": sorted({r for x in inside for r in x[4]}),
                 "samples": len(inside), "samples_inside_region": n_inside, "window": where,
+                "source": self.source,
                 "window_s": round(t1 - t0, 3),
                 "power_w_median": statistics.median(x[3] for x in inside),
                 "power_w_max": max(x[3] for x in inside)}
@@ -252,17 +346,23 @@ def _numa_nodes_of(addr_lo, addr_hi):
     return nodes
 
 
+def gpu_pci_bus(local):
+    """PCI address of CUDA device `local` (domain:bus:device.function), or
+    None where torch does not report it."""
+    import torch
+    try:
+        p = torch.cuda.get_device_properties(local)
+        return "%04x:%02x:%02x.0" % (p.pci_domain_id, p.pci_bus_id, p.pci_device_id)
+    except (AttributeError, RuntimeError):
+        return None
+
+
 def host_numa_note(local, tensors=()):
     """Where the end-to-end leg's pinned host buffers sit relative to the
     GPU: the GPU's NUMA node (sysfs), the nodes of this process's CPUs, and
     the nodes holding the buffers' pages."""
-    import torch
     out = {}
-    try:
-        p = torch.cuda.get_device_properties(local)
-        bus = "%04x:%02x:%02x.0" % (p.pci_domain_id, p.pci_bus_id, p.pci_device_id)
-    except (AttributeError, RuntimeError):
-        bus = None
+    bus = gpu_pci_bus(local)
     if bus:
         try:
             with open("/sys/bus/pci/devices/%s/numa_node" % bus.lower()) as f:
@@ -400,6 +500,61 @@ def run_reference(args, w):
                              "kind": "oracle", "sample": sample},
             "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------ vendor context ---
+
+def run_vendor(args, w):
+    """Context, not an arm of the comparison: the vendor GEMM (torch.matmul,
+    i.e. cuBLAS) on the workload's A and B alone, no epilogue tensors, timed
+    under the same protocol (per-launch CUDA events on one stream, the L2
+    flushed before each launch when the inputs are smaller than twice it).
+    Rank 0 only."""
+    import torch
+
+    from dense_gemm_elementwise_gb300 import workloads as W
+    rank, world, local = dist_setup(args.gpus)
+    if rank != 0:
+        return
+    torch.cuda.set_device(local)
+    dev_ = torch.device("cuda", local)
+    stream = torch.cuda.Stream(device=dev_)
+    clocks = ClockSampler(local, gpu_pci_bus(local)).start()
+    A, Bm, _, _ = W.make_inputs(w)
+    Ad, Bd = A.to(dev_), Bm.to(dev_)
+    out = torch.empty(w.L, w.M, w.N, dtype=W.TORCH_DTYPE[w.outs[0][1]], device=dev_)
+    in_bytes = Ad.numel() * Ad.element_size() + Bd.numel() * Bd.element_size()
+    flush = in_bytes < 2 * L2_BYTES
+    if flush:
+        fbuf = torch.empty(512 << 20, dtype=torch.uint8, device=dev_)
+        cbuf = torch.ones(64 << 20, dtype=torch.float32, device=dev_)
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            torch.matmul(Ad, Bd, out=out)
+    torch.cuda.synchronize()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
+    t0 = time.time()
+    with torch.cuda.stream(stream):
+        for s_, e_ in evs:
+            if flush:
+                fbuf.zero_()
+                cbuf.sum()
+            s_.record(stream)
+            torch.matmul(Ad, Bd, out=out)
+            e_.record(stream)
+    torch.cuda.synchronize()
+    t1 = time.time()
+    clk = clocks.window(t0, t1)
+    clocks.stop()
+    ms = sum(s_.elapsed_time(e_) for s_, e_ in evs) / args.steps
+    gemm_flops = 2.0 * w.L * w.M * w.N * w.K
+    line = {"impl": "vendor", "metric": "vendor GEMM TFLOP/s (torch.matmul: A @ B only)",
+            "value": gemm_flops / (ms * 1e-3) / 1e12, "unit": "TFLOP/s", "n_gpus": 1,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+            "higher_is_better": True, "dtype": w.ab, "data": "synthetic",
+            "config": workload_config(w, 1), "l2": l2_note(flush, in_bytes), "clocks": clk}
     print(json.dumps(line), flush=True)
 
 
@@ -566,7 +721,7 @@ def config_entry(m, ms, unfused, stream=None):
     per-launch CUDA-event timing (the headline protocol) and, for workloads
     whose inputs fit in the L2, the back-to-back stream figure."""
     w = m.w
-    roof = roofline(m.flops, w.alg_bytes(), ms, ncu_traffic(w.name))
+    roof = roofline(m.flops, w.alg_bytes(), ms, ncu_traffic(w.name, m.info))
     return {"workload": w.name, "L": w.L, "M": w.M, "N": w.N, "K": w.K, "ab_dtype": w.ab,
             "outs": [n + ":" + dt for n, dt in w.outs],
             "ms_per_step": ms, "value": m.flops / (ms * 1e-3) / 1e12, "unit": "TFLOP/s",
@@ -586,7 +741,7 @@ def run_ours(args, w):
     torch.cuda.set_device(local)
     dev_ = torch.device("cuda", local)
     stream = torch.cuda.Stream(device=dev_)
-    clocks = ClockSampler(local).start()
+    clocks = ClockSampler(local, gpu_pci_bus(local)).start()
     opts = parse_opts(B, args.opt)
     m = Measured(w, dev_, stream, world, opts)
     inputs = m.inputs
@@ -606,7 +761,7 @@ def run_ours(args, w):
         raise RuntimeError("device-side timeout during the timed region")
     value = world * flops / (ms_max * 1e-3) / 1e12
 
-    roof = roofline(flops, w.alg_bytes(), ms, ncu_traffic(w.name))
+    roof = roofline(flops, w.alg_bytes(), ms, ncu_traffic(w.name, info))
 
     unfused = None
     if not args.no_unfused:
@@ -780,7 +935,7 @@ def run_grouped(args, w):
     torch.cuda.set_device(local)
     dev_ = torch.device("cuda", local)
     stream = torch.cuda.Stream(device=dev_)
-    clocks = ClockSampler(local).start()
+    clocks = ClockSampler(local, gpu_pci_bus(local)).start()
     inputs = W.make_grouped_inputs(w)
     As, Bs, auxs, scalars = inputs
     Ad = [a.to(dev_) for a in As]
@@ -952,6 +1107,8 @@ def main():
         w = dataclasses.replace(w, M=m, N=n, K=k, name="%s@%dx%dx%d" % (w.name, m, n, k))
     if args.impl == "reference":
         run_reference(args, w)
+    elif args.impl == "vendor":
+        run_vendor(args, w)
     else:
         from dense_gemm_elementwise_gb300 import build as gbuild
         gbuild.build()
@@ -959,4 +1116,7 @@ def main():
 
 
 if __name__ == "__main__":
-    main()
+    if len(sys.argv) == 4 and sys.argv[1] == "--nvml-sampler":
+        nvml_sampler_main(sys.argv[2], int(sys.argv[3]))
+    else:
+        main()

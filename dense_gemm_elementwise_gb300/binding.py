@@ -76,7 +76,7 @@ class ge_plan_info(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in
                 ("cta_group", "tile_m", "tile_n", "tile_k", "stages", "epi_chunk", "aux_stages",
                  "grid", "num_tiles", "smem_bytes", "n_instr", "n_regs", "num_sms",
-                 "epi_variant", "cluster_n", "epi_warps")]
+                 "epi_variant", "cluster_n", "epi_warps", "raster_group")]
 
 
 class GemmEpiError(RuntimeError):

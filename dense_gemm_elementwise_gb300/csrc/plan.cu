@@ -815,6 +815,7 @@ int gemm_epi_plan_info(const gemm_epi_plan *pl, ge_plan_info *info) {
   info->epi_variant = pl->epi;
   info->cluster_n = 1;
   info->epi_warps = pl->lay.warps;
+  info->raster_group = pl->lay.raster_group;
   return GE_OK;
 }
 

@@ -1,5 +1,5 @@
-"""Host-side logic of the benchmark that needs no GPU: which nvidia-smi
-samples count as "during the timed region"."""
+"""Host-side logic of the benchmark that needs no GPU: which clock samples
+count as "during the timed region"."""
 import datetime
 import importlib.util
 import os
@@ -72,6 +72,70 @@ def test_unparseable_timestamp_falls_back_to_arrival_time():
                           "Not Active, Not Active\n")]
     w = s.window(t0, t0 + 0.2)
     assert w["samples"] == 1 and w["sm_mhz"] == 1800 and w["reasons"] == []
+
+
+def test_nvml_lines_decode_reason_bits():
+    """Samples from the NVML child: wall time, SM clock, max, power, reason
+    bits (sw_power_cap 0x4, hw_slowdown 0x8, sw_thermal 0x20, hw_thermal
+    0x40, from nvml.h); other bits (idle 0x1) are not reasons to report."""
+    bench = load_bench()
+    s = bench.ClockSampler(0)
+    s.proc = _Done()
+    s.source = "nvml every 2 ms"
+    t0 = 1_800_000_000.0
+    s.lines = [(t0 + 0.5, "%.6f,1800,2070,900.500,4\n" % (t0 + 0.002)),
+               (t0 + 0.5, "%.6f,1700,2070,1200.000,5\n" % (t0 + 0.004)),
+               (t0 + 0.5, "%.6f,1600,2070,1300.000,72\n" % (t0 + 0.006)),  # 0x48
+               (t0 + 0.5, "%.6f,2070,2070,100.000,1\n" % (t0 + 1.0))]
+    w = s.window(t0, t0 + 0.01)
+    assert w["samples"] == 3 and w["samples_inside_region"] == 3
+    assert w["sm_mhz"] == 1700 and w["power_w_max"] == 1300.0
+    assert w["reasons"] == ["hw_slowdown", "hw_thermal_slowdown", "sw_power_cap"]
+    assert w["source"] == "nvml every 2 ms"
+    w = s.window(t0 + 0.9, t0 + 1.1)
+    assert w["reasons"] == []
+
+
+def test_sampler_falls_back_when_nvml_cannot_start(monkeypatch):
+    """A child that exits without a sample (no NVML, unknown device) leaves
+    the sampler on nvidia-smi, or on nothing, never hanging."""
+    bench = load_bench()
+    s = bench.ClockSampler(0, "ffff:ff:1f.0")
+    s.start()
+    try:
+        assert s.source in (None, "nvidia-smi every 50 ms")
+    finally:
+        s.stop()
+
+
+def test_traffic_record_needs_the_same_device_code_and_plan(monkeypatch, tmp_path):
+    """A committed ncu traffic figure is reported only for the device code
+    and launch configuration it was captured on."""
+    import json
+    bench = load_bench()
+    (tmp_path / "profiles").mkdir()
+    rec = {"w": {"kernel_hash": "h1", "dram_bytes_per_launch": 123,
+                 "plan": {"cta_group": 2, "tile_n": 256, "raster_group": 16}},
+           "old": {"kernel_hash": "h1", "dram_bytes_per_launch": 7}}
+    (tmp_path / "profiles" / "traffic.json").write_text(json.dumps(rec))
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    monkeypatch.setattr(bench, "kernel_source_hash", lambda: "h1")
+    plan = {"cta_group": 2, "tile_n": 256, "raster_group": 16, "stages": 5}
+    assert bench.ncu_traffic("w", plan) == 123
+    assert bench.ncu_traffic("w", dict(plan, tile_n=128)) is None
+    assert bench.ncu_traffic("w", dict(plan, raster_group=8)) is None
+    assert bench.ncu_traffic("w", None) is None
+    assert bench.ncu_traffic("old", plan) == 7  # a record without a plan: code only
+    assert bench.ncu_traffic("missing", plan) is None
+    monkeypatch.setattr(bench, "kernel_source_hash", lambda: "h2")
+    assert bench.ncu_traffic("w", plan) is None
+
+
+def test_device_code_hash_ignores_host_only_sources():
+    bench = load_bench()
+    csrc = os.path.join(ROOT, "dense_gemm_elementwise_gb300", "csrc")
+    assert set(bench.HOST_ONLY_SOURCES) <= set(os.listdir(csrc))
+    assert len(bench.kernel_source_hash()) == 16
 
 
 def test_roofline_takes_the_binding_bound(monkeypatch):
