@@ -1165,6 +1165,8 @@ def main():
         w = W.GROUPED_BY_NAME[args.workload]
         if args.impl == "reference":
             run_grouped_reference(args, w)
+        elif args.impl == "vendor":
+            raise SystemExit("--impl vendor times batched workloads only")
         else:
             from dense_gemm_elementwise_gb300 import build as gbuild
             gbuild.build()
