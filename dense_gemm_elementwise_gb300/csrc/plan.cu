@@ -511,11 +511,14 @@ int configure(gemm_epi_plan *pl) {
     const int64_t tiles = pl->L * Lo->num_m_blk * int64_t(Lo->num_n_blk);
     if (tiles > (int64_t(1) << 30)) return GE_ERR_SHAPE;
     Lo->num_tiles = static_cast<int>(tiles);
-    // 12 M tiles per raster group: at 8192^3 as fast as 16 (647.6 against
-    // 648.1 us over 20 launches, 702.7 against 703.6 over 200, four
-    // interleaved repetitions each) and 8 (652.1, 708.9), with 6.5 % fewer
-    // DRAM reads than 16 (1.19 against 1.27 GB per launch)
-    Lo->raster_group = o.raster_group ? o.raster_group : 12;
+    // Raster groups: all M tiles in one group when there are at most 16,
+    // else 12 M tiles per group.  At 8192^3 (32 M tiles) 12 is as fast as 16
+    // (647.6 against 648.1 us over 20 launches, 702.7 against 703.6 over
+    // 200, four interleaved repetitions each) and 8 (652.1, 708.9) and reads
+    // 6.5 % less from DRAM than 16 (1.19 against 1.27 GB per launch); with 16
+    // M tiles per batch (L=8, 4096 x 4096 x 2048) one group of 16 reads 6 %
+    // less than 12 + 4 (0.62 against 0.66 GB) and runs 0.3 % faster.
+    Lo->raster_group = o.raster_group ? o.raster_group : (Lo->num_m_blk <= 16 ? 16 : 12);
     int sms = pl->num_sms;
     if (o.max_ctas) sms = std::min(sms, o.max_ctas);
     int units = std::max(1, sms / cg);
