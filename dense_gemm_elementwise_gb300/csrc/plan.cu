@@ -820,7 +820,10 @@ int gemm_epi_plan_info(const gemm_epi_plan *pl, ge_plan_info *info) {
   info->epi_variant = pl->epi;
   info->cluster_n = 1;
   info->epi_warps = pl->lay.warps;
-  info->raster_group = pl->lay.raster_group;
+  // the group size in effect: a batched launch with fewer M tiles than the
+  // group size runs them all as one group
+  info->raster_group = pl->n_groups ? pl->lay.raster_group
+                                    : std::min(pl->lay.raster_group, pl->lay.num_m_blk);
   return GE_OK;
 }
 

@@ -219,7 +219,8 @@ typedef struct {
                                                  this program when the plan was made        */
   int32_t cluster_n;                          /* always 1: no operand sharing between pairs */
   int32_t epi_warps;                          /* epilogue warps per CTA (4 or 8)         */
-  int32_t raster_group;                       /* M tiles per raster group                */
+  int32_t raster_group;                       /* M tiles per raster group (batched: the
+                                                 group in effect, at most the M tiles)    */
 } ge_plan_info;
 
 typedef struct gemm_epi_plan gemm_epi_plan;
