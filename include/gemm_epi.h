@@ -141,7 +141,8 @@ typedef struct {
   int32_t tile_n;       /* 0 auto, else the MMA N: 64, 128 or 256                       */
   int32_t stages;       /* 0 auto (as many as fit), else 2..8 shared-memory stages      */
   int32_t max_ctas;     /* 0 = one CTA per SM, else a cap on the persistent grid        */
-  int32_t raster_group; /* 0 auto, else M tiles per raster group (L2 reuse of B)        */
+  int32_t raster_group; /* 0 auto, else M tiles per raster group (L2 reuse of B); auto:
+                           all M tiles when there are at most 16, else 12 (grouped: 8) */
   int32_t timeout_ms;   /* 0 = 1000; bound on every device-side wait                    */
   uint32_t debug_flags; /* 0; GE_DEBUG_* below, for tests only                          */
   int32_t cluster_n;    /* 0 or 1 (one CTA, or one CTA pair, per cluster); any other
