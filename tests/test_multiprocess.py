@@ -53,8 +53,8 @@ def test_max_over_ranks_two_gloo_ranks():
 
 
 def test_reference_arm_under_torchrun():
-    """bench.py --impl reference launched as the driver launches N = 2: one
-    JSON line, from rank 0, the other rank exits 0 without work."""
+    """bench.py --impl reference launched under torchrun with N = 2 ranks:
+    one JSON line, from rank 0, the other rank exits 0 without work."""
     port = free_port()
     cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node", "2",
            "--master-addr", "127.0.0.1", "--master-port", str(port), "bench.py",
