@@ -110,6 +110,29 @@ def test_more_stages_than_default(stages):
     _gpu.compare(w, gpu, _gpu.oracle_rows(w, inputs))
 
 
+@pytest.mark.parametrize("variant", [(1, 128), (2, 256)], ids=lambda v: "cg%d_n%d" % v)
+def test_many_batches(variant):
+    """L = 200 small problems in one batched launch: the batch coordinate of
+    every TMA box and the (l, m, n) order of the persistent schedule,
+    bit-exact against the oracle."""
+    w = small(W.MY_EPILOGUE_128, 200, 136, 264, 72)
+    inputs = W.make_inputs(w)
+    gpu, info = _gpu.run_gpu(w, inputs, options=opts(variant))
+    assert info["num_tiles"] >= 200
+    _gpu.compare(w, gpu, _gpu.oracle_rows(w, inputs))
+
+
+def test_wide_and_tall_extents():
+    """One very wide (N = 65,544) and one very tall (M = 65,537) problem:
+    column and row coordinates far past any tile count, ragged at the far
+    edge, bit-exact against the oracle."""
+    for (M, N, K) in ((130, 65544, 40), (65537, 136, 24)):
+        w = small(W.MY_EPILOGUE_128, 1, M, N, K)
+        inputs = W.make_inputs(w)
+        gpu, _ = _gpu.run_gpu(w, inputs)
+        _gpu.compare(w, gpu, _gpu.oracle_rows(w, inputs))
+
+
 def test_small_grid_many_tiles_per_cta():
     """Four CTAs loop over many tiles: both TMEM accumulators, the aux
     prefetch across tile boundaries and the raster order all wrap."""
