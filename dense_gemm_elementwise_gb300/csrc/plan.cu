@@ -425,44 +425,21 @@ double est_cycles(const gemm_epi_plan *pl, int cg, int bn, int units) {
   return waves * per_tile + (bn / CH) * 300.0;
 }
 
-// SM cycles one epilogue warp spends on one 32-column step (accumulator
-// loads, staged aux boxes, the program, staging stores), fitted to traces of
-// the built-in epilogues with 8 warps: ~2700 with one aux tensor and one
-// output, ~4300 with one aux, a row vector and two outputs, ~4600 with two
-// aux tensors and two outputs; transcendental activations add their own
-// evaluation.
-double est_step_cycles(const EpiProgram &P) {
-  int act = 0;
-  for (int i = 0; i < P.n_ins; ++i) {
-    const uint32_t op = P.ins[i] & 0xffu;
-    act += op >= OP_SIGMOID && op <= OP_HARDSWISH;
-  }
-  return 1600.0 + 750.0 * (P.n_tma_aux + P.n_out) + 600.0 * (P.n_bcast + P.n_cbcast) + 1500.0 * act;
-}
-
 // Epilogue warps: the option, else 8 — two warps per lane quarter overlap
 // each other's waits: with built-in epilogues measured equal or faster on
-// every workload (up to 1.5x where the epilogue outweighs a short
-// mainloop); with the interpreter, which then spills a few registers, 1.13x
-// to 1.27x faster on transcendental and multi-output epilogues and 4 %
-// slower on a cheap one.  Except: a compiled epilogue (built-in or compiled
-// at plan time) takes 4 warps when 4 warps' epilogue of a tile needs at most
-// half of the tile's mainloop, i.e. stays hidden with room to spare.  There
-// the epilogue's shared-memory traffic comes in fewer, longer-spaced bursts:
-// at 8192^3 with the Alpha-Beta epilogue 1% more TFLOP/s under the power cap
-// (500-step runs, three interleaved repetitions), ~4% more per SM clock.
-// `mainloop_cycles`: one tile's k-blocks at the cost model's rate (0: no
-// estimate, as for grouped launches).
-int pick_epi_warps(const gemm_epi_plan *pl, int *warps, int bn = 0, double mainloop_cycles = 0) {
+// every workload (up to 1.5x where the epilogue outweighs a short mainloop;
+// at 8192^3, where the epilogue hides under a 128-k-block mainloop, 620.5-
+// 620.6 against 622.9-626.6 us over 20 launches and 683-691 against 691-696
+// over 300, four interleaved repetitions each); with the interpreter, which
+// then spills a few registers, 1.13x to 1.27x faster on transcendental and
+// multi-output epilogues and 4 % slower on a cheap one.  The interpreter of
+// programs with more than four live values holds twice the registers and
+// runs on 4.
+int pick_epi_warps(const gemm_epi_plan *pl, int *warps) {
   const int w = pl->opt.epi_warps;
   if (w != 0 && w != 4 && w != 8) return GE_ERR_INVALID;
-  // the 8-register interpreter holds twice the program registers: 4 warps
   if (w == 8 && pl->epi == -2) return GE_ERR_UNSUPPORTED;
   *warps = w ? w : (pl->epi == -2 ? 4 : 8);
-  if (w == 0 && (pl->epi >= 0 || pl->epi == kEpiSpecialized) && mainloop_cycles > 0) {
-    const double epi4 = (bn / EW) * est_step_cycles(pl->prog);  // 4 warps: every step of the tile
-    if (epi4 <= 0.5 * mainloop_cycles) *warps = 4;
-  }
   return GE_OK;
 }
 
@@ -494,8 +471,7 @@ int configure(gemm_epi_plan *pl) {
   const int cg = cand[best][0], bn = cand[best][1];
 
   int warps = 0;
-  const int64_t kb = (pl->K + BK - 1) / BK;
-  int st = pick_epi_warps(pl, &warps, bn, double(kb) * est_kblock_cycles(cg, bn));
+  int st = pick_epi_warps(pl, &warps);
   if (st != GE_OK) return st;
   st = make_layout(&pl->lay, cg, bn, o.stages, pl->prog, pl->max_smem, 4, 5, warps);
   if (st != GE_OK) return st;

@@ -164,10 +164,8 @@ typedef struct {
   int32_t cd_major;
   /* 0 auto, else the epilogue warps per CTA: 4 (one per accumulator lane
    * quarter) or 8 (two per quarter, each taking every other 32-column
-   * step).  Auto is 8, except 4 for a built-in or plan-time compiled
-   * epilogue whose estimated 4-warp epilogue of a tile needs at most half of
-   * the tile's mainloop (long K), and 4 for the interpreter of programs
-   * with more than four live values.  Results are identical either way;
+   * step).  Auto is 8, except 4 for the interpreter of programs with more
+   * than four live values.  Results are identical either way;
    * GE_ERR_INVALID otherwise.                                              */
   int32_t epi_warps;
   /* 0 (default): an epilogue outside the built-in set gets a fused kernel

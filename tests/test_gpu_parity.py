@@ -561,9 +561,9 @@ def test_run_captured_in_cuda_graph():
         B.gemm_epi_plan_destroy(plan)
 
 
-def test_epilogue_warps_follow_the_mainloop_length():
-    """Compiled epilogues take 4 warps when 4 warps' epilogue of a tile fits
-    in half of its mainloop (long K), else 8; the option overrides."""
+def test_epilogue_warps_default_and_option():
+    """Compiled epilogues and the 4-register interpreter take 8 warps at any
+    K; the option overrides."""
     def warps(w, **opt):
         plan = B.gemm_epi_plan_create(w.L, w.M, w.N, w.K, _gpu.dtypes_of(w), B.make_dag(w.dag),
                                       B.ge_options(**opt) if opt else None)
@@ -572,10 +572,10 @@ def test_epilogue_warps_follow_the_mainloop_length():
         finally:
             B.gemm_epi_plan_destroy(plan)
     ab, brs = W.ALPHA_BETA_X_8192, W.BIAS_RELU_SQUARE_L8
-    assert warps(ab) == 4                                     # K = 8192: 128 k-blocks a tile
+    assert warps(ab) == 8                                     # K = 8192: 128 k-blocks a tile
     assert warps(dataclasses.replace(ab, K=1024)) == 8        # 16 k-blocks a tile
     assert warps(brs) == 8                                    # K = 2048, three epilogue tensors
-    assert warps(ab, epi_warps=8) == 8
+    assert warps(ab, epi_warps=4) == 4
     assert warps(ab, debug_flags=B.GE_DEBUG_FORCE_INTERPRETER) == 8
 
 

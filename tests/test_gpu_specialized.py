@@ -79,12 +79,12 @@ def test_plan_time_compilation_is_cached():
 
 
 def test_specialized_four_warps_at_long_k():
-    """A long-K problem puts a compiled epilogue on 4 warps: the compiled
+    """A compiled epilogue on 4 warps (the option) at long K: the compiled
     kernel is then the 4-warp instance, still bit-identical to the
     interpreter and exact against the oracle."""
     w = dataclasses.replace(EXAMPLES["relu_aux_store"], L=1, M=256, N=264, K=8192)
     inputs = W.make_inputs(w)
-    spec, info = _gpu.run_gpu(w, inputs)
+    spec, info = _gpu.run_gpu(w, inputs, options=B.ge_options(epi_warps=4))
     assert info["epi_variant"] == -3 and info["epi_warps"] == 4, info
     interp, info2 = _gpu.run_gpu(w, inputs, options=B.ge_options(specialize=-1))
     assert info2["epi_variant"] in (-1, -2)
